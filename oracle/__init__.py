@@ -1,0 +1,326 @@
+"""fp64 CPU oracle for FlashPrefill V2 block-sparse prefill attention with mean correction.
+
+TEST INFRASTRUCTURE ONLY: the test-suite, the smoke check and the benchmark's
+CPU-baseline leg are its only users. The product library never imports it.
+
+The arithmetic lives in ``fp_oracle.c`` (plain C, fp64, POSIX threads). This
+wrapper marshals numpy arrays to it, and does host-side bookkeeping only:
+segment enumeration (request b, KV head h, tile t), CSR assembly from the
+oracle's own selection, and scattering tile rows back to [T, Hq, d] through
+the PackGQA row map (pos(r) = floor(r/g), head(r) = h g + r mod g; FlashPrefill
+V2 Sec.3.3 Eq.13).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import dataclasses
+from typing import Optional, Sequence
+
+import numpy as np
+
+from .build import build as _build_lib, LIB_PATH
+
+ORC_CORRECTION = 1
+ORC_DENSE = 2
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("hq", ctypes.c_int32), ("hkv", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("block", ctypes.c_int32), ("page_size", ctypes.c_int32), ("tile_rows", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("c_q", ctypes.c_double), ("c_k", ctypes.c_double), ("c_v", ctypes.c_double),
+        ("cu_seqlens", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
+        ("pt_stride", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+        ("q", ctypes.c_void_p), ("k_pages", ctypes.c_void_p), ("v_pages", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            _build_lib()
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER(_Problem)
+        vp = ctypes.c_void_p
+        L.orc_decode_bf16.restype = ctypes.c_double
+        L.orc_decode_bf16.argtypes = [ctypes.c_uint16]
+        L.orc_decode_e4m3.restype = ctypes.c_double
+        L.orc_decode_e4m3.argtypes = [ctypes.c_uint8]
+        L.orc_validate.argtypes = [P]
+        L.orc_pool.argtypes = [P, ctypes.c_int, ctypes.c_int, vp, vp, vp]
+        L.orc_pool_all.argtypes = [P, vp, vp, vp, vp]
+        L.orc_energies.argtypes = [P, vp, ctypes.c_long, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp]
+        L.orc_select.argtypes = [vp, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int, vp, vp]
+        L.orc_attend_tile.argtypes = [P, vp, vp, ctypes.c_long, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp,
+                                      ctypes.c_int, vp, vp]
+        L.orc_run_segments.argtypes = [P, vp, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                       ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int, vp, vp, vp,
+                                       ctypes.c_int, ctypes.c_int, vp, vp, vp, ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _raw(x) -> np.ndarray:
+    """Element bytes of a bf16 / float8_e4m3fn torch tensor (or an already-raw numpy array)."""
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x)
+    import torch
+    x = x.detach().to("cpu").contiguous()
+    if x.dtype == torch.bfloat16:
+        return x.view(torch.int16).numpy().view(np.uint16)
+    if x.dtype == torch.float8_e4m3fn:
+        return x.view(torch.uint8).numpy()
+    raise TypeError(f"unsupported element type {x.dtype}")
+
+
+@dataclasses.dataclass
+class Problem:
+    """Host copy of one attention layer's inputs, as raw element bytes."""
+    q: np.ndarray            # [T, hq, d] uint16 (bf16 bits) or uint8 (e4m3 bits)
+    k_pages: np.ndarray      # [num_pages, page, hkv, d]
+    v_pages: np.ndarray
+    cu_seqlens: np.ndarray   # [batch+1] int32
+    page_table: np.ndarray   # [batch, stride] int32
+    hq: int
+    hkv: int
+    dtype: str = "bf16"
+    c_q: float = 1.0
+    c_k: float = 1.0
+    c_v: float = 1.0
+    block: int = 128
+    tile_rows: int = 128
+
+    @classmethod
+    def from_workload(cls, w, tile_rows: int = 128) -> "Problem":
+        return cls(q=_raw(w.q), k_pages=_raw(w.k_pages), v_pages=_raw(w.v_pages),
+                   cu_seqlens=np.asarray(w.host_cu_seqlens, dtype=np.int32),
+                   page_table=np.ascontiguousarray(w.page_table.to("cpu").numpy().astype(np.int32)),
+                   hq=w.hq, hkv=w.hkv, dtype=w.dtype, c_q=w.c_q, c_k=w.c_k, c_v=w.c_v, tile_rows=tile_rows)
+
+    def __post_init__(self):
+        self.q = np.ascontiguousarray(self.q)
+        self.k_pages = np.ascontiguousarray(self.k_pages)
+        self.v_pages = np.ascontiguousarray(self.v_pages)
+        self.cu_seqlens = np.ascontiguousarray(self.cu_seqlens, dtype=np.int32)
+        self.page_table = np.ascontiguousarray(self.page_table, dtype=np.int32)
+        if self.page_table.ndim == 1:
+            self.page_table = self.page_table[None, :]
+
+    @property
+    def d(self) -> int:
+        return int(self.q.shape[-1])
+
+    @property
+    def page_size(self) -> int:
+        return int(self.k_pages.shape[1])
+
+    @property
+    def batch(self) -> int:
+        return len(self.cu_seqlens) - 1
+
+    @property
+    def g(self) -> int:
+        return self.hq // self.hkv
+
+    def lengths(self):
+        return np.diff(self.cu_seqlens).astype(np.int64)
+
+    def c_struct(self) -> _Problem:
+        s = _Problem()
+        s.batch, s.hq, s.hkv, s.d = self.batch, self.hq, self.hkv, self.d
+        s.block, s.page_size, s.tile_rows = self.block, self.page_size, self.tile_rows
+        s.dtype = 0 if self.dtype == "bf16" else 1
+        s.c_q, s.c_k, s.c_v = self.c_q, self.c_k, self.c_v
+        s.cu_seqlens = self.cu_seqlens.ctypes.data
+        s.page_table = self.page_table.ctypes.data
+        s.pt_stride = self.page_table.shape[1]
+        s.num_pages = self.k_pages.shape[0]
+        s.q = self.q.ctypes.data
+        s.k_pages = self.k_pages.ctypes.data
+        s.v_pages = self.v_pages.ctypes.data
+        return s
+
+
+@dataclasses.dataclass
+class Segments:
+    """Segment enumeration in (request, KV head, tile) order."""
+    b: np.ndarray
+    h: np.ndarray
+    t: np.ndarray
+    D: np.ndarray            # diagonal block of each tile
+    full_off: np.ndarray     # offset of each segment's D+1 per-block entries
+    full_total: int
+    blk_base: np.ndarray     # first pooled row of each request
+    total_blocks: int
+
+    def __len__(self):
+        return len(self.b)
+
+
+def segments(p: Problem) -> Segments:
+    L = p.lengths()
+    nb = (L + p.block - 1) // p.block
+    ntiles = (p.g * L + p.tile_rows - 1) // p.tile_rows
+    bs, hs, ts = [], [], []
+    for b in range(p.batch):
+        for h in range(p.hkv):
+            bs.append(np.full(ntiles[b], b))
+            hs.append(np.full(ntiles[b], h))
+            ts.append(np.arange(ntiles[b]))
+    cat = lambda xs: np.concatenate(xs).astype(np.int32) if xs else np.zeros(0, np.int32)
+    b, h, t = cat(bs), cat(hs), cat(ts)
+    D = ((t.astype(np.int64) * p.tile_rows) // p.g) // p.block
+    full_off = np.concatenate([[0], np.cumsum(D + 1)]).astype(np.int64)
+    blk_base = np.concatenate([[0], np.cumsum(nb)]).astype(np.int64)
+    return Segments(b=b, h=h, t=t, D=D.astype(np.int64), full_off=full_off[:-1].copy(), full_total=int(full_off[-1]),
+                    blk_base=blk_base[:-1].copy(), total_blocks=int(blk_base[-1]))
+
+
+@dataclasses.dataclass
+class Pooled:
+    kbar: np.ndarray   # [total_blocks, hkv, d] fp64
+    vbar: np.ndarray
+    cnt: np.ndarray    # [total_blocks] int32
+
+
+def pool(p: Problem, seg: Optional[Segments] = None) -> Pooled:
+    """Block means of every (request, KV head) (Eq.5)."""
+    seg = seg or segments(p)
+    nb = max(seg.total_blocks, 1)
+    kbar = np.zeros((nb, p.hkv, p.d))
+    vbar = np.zeros((nb, p.hkv, p.d))
+    cnt = np.zeros(nb, dtype=np.int32)
+    s = p.c_struct()
+    rc = lib().orc_pool_all(ctypes.byref(s), _ptr(seg.blk_base), _ptr(kbar), _ptr(vbar), _ptr(cnt))
+    if rc:
+        raise RuntimeError(f"oracle pool failed: {rc}")
+    return Pooled(kbar, vbar, cnt)
+
+
+def _threads(n: Optional[int]) -> int:
+    return int(n) if n else max(1, os.cpu_count() or 1)
+
+
+@dataclasses.dataclass
+class Selection:
+    sel_full: np.ndarray     # uint8 per (segment, J<=D)
+    near_full: np.ndarray
+    energy_full: Optional[np.ndarray]
+
+    def selected(self, seg: Segments, s: int) -> np.ndarray:
+        o = seg.full_off[s]
+        return np.nonzero(self.sel_full[o:o + seg.D[s] + 1])[0].astype(np.int32)
+
+    def near(self, seg: Segments, s: int) -> np.ndarray:
+        o = seg.full_off[s]
+        return np.nonzero(self.near_full[o:o + seg.D[s] + 1])[0].astype(np.int32)
+
+
+def select(p: Problem, alpha: float, sink: int, window: int, seg: Optional[Segments] = None,
+           pooled: Optional[Pooled] = None, seg_ids: Optional[Sequence[int]] = None, energies: bool = False,
+           nthreads: Optional[int] = None) -> Selection:
+    """Scoring (Eq.19) + thresholding with forced blocks (Eq.20) for the listed segments (all by default)."""
+    seg = seg or segments(p)
+    pooled = pooled or pool(p, seg)
+    ids = np.arange(len(seg), dtype=np.int64) if seg_ids is None else np.asarray(seg_ids, dtype=np.int64)
+    sel = np.zeros(max(seg.full_total, 1), np.uint8)
+    near = np.zeros(max(seg.full_total, 1), np.uint8)
+    en = np.zeros(max(seg.full_total, 1)) if energies else None
+    s = p.c_struct()
+    rc = lib().orc_run_segments(ctypes.byref(s), _ptr(ids), len(ids), _ptr(seg.b), _ptr(seg.h), _ptr(seg.t),
+                                _ptr(seg.blk_base), _ptr(pooled.kbar), _ptr(pooled.vbar), _ptr(pooled.cnt),
+                                _ptr(seg.full_off), 1, float(alpha), int(sink), int(window), _ptr(sel), _ptr(near),
+                                _ptr(en), 0, 0, None, None, None, _threads(nthreads))
+    if rc:
+        raise RuntimeError(f"oracle select failed: {rc}")
+    return Selection(sel, near, en)
+
+
+def csr_from_selection(seg: Segments, selection: Selection):
+    """CSR (cu, idx) over all segments in order; idx ascending block ids (Sec.3.3 Eq.17)."""
+    counts = np.zeros(len(seg), dtype=np.int64)
+    parts = []
+    for s in range(len(seg)):
+        ids = selection.selected(seg, s)
+        counts[s] = len(ids)
+        parts.append(ids)
+    cu = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    idx = np.concatenate(parts).astype(np.int32) if parts else np.zeros(0, np.int32)
+    return cu, idx
+
+
+def selection_from_csr(seg: Segments, cu: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """Per-(segment, J<=D) selection bytes from a CSR produced elsewhere."""
+    full = np.zeros(max(seg.full_total, 1), np.uint8)
+    for s in range(len(seg)):
+        ids = idx[cu[s]:cu[s + 1]]
+        if len(ids) and (ids.min() < 0 or ids.max() > seg.D[s]):
+            raise ValueError(f"segment {s}: block id outside [0, D]")
+        full[seg.full_off[s] + ids.astype(np.int64)] = 1
+    return full
+
+
+def attend(p: Problem, sel_full: np.ndarray, correction: bool = True, dense: bool = False,
+           seg: Optional[Segments] = None, pooled: Optional[Pooled] = None, seg_ids: Optional[Sequence[int]] = None,
+           nthreads: Optional[int] = None):
+    """Mean-corrected block-sparse attention (Eq.6; Eq.4 without correction) of the listed segments.
+
+    Returns (O [n, tile_rows, d], lse [n, tile_rows]) for the n listed segments."""
+    seg = seg or segments(p)
+    pooled = pooled or pool(p, seg)
+    ids = np.arange(len(seg), dtype=np.int64) if seg_ids is None else np.asarray(seg_ids, dtype=np.int64)
+    O = np.zeros((len(ids), p.tile_rows, p.d))
+    lse = np.zeros((len(ids), p.tile_rows))
+    flags = (ORC_CORRECTION if correction else 0) | (ORC_DENSE if dense else 0)
+    s = p.c_struct()
+    sel_full = np.ascontiguousarray(sel_full, dtype=np.uint8)
+    rc = lib().orc_run_segments(ctypes.byref(s), _ptr(ids), len(ids), _ptr(seg.b), _ptr(seg.h), _ptr(seg.t),
+                                _ptr(seg.blk_base), _ptr(pooled.kbar), _ptr(pooled.vbar), _ptr(pooled.cnt),
+                                _ptr(seg.full_off), 0, 0.0, 0, 0, None, None, None, 1, flags, _ptr(sel_full),
+                                _ptr(O), _ptr(lse), _threads(nthreads))
+    if rc:
+        raise RuntimeError(f"oracle attention failed: {rc}")
+    return O, lse
+
+
+def tile_rows_to_tokens(p: Problem, seg: Segments, seg_ids: Sequence[int], O_tiles: np.ndarray,
+                        lse_tiles: np.ndarray):
+    """Scatter tile rows to O [T, hq, d] and LSE [T, hq] (NaN where a row was not computed)."""
+    T = int(p.cu_seqlens[-1])
+    O = np.full((T, p.hq, p.d), np.nan)
+    lse = np.full((T, p.hq), np.nan)
+    L = p.lengths()
+    for i, s in enumerate(seg_ids):
+        b, h, t = int(seg.b[s]), int(seg.h[s]), int(seg.t[s])
+        r0 = t * p.tile_rows
+        r1 = min(r0 + p.tile_rows, p.g * int(L[b]))
+        r = np.arange(r0, r1)
+        pos = p.cu_seqlens[b] + r // p.g
+        head = h * p.g + r % p.g
+        O[pos, head] = O_tiles[i, :r1 - r0]
+        lse[pos, head] = lse_tiles[i, :r1 - r0]
+    return O, lse
+
+
+def run(p: Problem, alpha: float, sink: int, window: int, correction: bool = True, dense: bool = False,
+        nthreads: Optional[int] = None):
+    """The whole layer: returns dict(cu, idx, sel, O [T,hq,d], lse [T,hq], pooled, seg)."""
+    seg = segments(p)
+    pooled = pool(p, seg)
+    selection = select(p, alpha, sink, window, seg=seg, pooled=pooled, nthreads=nthreads)
+    cu, idx = csr_from_selection(seg, selection)
+    ids = np.arange(len(seg))
+    Ot, lt = attend(p, selection.sel_full, correction=correction, dense=dense, seg=seg, pooled=pooled,
+                    nthreads=nthreads)
+    O, lse = tile_rows_to_tokens(p, seg, ids, Ot, lt)
+    return dict(cu=cu, idx=idx, selection=selection, O=O, lse=lse, pooled=pooled, seg=seg)
