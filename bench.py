@@ -1,0 +1,397 @@
+#!/usr/bin/env python3
+"""Benchmark of one FlashPrefill V2 attention layer (Stage 1 + Stage 2) on GB300.
+
+A step is one pass of the whole hot path over one layer: fp_select (pooling,
+scoring, thresholding, CSR) followed by fp_attention (exact blocks + mean
+correction + epilogue), both through the C ABI, inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0). `value` is milliseconds per layer for the whole
+job (N GPUs each run one layer per step, so value = step time / N); lower is
+better. `--impl reference` times the fp64 CPU oracle on the host cores instead
+(a bounded sample of the same workload, extrapolated to a layer).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_sparse_long_mean_gb300 import synth  # noqa: E402
+
+METRIC = "sparse prefill-attn ms/layer & dense-equiv TFLOP/s at 128K; tensor-pipe %"
+UNIT = "ms/layer"
+DEFAULT_WORKLOAD = "qwen30b_128k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS_PER_STEP = 7   # fp_select: prep, pool, score, csr scan, csr expand; fp_attention: prep, attention
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ work accounting
+
+def accounting(w, cu: np.ndarray, idx: np.ndarray):
+    """FLOP and byte counts of one layer from the workload and its CSR."""
+    import oracle   # segment enumeration only (host bookkeeping)
+    op_seg = segments_of(w)
+    D = op_seg["D"]
+    rows = op_seg["rows"]
+    counts = np.diff(cu)
+    nseg = len(D)
+    # mean-correction chunks per tile: 128-block chunks of [0, D) holding a pruned block
+    chunks = np.zeros(nseg, np.int64)
+    sel_lo = 0
+    for s in range(nseg):
+        ids = idx[cu[s]:cu[s + 1]]
+        d = int(D[s])
+        if d == 0:
+            continue
+        nch = (d + 127) // 128
+        full = np.bincount(ids[ids < d] // 128, minlength=nch)[:nch]
+        cap = np.minimum(128, d - 128 * np.arange(nch))
+        chunks[s] = int(np.sum(full < cap))
+    tile = 4.0 * 128 * 128 * 128
+    executed = tile * float(np.sum(counts) + np.sum(chunks))
+    d = 128
+    dense_equiv = 4.0 * d * w.hq * sum(L * (L + 1) / 2 for L in w.lengths)
+    eb = 2 if w.dtype == "bf16" else 1
+    T = w.total_tokens
+    nblk = sum((L + 127) // 128 for L in w.lengths)
+    stage1_bytes = (T * w.hq * d * eb + 2 * T * w.hkv * d * eb      # Q, K, V read once
+                    + nblk * w.hkv * d * (4 + 4 + 2 * eb)            # means written (fp32 + operand copies)
+                    + 4 * (nseg + 1) + 4 * int(cu[-1]))              # CSR written
+    causal_blocks = int(np.sum(D + 1))
+    return dict(executed_flop=executed, dense_equiv_flop=dense_equiv, stage1_bytes=stage1_bytes,
+                nnz=int(cu[-1]), causal_blocks=causal_blocks, density=int(cu[-1]) / max(causal_blocks, 1),
+                corr_chunks=int(np.sum(chunks)), segments=nseg, rows=rows)
+
+
+def segments_of(w):
+    g = w.hq // w.hkv
+    Ds, rows = [], []
+    for L in w.lengths:
+        nt = (g * L + 127) // 128
+        t = np.arange(nt)
+        for _ in range(w.hkv):
+            Ds.append((t * 128 // g) // 128)
+            rows.append(np.minimum(128, g * L - 128 * t))
+    cat = lambda x: np.concatenate(x) if x else np.zeros(0, np.int64)
+    return dict(D=cat(Ds).astype(np.int64), rows=cat(rows).astype(np.int64))
+
+
+# ------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.idx = device_index
+        self.path = os.path.join("/tmp", f"fp_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.idx), "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- CPU oracle
+
+def oracle_sample_time(w, cu: np.ndarray, idx: np.ndarray, target_s: float = 12.0, threads: int | None = None):
+    """Times the fp64 oracle on a seeded sample of segments of the workload and extrapolates to one layer
+    by the oracle's per-segment work (pooling is timed in full)."""
+    import oracle
+    threads = threads or max(1, os.cpu_count() or 1)
+    op = oracle.Problem.from_workload(w)
+    seg = oracle.segments(op)
+    t0 = time.perf_counter()
+    pooled = oracle.pool(op, seg)
+    t_pool = time.perf_counter() - t0
+    counts = np.diff(cu)
+    # per-segment oracle work: scoring rows x (D+1) x d, attention rows x (exact keys + corrections) x 2d
+    D = seg.D
+    rows = np.minimum(128, (w.hq // w.hkv) * np.asarray(w.lengths)[seg.b] - 128 * seg.t)
+    work = rows * (D + 1) * 128 + rows * (counts * 128 + np.maximum(D - counts + 1, 0)) * 256
+    rng = np.random.default_rng(1234)
+    order = rng.permutation(len(seg))
+    # calibrate on a handful of segments, then size the sample for ~target_s seconds
+    n = min(len(seg), max(threads, 4))
+    elapsed, done = 0.0, 0
+    taken = []
+    while done < len(seg):
+        ids = order[done:done + n]
+        t0 = time.perf_counter()
+        sel = oracle.select(op, w.alpha, w.sink_blocks, w.window_blocks, seg=seg, pooled=pooled, seg_ids=ids,
+                            nthreads=threads)
+        oracle.attend(op, sel.sel_full, seg=seg, pooled=pooled, seg_ids=ids, nthreads=threads)
+        elapsed += time.perf_counter() - t0
+        done += len(ids)
+        taken.extend(ids.tolist())
+        if elapsed >= target_s:
+            break
+        per = elapsed / max(float(np.sum(work[np.array(taken)])), 1.0)
+        n = int(min(len(seg) - done, max(threads, (target_s - elapsed) / max(per * np.mean(work), 1e-12))))
+        if n <= 0:
+            break
+    frac = float(np.sum(work[np.array(taken)])) / max(float(np.sum(work)), 1.0)
+    ms_layer = (t_pool + elapsed / max(frac, 1e-12)) * 1e3
+    sample = (f"{len(taken)} of {len(seg)} segments ({100 * frac:.3f}% of the layer's oracle work) "
+              f"selected + attended, pooling in full; extrapolated by per-segment work")
+    return ms_layer, threads, sample, elapsed + t_pool
+
+
+# ---------------------------------------------------------------------- our arm
+
+def run_ours(args, rank: int, world: int, dist_on: bool):
+    from block_sparse_long_mean_gb300 import binding as B
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = synth.make_workload(args.workload, device=dev, seed=synth.BASE_SEED + rank)
+    p = B.Problem.from_workload(w)
+    bufs = B.Buffers(p, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flags = B.FP_MEAN_CORRECTION
+
+    def step(s1=None, s2=None, s3=None):
+        if s1 is not None:
+            s1.record(stream)
+        B.fp_select(p, w.q, w.k_pages, w.v_pages, w.alpha, w.sink_blocks, w.window_blocks, bufs.csr_cu,
+                    bufs.csr_idx, bufs.kbar, bufs.vbar, bufs.kbar_op, bufs.vbar_op, bufs.workspace, stream)
+        if s2 is not None:
+            s2.record(stream)
+        B.fp_attention(p, w.q, w.k_pages, w.v_pages, bufs.csr_cu, bufs.csr_idx, bufs.kbar_op, bufs.vbar_op, flags,
+                       bufs.out, None, bufs.workspace, stream)
+        if s3 is not None:
+            s3.record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    code = B.fp_device_status(bufs.workspace, stream)
+    if code != 0:
+        raise RuntimeError(f"device status {B.STATUS.get(code, code)}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index)
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    start.record(stream)
+    for i in range(args.steps):
+        step(*ev[i])
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if dist_on:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(stop)
+    s1 = [e[0].elapsed_time(e[1]) for e in ev]
+    s2 = [e[1].elapsed_time(e[2]) for e in ev]
+    if dist_on:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+
+    # end to end through the public API from pinned host buffers
+    h_q = torch.empty(w.q.shape, dtype=w.q.dtype, pin_memory=True)
+    h_k = torch.empty(w.k_pages.shape, dtype=w.k_pages.dtype, pin_memory=True)
+    h_v = torch.empty(w.v_pages.shape, dtype=w.v_pages.dtype, pin_memory=True)
+    h_q.copy_(w.q)
+    h_k.copy_(w.k_pages)
+    h_v.copy_(w.v_pages)
+    h_pt = w.page_table.cpu().pin_memory()
+    h_cu = w.cu_seqlens.cpu().pin_memory()
+    h_out = torch.empty(bufs.out.shape, dtype=bufs.out.dtype, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 10))
+
+    def e2e_step():
+        w.q.copy_(h_q, non_blocking=True)
+        w.k_pages.copy_(h_k, non_blocking=True)
+        w.v_pages.copy_(h_v, non_blocking=True)
+        w.page_table.copy_(h_pt, non_blocking=True)
+        w.cu_seqlens.copy_(h_cu, non_blocking=True)
+        step()
+        h_out.copy_(bufs.out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = es.elapsed_time(ee) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_pt, h_cu))
+    d2h = h_out.numel() * h_out.element_size()
+
+    cu = bufs.csr_cu.cpu().numpy().astype(np.int64)
+    idx = bufs.csr_idx[:int(cu[-1])].cpu().numpy()
+    acc = accounting(w, cu, idx)
+    pk, pk_src = peaks()
+    s1_ms, s2_ms = float(np.median(s1)), float(np.median(s2))
+    s2_mean = float(np.mean(s2))
+    achieved_tflops = acc["executed_flop"] / (s2_mean * 1e-3) / 1e12
+    peak_t = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if w.dtype == "e4m3":
+        peak_t *= 2.0   # FP8 dense rate = 2x BF16 (nominal 4.5 vs 2.25 PFLOP/s)
+    stage1_gbs = acc["stage1_bytes"] / (float(np.mean(s1)) * 1e-3) / 1e9
+    res = dict(metric=METRIC, value=ms_step / world, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
+               ms_per_step=ms_step, higher_is_better=False, scaling="weak", vs_baseline=None,
+               dtype=w.dtype, data="synthetic",
+               config=dict(workload=f"{args.workload}: batch {w.batch}, L={max(w.lengths)}, Hq={w.hq}, "
+                                    f"Hkv={w.hkv}, d=128, B=128, page 64, alpha={w.alpha}, sink 1, window 1",
+                           tokens=w.total_tokens, inputs_larger_than_l2=True, l2_flush=False,
+                           parallelism=f"replicas x{world}"),
+               stage1_ms=s1_ms, stage2_ms=s2_ms,
+               executed_tflops=achieved_tflops,
+               dense_equiv_tflops=acc["dense_equiv_flop"] / (ms_step * 1e-3) / 1e12,
+               stage1_gbs=stage1_gbs, density=acc["density"], correction_chunks=acc["corr_chunks"],
+               roofline=dict(bound="tensor", kernel="fp_attention (Stage 2)", achieved=achieved_tflops,
+                             peak=peak_t, unit="TFLOP/s", frac=achieved_tflops / peak_t,
+                             peak_source=f"{pk_src} bf16 burst" + (" x2 for e4m3" if w.dtype == "e4m3" else ""),
+                             traffic=None),
+               stage1_roofline=dict(bound="hbm", achieved=stage1_gbs, peak=float(pk.get("hbm_gbs", 6800.0)),
+                                    unit="GB/s", frac=stage1_gbs / float(pk.get("hbm_gbs", 6800.0))),
+               e2e=dict(value=e2e_ms, unit=UNIT, h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h)),
+               gpu_launches=KERNELS_PER_STEP * args.steps,
+               clocks=clk)
+    if args.dense_steps > 0:
+        dstart, dstop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        B.fp_attention(p, w.q, w.k_pages, w.v_pages, bufs.csr_cu, bufs.csr_idx, bufs.kbar_op, bufs.vbar_op,
+                       B.FP_DENSE, bufs.out, None, bufs.workspace, stream)
+        dstart.record(stream)
+        for _ in range(args.dense_steps):
+            B.fp_attention(p, w.q, w.k_pages, w.v_pages, bufs.csr_cu, bufs.csr_idx, bufs.kbar_op, bufs.vbar_op,
+                           B.FP_DENSE, bufs.out, None, bufs.workspace, stream)
+        dstop.record(stream)
+        torch.cuda.synchronize(dev)
+        dense_ms = dstart.elapsed_time(dstop) / args.dense_steps
+        res["dense_mode_ms"] = dense_ms
+        res["speedup_vs_dense_mode"] = dense_ms / ms_step
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ms_cpu, cores, sample, _ = oracle_sample_time(w, cu, idx, target_s=args.cpu_seconds)
+        res["cpu_baseline"] = dict(value=ms_cpu, unit=UNIT, cores=cores, kind="oracle", sample=sample)
+    return res
+
+
+def run_reference(args):
+    """The fp64 CPU oracle as the reference arm: each step times a bounded sample of the layer."""
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = synth.make_workload(args.workload, device=dev)
+    # the oracle's own selection defines the CSR used for work accounting
+    import oracle
+    op = oracle.Problem.from_workload(w)
+    seg = oracle.segments(op)
+    pooled = oracle.pool(op, seg)
+    sample_ids = np.random.default_rng(7).choice(len(seg), size=min(len(seg), 64), replace=False)
+    sel = oracle.select(op, w.alpha, w.sink_blocks, w.window_blocks, seg=seg, pooled=pooled, seg_ids=sample_ids)
+    # selected counts: forced set estimate for unsampled segments, the oracle's own for sampled ones
+    counts = np.minimum(seg.D + 1, 3)
+    for s in sample_ids:
+        counts[s] = len(sel.selected(seg, s))
+    cu = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    idx = np.zeros(int(cu[-1]), np.int64)
+    per_step = max(2.0, min(args.cpu_seconds, 150.0 / max(args.steps + args.warmup, 1)))
+    times = []
+    for i in range(args.warmup + args.steps):
+        ms, cores, sample, _ = oracle_sample_time(w, cu, idx, target_s=per_step)
+        if i >= args.warmup:
+            times.append(ms)
+    v = float(np.mean(times))
+    return dict(impl="reference", metric=METRIC, value=v, unit=UNIT, n_gpus=1, steps=args.steps,
+                warmup=args.warmup, ms_per_step=v, higher_is_better=False, scaling="weak", vs_baseline=None,
+                dtype="f64", data="synthetic", config=dict(workload=args.workload, tokens=w.total_tokens),
+                cpu_baseline=dict(value=v, unit=UNIT, cores=cores, kind="oracle", sample=sample),
+                e2e=dict(value=v, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--dense-steps", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    dist_on = world > 1
+    if dist_on:
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world, dist_on)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist_on:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

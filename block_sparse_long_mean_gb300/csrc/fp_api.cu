@@ -1,0 +1,196 @@
+// Host side of the C ABI declared in include/fp.h: argument validation,
+// sizing, workspace layout and the launch sequence of each stage.
+#include <stdio.h>
+#include <string.h>
+
+#include "fp_internal.cuh"
+
+namespace fp {
+namespace {
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+// Validates the description; fills the sizes from host_cu_seqlens.
+fp_status describe(const fp_problem *p, Sizes *s) {
+    if (!p || !p->host_cu_seqlens) return FP_ERR_INVALID_ARG;
+    if (p->batch < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0) return FP_ERR_INVALID_ARG;
+    if (p->num_q_heads % p->num_kv_heads) return FP_ERR_UNSUPPORTED;
+    int g = p->num_q_heads / p->num_kv_heads;
+    if (!is_pow2(g) || g > 16) return FP_ERR_UNSUPPORTED;
+    if (p->head_dim != kHeadDim || p->block_size != kBlock) return FP_ERR_UNSUPPORTED;
+    if (!is_pow2(p->page_size) || p->page_size < 8 || p->page_size > 128) return FP_ERR_UNSUPPORTED;
+    if (p->dtype != FP_DTYPE_BF16 && p->dtype != FP_DTYPE_E4M3) return FP_ERR_UNSUPPORTED;
+    if (p->dtype == FP_DTYPE_E4M3 && !(p->c_q > 0.f && p->c_k > 0.f && p->c_v > 0.f)) return FP_ERR_INVALID_ARG;
+    if (p->num_pages < 0 || p->page_table_stride < 0) return FP_ERR_INVALID_ARG;
+    if (p->host_cu_seqlens[0] != 0) return FP_ERR_INVALID_ARG;
+    Sizes r;
+    r.g = g;
+    for (int b = 0; b < p->batch; ++b) {
+        int64_t L = (int64_t)p->host_cu_seqlens[b + 1] - p->host_cu_seqlens[b];
+        if (L < 0) return FP_ERR_INVALID_ARG;
+        if (L > kMaxLen) return FP_ERR_UNSUPPORTED;
+        int64_t nb = (L + kBlock - 1) / kBlock;
+        int64_t nt = (g * L + kTileRows - 1) / kTileRows;
+        int64_t words = (nb + 31) / 32;
+        if ((L + p->page_size - 1) / p->page_size > p->page_table_stride) return FP_ERR_INVALID_ARG;
+        r.nseg += p->num_kv_heads * nt;
+        r.nblocks += nb;
+        r.mask_words += p->num_kv_heads * nt * words;
+        // sum over the request's tiles of (D + 1), D = floor(128 t / g / 128) = floor(t / g)
+        for (int64_t t = 0; t < nt; ++t) r.capacity += p->num_kv_heads * (t / g + 1);
+        r.total_tokens += L;
+        if (L > r.max_len) r.max_len = (int32_t)L;
+        if (nb > r.max_blocks) r.max_blocks = (int32_t)nb;
+    }
+    if (r.nseg >= INT32_MAX || r.nblocks >= INT32_MAX || r.mask_words >= INT32_MAX || r.total_tokens >= INT32_MAX)
+        return FP_ERR_UNSUPPORTED;
+    if (r.total_tokens > 0 && (!p->cu_seqlens || !p->page_table)) return FP_ERR_INVALID_ARG;
+    *s = r;
+    return FP_OK;
+}
+
+WsLayout layout(const fp_problem *p, const Sizes &s) {
+    WsLayout w;
+    int64_t o = 0;
+    w.status = o; o = align256(o + 64 * 4);
+    w.req = o; o = align256(o + (int64_t)sizeof(ReqInfo) * (p->batch + 1));
+    w.seg_count = o; o = align256(o + 4 * (s.nseg + 1));
+    w.mask = o; o = align256(o + 4 * (s.mask_words + 1));
+    w.work = o; o = align256(o + 4 * (s.nseg + 1));
+    w.hist = o; o = align256(o + 4 * (int64_t)(kMaxBlocks + 2));
+    w.counters = o; o = align256(o + 4 * 64);
+    w.total = o;
+    return w;
+}
+
+fp_status make_ctx(const fp_problem *p, void *workspace, size_t ws_bytes, fp_stream_t stream, Ctx *c) {
+    Sizes s;
+    fp_status st = describe(p, &s);
+    if (st != FP_OK) return st;
+    if (!workspace) return FP_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256) return FP_ERR_INVALID_ARG;
+    WsLayout w = layout(p, s);
+    if ((int64_t)ws_bytes < w.total) return FP_ERR_WORKSPACE;
+    c->p = *p;
+    c->s = s;
+    c->ws = w;
+    c->wsbase = static_cast<char *>(workspace);
+    c->stream = reinterpret_cast<cudaStream_t>(stream);
+    return FP_OK;
+}
+
+fp_status launched(cudaError_t e) {
+    if (e != cudaSuccess) {
+        fprintf(stderr, "libfp: CUDA error: %s\n", cudaGetErrorString(e));
+        return FP_ERR_CUDA;
+    }
+    return FP_OK;
+}
+
+}  // namespace
+}  // namespace fp
+
+using namespace fp;
+
+extern "C" {
+
+int64_t fp_workspace_bytes(const fp_problem *p) {
+    Sizes s;
+    fp_status st = describe(p, &s);
+    if (st != FP_OK) return st;
+    return layout(p, s).total;
+}
+
+int64_t fp_num_segments(const fp_problem *p) {
+    Sizes s;
+    fp_status st = describe(p, &s);
+    return st != FP_OK ? st : s.nseg;
+}
+
+int64_t fp_num_blocks(const fp_problem *p) {
+    Sizes s;
+    fp_status st = describe(p, &s);
+    return st != FP_OK ? st : s.nblocks;
+}
+
+int64_t fp_csr_capacity(const fp_problem *p) {
+    Sizes s;
+    fp_status st = describe(p, &s);
+    return st != FP_OK ? st : s.capacity;
+}
+
+fp_status fp_select(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages, float alpha,
+                    int32_t sink_blocks, int32_t window_blocks, int32_t *csr_cu, int32_t *csr_idx,
+                    int64_t csr_idx_capacity, float *kbar, float *vbar, void *kbar_op, void *vbar_op,
+                    void *workspace, size_t workspace_bytes, fp_stream_t stream) {
+    Ctx c;
+    fp_status st = make_ctx(p, workspace, workspace_bytes, stream, &c);
+    if (st != FP_OK) return st;
+    if (!(alpha >= 0.f) || sink_blocks < 0 || window_blocks < 0 || csr_idx_capacity < 0) return FP_ERR_INVALID_ARG;
+    if (!csr_cu) return FP_ERR_INVALID_ARG;
+    if (c.s.total_tokens > 0 && (!q || !k_pages || !v_pages || !kbar || !vbar || !kbar_op || !vbar_op))
+        return FP_ERR_INVALID_ARG;
+    if (c.s.nseg > 0 && !csr_idx) return FP_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(c.status(), 0, 64 * 4, c.stream);
+    if (e == cudaSuccess) e = launch_prep(c);
+    if (e == cudaSuccess && c.s.nblocks > 0) e = launch_pool(c, k_pages, v_pages, kbar, vbar, kbar_op, vbar_op);
+    if (e == cudaSuccess && c.s.nseg > 0) e = launch_score(c, q, kbar, alpha, sink_blocks, window_blocks);
+    if (e == cudaSuccess) e = launch_csr(c, csr_cu, csr_idx, csr_idx_capacity);
+    return launched(e);
+}
+
+fp_status fp_attention(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages,
+                       const int32_t *csr_cu, const int32_t *csr_idx, int64_t csr_idx_capacity,
+                       const void *kbar_op, const void *vbar_op, int32_t flags, void *out, float *lse,
+                       void *workspace, size_t workspace_bytes, fp_stream_t stream) {
+    Ctx c;
+    fp_status st = make_ctx(p, workspace, workspace_bytes, stream, &c);
+    if (st != FP_OK) return st;
+    if (flags & ~(FP_MEAN_CORRECTION | FP_DENSE)) return FP_ERR_INVALID_ARG;
+    bool dense = flags & FP_DENSE;
+    bool corr = (flags & FP_MEAN_CORRECTION) && !dense;
+    if (csr_idx_capacity < 0) return FP_ERR_INVALID_ARG;
+    if (c.s.total_tokens > 0 && (!q || !k_pages || !v_pages || !out)) return FP_ERR_INVALID_ARG;
+    if (c.s.nseg > 0 && !dense && (!csr_cu || !csr_idx)) return FP_ERR_INVALID_ARG;
+    if (c.s.nseg > 0 && corr && (!kbar_op || !vbar_op)) return FP_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(c.status(), 0, 64 * 4, c.stream);
+    if (e == cudaSuccess) e = launch_prep(c);
+    if (e == cudaSuccess && c.s.nseg > 0)
+        e = launch_attention(c, q, k_pages, v_pages, csr_cu, csr_idx, csr_idx_capacity, kbar_op, vbar_op,
+                             (corr ? FP_MEAN_CORRECTION : 0) | (dense ? FP_DENSE : 0), out, lse);
+    return launched(e);
+}
+
+fp_status fp_device_status(const void *workspace, fp_stream_t stream) {
+    if (!workspace) return FP_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t code = 0;
+    cudaError_t e = cudaMemcpyAsync(&code, workspace, sizeof code, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        fprintf(stderr, "libfp: CUDA error: %s\n", cudaGetErrorString(e));
+        return FP_ERR_CUDA;
+    }
+    return (fp_status)code;
+}
+
+const char *fp_status_string(fp_status s) {
+    switch (s) {
+        case FP_OK: return "ok";
+        case FP_ERR_INVALID_ARG: return "invalid argument";
+        case FP_ERR_UNSUPPORTED: return "unsupported problem";
+        case FP_ERR_WORKSPACE: return "workspace too small";
+        case FP_ERR_CUDA: return "CUDA error";
+        case FP_ERR_CAPACITY: return "CSR capacity too small";
+        case FP_ERR_DEVICE_PAGE: return "device: page id out of range";
+        case FP_ERR_DEVICE_CSR: return "device: malformed CSR segment";
+        case FP_ERR_DEVICE_OVERFLOW: return "device: CSR index capacity exceeded";
+        case FP_ERR_DEVICE_TIMEOUT: return "device: bounded wait expired";
+        case FP_ERR_DEVICE_SEQLEN: return "device: cu_seqlens differ from host copy";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

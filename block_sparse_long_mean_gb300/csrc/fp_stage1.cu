@@ -1,0 +1,430 @@
+// Stage 1 of FlashPrefill V2 (Alg.1 steps 1-5): request tables, block mean
+// pooling (Eq.5), pooled-key scoring (Eq.19), max-based thresholding with
+// forced blocks (Eq.20) and CSR assembly (Sec.3.3 "Index-Driven Sparse
+// Traversal").
+#include <math.h>
+
+#include "fp_internal.cuh"
+
+namespace fp {
+namespace {
+
+// ------------------------------------------------------------ block scan helper
+
+// Inclusive scan of three int32 lanes across a CTA of blockDim.x threads
+// (a multiple of 32). Returns the inclusive values; totals go to `tot`.
+__device__ void block_scan3(int32_t v[3], int32_t tot[3]) {
+    __shared__ int32_t warp_sums[32][3];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int32_t n = __shfl_up_sync(0xffffffffu, v[k], o);
+            if (lane >= o) v[k] += n;
+        }
+    }
+    if (lane == 31)
+        for (int k = 0; k < 3; ++k) warp_sums[warp][k] = v[k];
+    __syncthreads();
+    if (warp == 0) {
+        for (int k = 0; k < 3; ++k) {
+            int32_t s = lane < nwarps ? warp_sums[lane][k] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int32_t n = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += n;
+            }
+            if (lane < nwarps) warp_sums[lane][k] = s;
+        }
+    }
+    __syncthreads();
+    for (int k = 0; k < 3; ++k) {
+        if (warp > 0) v[k] += warp_sums[warp - 1][k];
+        tot[k] = warp_sums[nwarps - 1][k];
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ prep kernel
+
+// Builds the per-request table from the device cu_seqlens and checks it
+// against the totals the host derived from host_cu_seqlens.
+__global__ void __launch_bounds__(1024) prep_kernel(const int32_t *__restrict__ cu, int batch, int hkv, int g,
+                                                    int64_t want_nseg, int64_t want_blocks, int64_t want_words,
+                                                    int64_t want_tokens, ReqInfo *__restrict__ req,
+                                                    int32_t *__restrict__ status) {
+    __shared__ int32_t carry[3];
+    __shared__ int bad;
+    if (threadIdx.x == 0) {
+        carry[0] = carry[1] = carry[2] = 0;
+        bad = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < batch; base += blockDim.x) {
+        const int b = base + threadIdx.x;
+        ReqInfo r = {};
+        int32_t v[3] = {0, 0, 0};
+        if (b < batch) {
+            int32_t q0 = cu[b], q1 = cu[b + 1];
+            int32_t L = q1 - q0;
+            if (q0 < 0 || L < 0 || L > kMaxLen || q1 > want_tokens) {
+                bad = 1;
+                L = 0;
+            }
+            r.q_start = q0;
+            r.len = L;
+            r.nblocks = (L + kBlock - 1) / kBlock;
+            r.ntiles = (g * L + kTileRows - 1) / kTileRows;
+            r.words = (r.nblocks + 31) / 32;
+            v[0] = r.nblocks;
+            v[1] = hkv * r.ntiles;
+            v[2] = hkv * r.ntiles * r.words;
+        }
+        int32_t own[3] = {v[0], v[1], v[2]};
+        int32_t tot[3];
+        block_scan3(v, tot);
+        if (b < batch) {
+            r.blk_base = carry[0] + v[0] - own[0];
+            r.seg_base = carry[1] + v[1] - own[1];
+            r.mask_base = carry[2] + v[2] - own[2];
+            req[b] = r;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0)
+            for (int k = 0; k < 3; ++k) carry[k] += tot[k];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        ReqInfo s = {};
+        s.blk_base = carry[0];
+        s.seg_base = carry[1];
+        s.mask_base = carry[2];
+        req[batch] = s;
+        if (bad || carry[0] != want_blocks || carry[1] != want_nseg || carry[2] != want_words ||
+            cu[batch] != want_tokens)
+            set_status(status, FP_ERR_DEVICE_SEQLEN);
+    }
+}
+
+// ----------------------------------------------------------------- pool kernel
+
+// One CTA per (request, block): the means of its <= 128 tokens for every KV
+// head (Eq.5). Each thread accumulates one 16-byte column vector of the
+// token rows over a strided subset of tokens in fp32; a shared-memory pass
+// sums the token groups. FP8 elements are descaled before summing.
+template <int kDtype>
+__global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ kp, const uint8_t *__restrict__ vp,
+                                                   const int32_t *__restrict__ page_table, int pt_stride,
+                                                   int num_pages, int page_size, const ReqInfo *__restrict__ req,
+                                                   int batch, int hkv, float c_k, float c_v,
+                                                   float *__restrict__ kbar, float *__restrict__ vbar,
+                                                   void *__restrict__ kbar_op, void *__restrict__ vbar_op,
+                                                   int32_t *__restrict__ status) {
+    using E = Elem<kDtype>;
+    constexpr int kEb = E::kBytes;
+    constexpr int kEpv = 16 / kEb;  // elements per 16-byte vector
+    __shared__ float red[2][256 * kEpv];
+    if (status_bad(status)) return;
+    const int gb = blockIdx.x;
+    const int b = find_req_by_block(req, batch, gb);
+    const ReqInfo r = req[b];
+    const int J = gb - r.blk_base;
+    const int n = min(kBlock, r.len - J * kBlock);
+    const int row_bytes = hkv * kHeadDim * kEb;
+    const int nvec = row_bytes / 16;
+    const int TG = nvec >= 256 ? 1 : 256 / nvec;
+    const int cols = 256 / TG;
+    const float sk = kDtype == FP_DTYPE_E4M3 ? c_k : 1.f;
+    const float sv = kDtype == FP_DTYPE_E4M3 ? c_v : 1.f;
+    for (int c0 = 0; c0 < nvec; c0 += cols) {
+        const int col = c0 + threadIdx.x % cols;
+        const int tg = threadIdx.x / cols;
+        float ak[kEpv], av[kEpv];
+#pragma unroll
+        for (int e = 0; e < kEpv; ++e) ak[e] = av[e] = 0.f;
+        if (col < nvec && tg < TG) {
+            for (int j = tg; j < n; j += TG) {
+                const int tok = J * kBlock + j;
+                const int page = page_table[(int64_t)b * pt_stride + tok / page_size];
+                if (page < 0 || page >= num_pages) {
+                    set_status(status, FP_ERR_DEVICE_PAGE, page);
+                    continue;
+                }
+                const int64_t off = ((int64_t)page * page_size + tok % page_size) * row_bytes + (int64_t)col * 16;
+                const uint4 kraw = *reinterpret_cast<const uint4 *>(kp + off);
+                const uint4 vraw = *reinterpret_cast<const uint4 *>(vp + off);
+                const typename E::T *ke = reinterpret_cast<const typename E::T *>(&kraw);
+                const typename E::T *ve = reinterpret_cast<const typename E::T *>(&vraw);
+#pragma unroll
+                for (int e = 0; e < kEpv; ++e) {
+                    ak[e] += E::to_float(ke[e]) * sk;
+                    av[e] += E::to_float(ve[e]) * sv;
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < kEpv; ++e) {
+            red[0][threadIdx.x * kEpv + e] = ak[e];
+            red[1][threadIdx.x * kEpv + e] = av[e];
+        }
+        __syncthreads();
+        const float inv_n = 1.f / (float)n;
+        for (int x = threadIdx.x; x < cols * kEpv; x += 256) {
+            const int lc = x / kEpv, e = x % kEpv;
+            const int colx = c0 + lc;
+            if (colx >= nvec) continue;
+            float sk_ = 0.f, sv_ = 0.f;
+            for (int t = 0; t < TG; ++t) {
+                sk_ += red[0][(t * cols + lc) * kEpv + e];
+                sv_ += red[1][(t * cols + lc) * kEpv + e];
+            }
+            const float mk = sk_ * inv_n, mv = sv_ * inv_n;
+            const int64_t oi = (int64_t)gb * hkv * kHeadDim + (int64_t)colx * kEpv + e;
+            kbar[oi] = mk;
+            vbar[oi] = mv;
+            if (kDtype == FP_DTYPE_E4M3) {
+                reinterpret_cast<__nv_fp8_e4m3 *>(kbar_op)[oi] = __nv_fp8_e4m3(mk / c_k);
+                reinterpret_cast<__nv_fp8_e4m3 *>(vbar_op)[oi] = __nv_fp8_e4m3(mv / c_v);
+            } else {
+                reinterpret_cast<__nv_bfloat16 *>(kbar_op)[oi] = __float2bfloat16_rn(mk);
+                reinterpret_cast<__nv_bfloat16 *>(vbar_op)[oi] = __float2bfloat16_rn(mv);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- score kernel
+
+// One CTA per segment (request b, KV head h, packed tile t), 128 threads.
+// Thread i owns block J = 128 c + i of chunk c and reduces its logits
+// s_rJ = q_r . kbar_J / sqrt(d) over the tile's rows r into the log-energy
+// lE_J = ln sum_r exp(s_rJ) with an online max (Eq.19 up to the common
+// factor exp(-M), which cancels in Eq.20). Selection (Eq.20):
+//   J kept  <=>  lE_J >= ln(alpha) + max_J' lE_J'  or J forced.
+// The result is a bitmask over J in [0, D] and the segment's count.
+constexpr int kScoreThreads = 128;
+constexpr int kKPad = kHeadDim + 1;
+constexpr size_t kScoreSmem = sizeof(float) * (kTileRows * kHeadDim + 128 * kKPad + kMaxBlocks);
+
+template <int kDtype>
+__global__ void __launch_bounds__(kScoreThreads) score_kernel(
+    const typename Elem<kDtype>::T *__restrict__ q, const float *__restrict__ kbar, const ReqInfo *__restrict__ req,
+    int batch, int hq, int hkv, int g, float log_alpha, int sink, int window, float c_q, int32_t nseg,
+    int32_t *__restrict__ seg_count, uint32_t *__restrict__ mask, int32_t *__restrict__ status) {
+    using E = Elem<kDtype>;
+    extern __shared__ float smem[];
+    float *qs = smem;                          // [128][128]
+    float *ks = qs + kTileRows * kHeadDim;     // [128][129]
+    float *lE = ks + 128 * kKPad;              // [kMaxBlocks]
+    __shared__ float red[kScoreThreads / 32];
+    __shared__ int cnt_red[kScoreThreads / 32];
+    if (status_bad(status)) return;
+    const int seg = nseg - 1 - blockIdx.x;  // heavier tiles (larger t) first
+    const SegCoord sc = decode_seg(req, batch, g, seg);
+    const ReqInfo r = req[sc.b];
+    const int r0 = sc.t * kTileRows;
+    const float qscale = kDtype == FP_DTYPE_E4M3 ? c_q : 1.f;
+    for (int e = threadIdx.x; e < kTileRows * kHeadDim; e += kScoreThreads) {
+        const int row = e / kHeadDim, c = e % kHeadDim;
+        float v = 0.f;
+        if (row < sc.rows) {
+            const int gr = r0 + row;
+            const int pos = gr / g, head = sc.h * g + gr % g;
+            v = E::to_float(q[((int64_t)(r.q_start + pos) * hq + head) * kHeadDim + c]) * qscale;
+        }
+        qs[e] = v;
+    }
+    const float inv_sqrt_d = 1.f / sqrtf((float)kHeadDim);
+    for (int c0 = 0; c0 <= sc.D; c0 += 128) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < 128 * kHeadDim; e += kScoreThreads) {
+            const int i = e / kHeadDim, c = e % kHeadDim;
+            const int J = c0 + i;
+            ks[i * kKPad + c] = J <= sc.D ? kbar[((int64_t)(r.blk_base + J) * hkv + sc.h) * kHeadDim + c] : 0.f;
+        }
+        __syncthreads();
+        const int J = c0 + threadIdx.x;
+        if (J <= sc.D) {
+            const float *kr = ks + threadIdx.x * kKPad;
+            float m = -INFINITY, l = 0.f;
+            for (int row = 0; row < sc.rows; row += 4) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int c = 0; c < kHeadDim; ++c) {
+                    const float kv = kr[c];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) acc[u] = fmaf(qs[(row + u) * kHeadDim + c], kv, acc[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (row + u >= sc.rows) break;
+                    const float s = acc[u] * inv_sqrt_d;
+                    if (s > m) {
+                        l = l * expf(m - s) + 1.f;
+                        m = s;
+                    } else {
+                        l += expf(s - m);
+                    }
+                }
+            }
+            lE[J] = m + logf(l);
+        }
+    }
+    __syncthreads();
+    float mx = -INFINITY;
+    for (int J = threadIdx.x; J <= sc.D; J += kScoreThreads) mx = fmaxf(mx, lE[J]);
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = red[0];
+    for (int w = 1; w < kScoreThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+    const float thr = log_alpha + mx;
+    const int64_t wbase = (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
+    int cnt = 0;
+    for (int w = threadIdx.x; w < r.words; w += kScoreThreads) {
+        uint32_t bits = 0;
+        for (int k = 0; k < 32; ++k) {
+            const int J = 32 * w + k;
+            if (J > sc.D) break;
+            const bool forced = J < sink || (J >= sc.D - window && J < sc.D) || J == sc.D;
+            if (forced || lE[J] >= thr) bits |= 1u << k;
+        }
+        mask[wbase + w] = bits;
+        cnt += __popc(bits);
+    }
+    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if ((threadIdx.x & 31) == 0) cnt_red[threadIdx.x >> 5] = cnt;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int tot = 0;
+        for (int w = 0; w < kScoreThreads / 32; ++w) tot += cnt_red[w];
+        seg_count[seg] = tot;
+    }
+}
+
+// ------------------------------------------------------------------ CSR kernels
+
+// Exclusive scan of the per-segment counts into csr_cu (one CTA).
+__global__ void __launch_bounds__(1024) csr_scan_kernel(const int32_t *__restrict__ count, int32_t nseg,
+                                                        int64_t capacity, int32_t *__restrict__ cu,
+                                                        int32_t *__restrict__ status) {
+    __shared__ int32_t carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    if (status_bad(status)) {
+        if (threadIdx.x == 0) cu[0] = 0;
+        return;
+    }
+    for (int base = 0; base < nseg; base += blockDim.x) {
+        const int i = base + threadIdx.x;
+        int32_t v[3] = {i < nseg ? count[i] : 0, 0, 0};
+        const int32_t own = v[0];
+        int32_t tot[3];
+        block_scan3(v, tot);
+        if (i < nseg) cu[i] = carry + v[0] - own;
+        __syncthreads();
+        if (threadIdx.x == 0) carry += tot[0];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        cu[nseg] = carry;
+        if (carry > capacity) set_status(status, FP_ERR_DEVICE_OVERFLOW, carry);
+    }
+}
+
+// One warp per segment: expands the selection bitmask into ascending block ids.
+__global__ void __launch_bounds__(256) csr_expand_kernel(const uint32_t *__restrict__ mask,
+                                                         const ReqInfo *__restrict__ req, int batch, int g,
+                                                         int32_t nseg, const int32_t *__restrict__ cu,
+                                                         int64_t capacity, int32_t *__restrict__ idx,
+                                                         int32_t *__restrict__ status) {
+    if (status_bad(status)) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t seg = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); seg < nseg; seg += warps) {
+        const SegCoord sc = decode_seg(req, batch, g, seg);
+        const ReqInfo r = req[sc.b];
+        const int64_t wbase = (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
+        const int nw = (sc.D + 1 + 31) / 32;
+        int64_t pos = cu[seg];
+        for (int w0 = 0; w0 < nw; w0 += 32) {
+            const int w = w0 + lane;
+            uint32_t word = w < nw ? mask[wbase + w] : 0u;
+            const int c = __popc(word);
+            int incl = c;
+            for (int o = 1; o < 32; o <<= 1) {
+                int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            int64_t p = pos + incl - c;
+            while (word) {
+                const int bit = __ffs(word) - 1;
+                if (p < capacity) idx[p] = 32 * w + bit;
+                ++p;
+                word &= word - 1;
+            }
+            pos += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const Ctx &c) {
+    const int threads = 1024;
+    prep_kernel<<<1, threads, 0, c.stream>>>(c.p.cu_seqlens, c.p.batch, c.p.num_kv_heads, c.s.g, c.s.nseg,
+                                             c.s.nblocks, c.s.mask_words, c.s.total_tokens, c.req(), c.status());
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pool(const Ctx &c, const void *k_pages, const void *v_pages, float *kbar, float *vbar,
+                        void *kbar_op, void *vbar_op) {
+    const dim3 grid((unsigned)c.s.nblocks);
+    if (c.p.dtype == FP_DTYPE_E4M3)
+        pool_kernel<FP_DTYPE_E4M3><<<grid, 256, 0, c.stream>>>(
+            (const uint8_t *)k_pages, (const uint8_t *)v_pages, c.p.page_table, c.p.page_table_stride,
+            c.p.num_pages, c.p.page_size, c.req(), c.p.batch, c.p.num_kv_heads, c.p.c_k, c.p.c_v, kbar, vbar,
+            kbar_op, vbar_op, c.status());
+    else
+        pool_kernel<FP_DTYPE_BF16><<<grid, 256, 0, c.stream>>>(
+            (const uint8_t *)k_pages, (const uint8_t *)v_pages, c.p.page_table, c.p.page_table_stride,
+            c.p.num_pages, c.p.page_size, c.req(), c.p.batch, c.p.num_kv_heads, 1.f, 1.f, kbar, vbar, kbar_op,
+            vbar_op, c.status());
+    return cudaGetLastError();
+}
+
+cudaError_t launch_score(const Ctx &c, const void *q, const float *kbar, float alpha, int sink, int window) {
+    const float log_alpha = alpha > 0.f ? logf(alpha) : -INFINITY;
+    const dim3 grid((unsigned)c.s.nseg);
+    cudaError_t e;
+    if (c.p.dtype == FP_DTYPE_E4M3) {
+        e = cudaFuncSetAttribute(score_kernel<FP_DTYPE_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kScoreSmem);
+        if (e != cudaSuccess) return e;
+        score_kernel<FP_DTYPE_E4M3><<<grid, kScoreThreads, kScoreSmem, c.stream>>>(
+            (const __nv_fp8_e4m3 *)q, kbar, c.req(), c.p.batch, c.p.num_q_heads, c.p.num_kv_heads, c.s.g,
+            log_alpha, sink, window, c.p.c_q, (int32_t)c.s.nseg, c.seg_count(), c.mask(), c.status());
+    } else {
+        e = cudaFuncSetAttribute(score_kernel<FP_DTYPE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kScoreSmem);
+        if (e != cudaSuccess) return e;
+        score_kernel<FP_DTYPE_BF16><<<grid, kScoreThreads, kScoreSmem, c.stream>>>(
+            (const __nv_bfloat16 *)q, kbar, c.req(), c.p.batch, c.p.num_q_heads, c.p.num_kv_heads, c.s.g,
+            log_alpha, sink, window, 1.f, (int32_t)c.s.nseg, c.seg_count(), c.mask(), c.status());
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_csr(const Ctx &c, int32_t *csr_cu, int32_t *csr_idx, int64_t capacity) {
+    csr_scan_kernel<<<1, 1024, 0, c.stream>>>(c.seg_count(), (int32_t)c.s.nseg, capacity, csr_cu, c.status());
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || c.s.nseg == 0) return e;
+    const int64_t warps = c.s.nseg;
+    const unsigned blocks = (unsigned)((warps + 7) / 8 < 65535 * 8 ? (warps + 7) / 8 : 65535 * 8);
+    csr_expand_kernel<<<blocks, 256, 0, c.stream>>>(c.mask(), c.req(), c.p.batch, c.s.g, (int32_t)c.s.nseg, csr_cu,
+                                                    capacity, csr_idx, c.status());
+    return cudaGetLastError();
+}
+
+}  // namespace fp

@@ -48,14 +48,16 @@ WORKLOADS = {
     "qwen30b_128k": dict(lengths=[131072], hq=32, hkv=4, dtype="bf16", alpha=0.1, paging="random", stripes=True),
     # the same layer in FP8 E4M3
     "qwen30b_128k_fp8": dict(lengths=[131072], hq=32, hkv=4, dtype="e4m3", alpha=0.2, paging="random",
-                             stripes=True),
+                             stripes=True, base="qwen30b_128k"),
     # continuous batching: 16 requests, log-uniform lengths in [4096, 131072]
     "varlen16": dict(lengths="loguniform16", hq=32, hkv=4, dtype="bf16", alpha=0.1, paging="random",
                      stripes=False),
     "varlen16_fp8": dict(lengths="loguniform16", hq=32, hkv=4, dtype="e4m3", alpha=0.2, paging="random",
-                         stripes=False),
+                         stripes=False, base="varlen16"),
 }
+# FP8 variants draw the same bf16 data as their base workload before quantising it
 WORKLOAD_INDEX = {name: i for i, name in enumerate(WORKLOADS)}
+WORKLOAD_INDEX.update({name: WORKLOAD_INDEX[spec["base"]] for name, spec in WORKLOADS.items() if "base" in spec})
 
 
 @dataclasses.dataclass
@@ -146,7 +148,7 @@ def make_workload(name: str, device="cpu", seed: int = BASE_SEED, lengths: Optio
                   hq: Optional[int] = None, hkv: Optional[int] = None, dtype: Optional[str] = None,
                   paging: Optional[str] = None, stripes: Optional[bool] = None, mu_scale: float = 1.0,
                   alpha: Optional[float] = None, sink_blocks: int = 1, window_blocks: int = 1,
-                  extra_page_frac: float = 0.05) -> Workload:
+                  extra_page_frac: float = 0.05, page_size: int = PAGE) -> Workload:
     """Builds a named workload; keyword arguments override its shape (for small test cases).
 
     mu_scale < 1 gives the "stress" variant with much denser block selection.
@@ -171,6 +173,7 @@ def make_workload(name: str, device="cpu", seed: int = BASE_SEED, lengths: Optio
     T = sum(lengths)
 
     # page table: pages dealt to requests in order from a (permuted) pool
+    PAGE = page_size
     pages_per = [(L + PAGE - 1) // PAGE for L in lengths]
     used = sum(pages_per)
     num_pages = max(1, used + int(math.ceil(extra_page_frac * used)))

@@ -1,0 +1,178 @@
+/*
+ * fp.h -- C ABI of the GB300 (sm_103a) FlashPrefill V2 block-sparse prefill
+ * attention library (libfp.so).
+ *
+ * Method: "FlashPrefill V2: Block-Sparse Prefill Attention for Long-Context
+ * LLM Serving" (arXiv 2608.19758). One attention layer runs in two calls:
+ *
+ *   fp_select     Stage 1 / index stage (Sec.3.1, Sec.3.3 "Single-Pass Score
+ *                 and Selection", Alg.1 steps 1-5): block means of K and V
+ *                 (Eq.5), pooled-key energies of every packed query tile
+ *                 (Eq.19), the max-based threshold with forced sink / window /
+ *                 diagonal blocks (Eq.3, Eq.20), compacted into a CSR index.
+ *   fp_attention  Stage 2 / attention stage (Sec.3.2, Sec.3.3, Alg.1 steps
+ *                 6-11): exact attention over the selected blocks, one
+ *                 mean-correction term per pruned causal block (Eq.6), online
+ *                 softmax, epilogue normalisation; BF16 or FP8-E4M3 (Eq.15).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers unless a name starts with
+ *     `host_`. The caller owns and allocates every buffer, the workspace
+ *     included; the library allocates nothing and keeps no state between
+ *     calls. Inputs are read-only; outputs are fully overwritten.
+ *   - Work is enqueued asynchronously on `stream`; no call synchronises the
+ *     host except fp_device_status. Results are deterministic for fixed
+ *     inputs (bit-identical across runs, page placements and request orders).
+ *   - Host-detected errors return a negative fp_status and enqueue nothing.
+ *     Device-detected errors (a page id out of range, a malformed CSR, an
+ *     index capacity overflow, an expired bounded wait) are recorded in the
+ *     workspace's status word; the kernels never trap. fp_device_status
+ *     reads it back.
+ *
+ * Layouts (row-major, innermost last)
+ *   q          [T, Hq, 128] elements of `dtype`; T = cu_seqlens[batch]
+ *   k_pages,   [num_pages, page_size, Hkv, 128] elements of `dtype`; token j
+ *   v_pages      of request b lives in page page_table[b * stride + j / page_size]
+ *                at slot j % page_size (Sec.3.3 "Paged and Variable-Length
+ *                Execution", Eq.22). Slots past a request's length must hold
+ *                finite values (they are multiplied by zero, never selected).
+ *   out        [T, Hq, 128] bf16
+ *   lse        [T, Hq] fp32, natural-log softmax denominator (optional)
+ *   kbar, vbar [num_blocks, Hkv, 128] fp32 block means; request b's blocks
+ *                are rows blk_base(b) .. blk_base(b) + ceil(L_b/128) - 1,
+ *                blk_base(b) = sum_{b' < b} ceil(L_b'/128)
+ *   kbar_op,   [num_blocks, Hkv, 128] the same means in the operand format:
+ *   vbar_op      bf16, or E4M3 of mean / c_k (resp. mean / c_v) for FP8
+ *   CSR        one segment per (request b, KV head h, packed tile t), in that
+ *                order (Sec.3.3 "Index-Driven Sparse Traversal"); tile t holds
+ *                packed rows [128 t, 128 t + 128) of Q' = PackGQA(Q), row r
+ *                being position floor(r/g) of query head h*g + r mod g
+ *                (Eq.12-13). csr_cu [num_segments + 1] int32 are offsets into
+ *                csr_idx [capacity] int32, which lists each segment's selected
+ *                128-token block ids (relative to the request) ascending.
+ *
+ * Limits: head_dim = block_size = 128; g = Hq / Hkv a power of two <= 16;
+ * page_size a power of two in [8, 128]; every request's query and KV lengths
+ * are equal (prefill without a cached prefix) and at most 1,048,576 tokens.
+ */
+#ifndef FP_H_
+#define FP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream handle (cudaStream_t); NULL is the legacy stream. */
+typedef struct CUstream_st *fp_stream_t;
+
+typedef enum {
+    FP_OK = 0,
+    /* detected on the host: nothing was enqueued */
+    FP_ERR_INVALID_ARG = -1,      /* null pointer, negative size, inconsistent description */
+    FP_ERR_UNSUPPORTED = -2,      /* outside the limits listed above */
+    FP_ERR_WORKSPACE = -3,        /* workspace smaller than fp_workspace_bytes() */
+    FP_ERR_CUDA = -4,             /* a CUDA runtime call or kernel launch failed */
+    FP_ERR_CAPACITY = -5,         /* CSR index capacity smaller than required */
+    /* detected on the device: recorded in the workspace status word */
+    FP_ERR_DEVICE_PAGE = -16,     /* a page id outside [0, num_pages) was needed */
+    FP_ERR_DEVICE_CSR = -17,      /* CSR segment malformed (ids outside [0, D] or not ascending) */
+    FP_ERR_DEVICE_OVERFLOW = -18, /* selected blocks exceed the CSR index capacity */
+    FP_ERR_DEVICE_TIMEOUT = -19,  /* a bounded pipeline wait expired */
+    FP_ERR_DEVICE_SEQLEN = -20    /* device cu_seqlens differ from host_cu_seqlens */
+} fp_status;
+
+typedef enum { FP_DTYPE_BF16 = 0, FP_DTYPE_E4M3 = 1 } fp_dtype;
+
+/* fp_attention flags */
+#define FP_MEAN_CORRECTION 1 /* add the Eq.6 surrogate of every pruned causal block (off: Eq.4) */
+#define FP_DENSE 2           /* ignore the CSR: every causal block is exact, no correction (alpha = 0) */
+
+/* Description of one attention layer's batch (Alg.1 inputs: packed queries,
+ * paged KV with page table, lengths {(L_b^q, L_b^kv)}). */
+typedef struct {
+    int32_t batch;                  /* number of requests (continuous batching) */
+    int32_t num_q_heads;            /* Hq */
+    int32_t num_kv_heads;           /* Hkv; g = Hq / Hkv (Eq.12) */
+    int32_t head_dim;               /* d, must be 128 */
+    int32_t block_size;             /* B, must be 128 */
+    int32_t page_size;              /* p of Eq.22 */
+    int32_t dtype;                  /* fp_dtype of q, k_pages, v_pages */
+    float c_q, c_k, c_v;            /* per-tensor dequantisation scales (Eq.15); ignored for BF16 */
+    const int32_t *cu_seqlens;      /* device [batch + 1], cu_seqlens[0] = 0, nondecreasing */
+    const int32_t *page_table;      /* device [batch * page_table_stride] */
+    int32_t page_table_stride;      /* entries per request row, >= ceil(max L_b / page_size) */
+    int32_t num_pages;              /* pages in the K/V pool (bounds checks) */
+    const int32_t *host_cu_seqlens; /* host copy of cu_seqlens, read for sizing only */
+} fp_problem;
+
+/* Sizing (host only, no device work, no synchronisation). Each returns a
+ * negative value if the description is invalid or unsupported. */
+
+/* Bytes of device workspace fp_select and fp_attention need (256-byte aligned
+ * base). One workspace may serve both calls of a layer; calls that overlap on
+ * the device must use distinct workspaces. */
+int64_t fp_workspace_bytes(const fp_problem *p);
+
+/* Number of CSR segments: sum_b Hkv * ceil(g * L_b / 128). */
+int64_t fp_num_segments(const fp_problem *p);
+
+/* Rows of the pooled-mean arrays: sum_b ceil(L_b / 128). */
+int64_t fp_num_blocks(const fp_problem *p);
+
+/* Worst-case CSR index entries, sum over segments of (D + 1) where D is the
+ * tile's diagonal block; passing this capacity can never overflow. */
+int64_t fp_csr_capacity(const fp_problem *p);
+
+/* Stage 1 (Alg.1 steps 1-5). Pools K/V block means (Eq.5; FP8 inputs
+ * descaled first), scores every packed 128-row query tile against the pooled
+ * keys of its causal blocks J <= D with logits q.kbar_J / sqrt(d) (Eq.19),
+ * keeps block J iff E_J >= alpha * max_{J' <= D} E_J' or J < sink_blocks or
+ * D - window_blocks <= J < D or J = D (Eq.20), and writes the CSR.
+ *   alpha          >= 0; 0 selects every causal block
+ *   sink_blocks    >= 0 leading blocks always kept
+ *   window_blocks  >= 0 blocks just before the diagonal block always kept
+ *   csr_cu         out [num_segments + 1]
+ *   csr_idx        out [csr_idx_capacity]; entries past csr_cu[num_segments] undefined
+ *   kbar, vbar     out fp32 means; kbar_op, vbar_op out operand-format means
+ *   workspace      device scratch of at least fp_workspace_bytes(p) bytes */
+fp_status fp_select(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages, float alpha,
+                    int32_t sink_blocks, int32_t window_blocks, int32_t *csr_cu, int32_t *csr_idx,
+                    int64_t csr_idx_capacity, float *kbar, float *vbar, void *kbar_op, void *vbar_op,
+                    void *workspace, size_t workspace_bytes, fp_stream_t stream);
+
+/* Stage 2 (Alg.1 steps 6-11). For every segment, walks its selected blocks in
+ * descending order (Eq.17) with exact Q'K^T and PV (token-causal mask on the
+ * diagonal block), then, with FP_MEAN_CORRECTION, one term per pruned block
+ * J < D with logit q.kbar_J / sqrt(d) + ln 128 and value vbar_J (Eq.6, Sec.3.2
+ * "Implementation"), all in one online softmax; the epilogue divides by the
+ * accumulated denominator. FP8 computes S = c_q c_k (Q~K~^T), quantises
+ * P~ = e4m3(256 exp(S - m)) and O = c_v sum P~V~ / sum P~ (Eq.15).
+ *   csr_cu, csr_idx   a CSR in fp_select's format (ignored with FP_DENSE); every
+ *                     segment is checked (ids in [0, D], ascending, within
+ *                     csr_idx_capacity) and a malformed one is skipped and
+ *                     reported as FP_ERR_DEVICE_CSR
+ *   kbar_op, vbar_op  operand-format means from fp_select (ignored without correction)
+ *   out               out [T, Hq, 128] bf16
+ *   lse               out [T, Hq] fp32 natural-log denominator, or NULL */
+fp_status fp_attention(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages,
+                       const int32_t *csr_cu, const int32_t *csr_idx, int64_t csr_idx_capacity,
+                       const void *kbar_op, const void *vbar_op, int32_t flags, void *out, float *lse,
+                       void *workspace, size_t workspace_bytes, fp_stream_t stream);
+
+/* Waits for `stream`, then returns the device-detected error recorded in
+ * `workspace` by the most recent fp_select or fp_attention on it (each call
+ * clears the status word when it starts), FP_OK if none, or FP_ERR_CUDA if
+ * the stream reported an error. */
+fp_status fp_device_status(const void *workspace, fp_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *fp_status_string(fp_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP_H_ */

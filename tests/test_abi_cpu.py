@@ -1,0 +1,103 @@
+"""CPU checks of the C-ABI library: it loads, exports every entry point the
+header declares, sizes problems like the oracle's segment enumeration and
+rejects invalid descriptions on the host (no device work is enqueued for them)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_long_mean_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "fp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_entry_point():
+    names = header_functions()
+    assert set(names) == set(B.EXPORTS), names
+    for n in names:
+        assert hasattr(B.lib, n), n
+        assert callable(getattr(B, n)), n
+
+
+def problem(lengths, hq=32, hkv=4, page=64, dtype="bf16", **kw):
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    stride = max(1, max((L + page - 1) // page for L in lengths) if lengths else 1)
+    pt = torch.zeros(len(lengths), stride, dtype=torch.int32)
+    return B.Problem(torch.from_numpy(cu), cu, pt, hq, hkv, num_pages=1 << 20, page_size=page, dtype=dtype, **kw)
+
+
+@pytest.mark.parametrize("lengths,hq,hkv", [
+    ([131072], 32, 4), ([32768], 32, 8), ([2048], 4, 1), ([300, 0, 129, 4096], 8, 2), ([1], 16, 1), ([], 8, 8),
+])
+def test_sizing_matches_oracle_segments(lengths, hq, hkv):
+    p = problem(lengths, hq, hkv)
+    op = oracle.Problem(q=np.zeros((1, hq, 128), np.uint16), k_pages=np.zeros((1, 64, hkv, 128), np.uint16),
+                        v_pages=np.zeros((1, 64, hkv, 128), np.uint16),
+                        cu_seqlens=np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32),
+                        page_table=np.zeros((max(len(lengths), 1), 1), np.int32), hq=hq, hkv=hkv)
+    seg = oracle.segments(op)
+    assert B.fp_num_segments(p) == len(seg)
+    assert B.fp_num_blocks(p) == seg.total_blocks
+    assert B.fp_csr_capacity(p) == int((seg.D + 1).sum())
+    assert B.fp_workspace_bytes(p) > 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(lengths=[256], hq=12, hkv=4), -2),      # g = 3 is not a power of two
+    (dict(lengths=[256], hq=64, hkv=2), -2),      # g = 32 > 16
+    (dict(lengths=[256], hq=10, hkv=4), -2),      # Hq % Hkv != 0
+    (dict(lengths=[256], page=48), -2),           # page size not a power of two
+    (dict(lengths=[256], page=256), -2),          # page larger than a block
+    (dict(lengths=[(1 << 20) + 128]), -2),        # longer than the supported maximum
+])
+def test_host_rejects_unsupported_descriptions(kw, code):
+    assert B.lib.fp_num_segments(problem(**kw).ref) == code
+
+
+def test_host_rejects_bad_arguments_before_any_device_work():
+    p = problem([256], hq=8, hkv=2)
+    p.c.head_dim = 64
+    assert B.lib.fp_workspace_bytes(p.ref) == -2
+    p = problem([256], hq=8, hkv=2)
+    fake = ctypes.c_void_p(1 << 20)    # never dereferenced: validation fails first
+    need = B.fp_workspace_bytes(p)
+    # workspace too small
+    assert B.lib.fp_select(p.ref, fake, fake, fake, 0.1, 1, 1, fake, fake, 10 ** 6, fake, fake, fake, fake, fake,
+                           need - 1, None) == -3
+    # negative alpha / window, null CSR
+    assert B.lib.fp_select(p.ref, fake, fake, fake, -0.5, 1, 1, fake, fake, 10 ** 6, fake, fake, fake, fake, fake,
+                           need, None) == -1
+    assert B.lib.fp_select(p.ref, fake, fake, fake, 0.1, 1, -1, fake, fake, 10 ** 6, fake, fake, fake, fake, fake,
+                           need, None) == -1
+    assert B.lib.fp_select(p.ref, fake, fake, fake, 0.1, 1, 1, None, fake, 10 ** 6, fake, fake, fake, fake, fake,
+                           need, None) == -1
+    # misaligned workspace
+    assert B.lib.fp_select(p.ref, fake, fake, fake, 0.1, 1, 1, fake, fake, 10 ** 6, fake, fake, fake, fake,
+                           ctypes.c_void_p((1 << 20) + 8), need, None) == -1
+    # unknown flags, missing means with correction on
+    assert B.lib.fp_attention(p.ref, fake, fake, fake, fake, fake, 10, fake, fake, 8, fake, None, fake, need,
+                              None) == -1
+    assert B.lib.fp_attention(p.ref, fake, fake, fake, fake, fake, 10, None, None, 1, fake, None, fake, need,
+                              None) == -1
+    # FP8 without scales
+    p8 = problem([256], hq=8, hkv=2, dtype="e4m3", c_q=0.0, c_k=1.0, c_v=1.0)
+    assert B.lib.fp_workspace_bytes(p8.ref) == -1
+    # device cu_seqlens missing although tokens exist
+    p = problem([256], hq=8, hkv=2)
+    p.c.cu_seqlens = None
+    assert B.lib.fp_num_segments(p.ref) == -1
+
+
+def test_status_strings():
+    for code, name in B.STATUS.items():
+        assert B.fp_status_string(code) and "unknown" not in B.fp_status_string(code), name
