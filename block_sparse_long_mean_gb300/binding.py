@@ -29,7 +29,7 @@ STATUS = {
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTS = ["fp_workspace_bytes", "fp_num_segments", "fp_num_blocks", "fp_csr_capacity", "fp_select",
-           "fp_attention", "fp_device_status", "fp_status_string"]
+           "fp_attention", "fp_device_status", "fp_status_string", "fp_select_noalloc"]
 
 
 class FpError(RuntimeError):
@@ -59,6 +59,8 @@ def _load():
         getattr(L, name).argtypes = [P]
     L.fp_select.restype = ctypes.c_int
     L.fp_select.argtypes = [P, vp, vp, vp, f32, i32, i32, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]
+    L.fp_select_noalloc.restype = ctypes.c_int
+    L.fp_select_noalloc.argtypes = [P, vp, vp, vp, f32, i32, i32, vp, vp, i64, vp, vp, vp, vp, vp, vp]
     L.fp_attention.restype = ctypes.c_int
     L.fp_attention.argtypes = [P, vp, vp, vp, vp, vp, i64, vp, vp, i32, vp, vp, vp, sz, vp]
     L.fp_device_status.restype = ctypes.c_int
@@ -162,6 +164,19 @@ def fp_attention(p: Problem, q, k_pages, v_pages, csr_cu, csr_idx, kbar_op, vbar
                             int(workspace.numel() * workspace.element_size()), _stream(stream))
     if check:
         _check(code, "fp_attention")
+    return code
+
+
+def fp_select_noalloc(p: Problem, q, k_pages, v_pages, alpha: float, sink_blocks: int, window_blocks: int, csr_cu,
+                      csr_idx, kbar, vbar, kbar_op, vbar_op, device_status=None, stream=None,
+                      check: bool = True) -> int:
+    """fp_select using the library's static scratch: for callers that cannot allocate a workspace."""
+    code = lib.fp_select_noalloc(p.ref, _p(q), _p(k_pages), _p(v_pages), float(alpha), int(sink_blocks),
+                                 int(window_blocks), _p(csr_cu), _p(csr_idx),
+                                 int(csr_idx.numel()) if csr_idx is not None else 0, _p(kbar), _p(vbar),
+                                 _p(kbar_op), _p(vbar_op), _p(device_status), _stream(stream))
+    if check:
+        _check(code, "fp_select_noalloc")
     return code
 
 

@@ -12,6 +12,8 @@ bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
+}  // namespace
+
 // Validates the description; fills the sizes from host_cu_seqlens.
 fp_status describe(const fp_problem *p, Sizes *s) {
     if (!p || !p->host_cu_seqlens) return FP_ERR_INVALID_ARG;
@@ -64,6 +66,8 @@ WsLayout layout(const fp_problem *p, const Sizes &s) {
     w.total = o;
     return w;
 }
+
+namespace {
 
 fp_status make_ctx(const fp_problem *p, void *workspace, size_t ws_bytes, fp_stream_t stream, Ctx *c) {
     Sizes s;

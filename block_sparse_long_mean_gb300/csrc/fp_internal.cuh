@@ -123,6 +123,10 @@ template <> struct Elem<FP_DTYPE_E4M3> {
     __device__ __forceinline__ static float to_float(T x) { return float(x); }
 };
 
+// Host sizing shared by the entry points (fp_api.cu).
+fp_status describe(const fp_problem *p, Sizes *s);
+WsLayout layout(const fp_problem *p, const Sizes &s);
+
 // ---------------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_prep(const Ctx &c);

@@ -162,6 +162,29 @@ fp_status fp_attention(const fp_problem *p, const void *q, const void *k_pages, 
                        const void *kbar_op, const void *vbar_op, int32_t flags, void *out, float *lse,
                        void *workspace, size_t workspace_bytes, fp_stream_t stream);
 
+/* fp_select without a caller-provided workspace, for callers that cannot
+ * allocate device memory (for example a plugin that receives only its input
+ * and output tensors, or code on a path where cudaMalloc's implicit
+ * synchronisation is not allowed). The paper has no counterpart: it is a
+ * packaging variant of fp_select that computes the same outputs, bit for bit.
+ * Scratch comes from a fixed 16 MiB device array inside the library, which
+ * every GPU that loads the library holds until the process exits.
+ *   - Problems whose workspace (fp_workspace_bytes) exceeds 16 MiB are
+ *     rejected with FP_ERR_WORKSPACE before anything is enqueued.
+ *   - It calls no allocator. The first call on each device looks up the
+ *     array's device address with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array and it keeps the previous call's contents:
+ *     calls whose work overlaps on the GPU race and must be serialised.
+ *   - device_status (device int32, nullable) receives the call's device
+ *     status code (FP_OK or a device error) when the work completes; the
+ *     workspace-based fp_device_status cannot see this call.
+ * Other arguments are those of fp_select. */
+fp_status fp_select_noalloc(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages,
+                            float alpha, int32_t sink_blocks, int32_t window_blocks, int32_t *csr_cu,
+                            int32_t *csr_idx, int64_t csr_idx_capacity, float *kbar, float *vbar, void *kbar_op,
+                            void *vbar_op, int32_t *device_status, fp_stream_t stream);
+
 /* Waits for `stream`, then returns the device-detected error recorded in
  * `workspace` by the most recent fp_select or fp_attention on it (each call
  * clears the status word when it starts), FP_OK if none, or FP_ERR_CUDA if
