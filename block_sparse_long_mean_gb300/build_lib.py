@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libfp.so")
-SOURCES = ["fp_api.cu", "fp_stage1.cu", "fp_stage2.cu", "fp_noalloc.cu"]
+SOURCES = ["fp_api.cu", "fp_stage1.cu", "fp_score.cu", "fp_stage2.cu", "fp_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

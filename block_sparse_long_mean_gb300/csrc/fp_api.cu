@@ -18,6 +18,7 @@ int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 fp_status describe(const fp_problem *p, Sizes *s) {
     if (!p || !p->host_cu_seqlens) return FP_ERR_INVALID_ARG;
     if (p->batch < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0) return FP_ERR_INVALID_ARG;
+    if (p->num_kv_heads > 64) return FP_ERR_UNSUPPORTED;
     if (p->num_q_heads % p->num_kv_heads) return FP_ERR_UNSUPPORTED;
     int g = p->num_q_heads / p->num_kv_heads;
     if (!is_pow2(g) || g > 16) return FP_ERR_UNSUPPORTED;
@@ -63,8 +64,60 @@ WsLayout layout(const fp_problem *p, const Sizes &s) {
     w.work = o; o = align256(o + 4 * (s.nseg + 1));
     w.hist = o; o = align256(o + 4 * (int64_t)(kMaxBlocks + 2));
     w.counters = o; o = align256(o + 4 * 64);
+    w.kstat = o; o = align256(o + 8 * (s.nblocks * p->num_kv_heads + 1));
     w.total = o;
     return w;
+}
+
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, fetched through the runtime once.
+EncodeTiled encoder() {
+    static EncodeTiled fn = [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            ptr = nullptr;
+        return reinterpret_cast<EncodeTiled>(ptr);
+    }();
+    return fn;
+}
+
+}  // namespace
+
+bool make_tmap(CUtensorMap *map, const void *base, bool u8, int rank, const uint64_t *dims, const uint64_t *strides,
+               const uint32_t *box) {
+    EncodeTiled fn = encoder();
+    if (!fn) {
+        fprintf(stderr, "libfp: cuTensorMapEncodeTiled unavailable\n");
+        return false;
+    }
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = fn(map, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                          const_cast<void *>(base), reinterpret_cast<const cuuint64_t *>(dims),
+                          reinterpret_cast<const cuuint64_t *>(strides), box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) fprintf(stderr, "libfp: cuTensorMapEncodeTiled failed (%d)\n", (int)r);
+    return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cached[dev] = n;
+    }
+    return cached[dev];
 }
 
 namespace {
@@ -140,7 +193,8 @@ fp_status fp_select(const fp_problem *p, const void *q, const void *k_pages, con
     cudaError_t e = cudaMemsetAsync(c.status(), 0, 64 * 4, c.stream);
     if (e == cudaSuccess) e = launch_prep(c);
     if (e == cudaSuccess && c.s.nblocks > 0) e = launch_pool(c, k_pages, v_pages, kbar, vbar, kbar_op, vbar_op);
-    if (e == cudaSuccess && c.s.nseg > 0) e = launch_score(c, q, kbar, alpha, sink_blocks, window_blocks);
+    if (e == cudaSuccess && c.s.nseg > 0)
+        e = launch_score(c, q, kbar, kbar_op, alpha, sink_blocks, window_blocks);
     if (e == cudaSuccess) e = launch_csr(c, csr_cu, csr_idx, csr_idx_capacity);
     return launched(e);
 }

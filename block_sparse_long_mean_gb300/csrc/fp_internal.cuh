@@ -2,6 +2,7 @@
 // helpers and the launchers each translation unit provides to fp_api.cu.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -35,7 +36,7 @@ enum StatusSlot { kStatusCode = 0, kStatusDetail = 1 };
 
 // Byte offsets of the workspace regions, derived on the host from the sizes.
 struct WsLayout {
-    int64_t status, req, seg_count, mask, work, hist, counters, total;
+    int64_t status, req, seg_count, mask, work, hist, counters, kstat, total;
 };
 
 struct Sizes {
@@ -57,6 +58,8 @@ struct Ctx {
     int32_t *work() const { return reinterpret_cast<int32_t *>(wsbase + ws.work); }
     int32_t *hist() const { return reinterpret_cast<int32_t *>(wsbase + ws.hist); }
     int32_t *counters() const { return reinterpret_cast<int32_t *>(wsbase + ws.counters); }
+    // per (pooled block, KV head): {|kbar - operand-format kbar|_2, |kbar|_2}
+    float2 *kstat() const { return reinterpret_cast<float2 *>(wsbase + ws.kstat); }
 };
 
 // ----------------------------------------------------------------- device helpers
@@ -123,6 +126,15 @@ template <> struct Elem<FP_DTYPE_E4M3> {
     __device__ __forceinline__ static float to_float(T x) { return float(x); }
 };
 
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// Encodes a tiled TMA descriptor with 128-byte swizzling over a row-major
+// tensor: dims innermost first, strides in bytes for dims 1..rank-1, box in
+// elements. Element type bf16, or 8-bit when u8. Returns false on failure.
+bool make_tmap(CUtensorMap *map, const void *base, bool u8, int rank, const uint64_t *dims, const uint64_t *strides,
+               const uint32_t *box);
+
 // Host sizing shared by the entry points (fp_api.cu).
 fp_status describe(const fp_problem *p, Sizes *s);
 WsLayout layout(const fp_problem *p, const Sizes &s);
@@ -132,7 +144,8 @@ WsLayout layout(const fp_problem *p, const Sizes &s);
 cudaError_t launch_prep(const Ctx &c);
 cudaError_t launch_pool(const Ctx &c, const void *k_pages, const void *v_pages, float *kbar, float *vbar,
                         void *kbar_op, void *vbar_op);
-cudaError_t launch_score(const Ctx &c, const void *q, const float *kbar, float alpha, int sink, int window);
+cudaError_t launch_score(const Ctx &c, const void *q, const float *kbar, const void *kbar_op, float alpha, int sink,
+                         int window);
 cudaError_t launch_csr(const Ctx &c, int32_t *csr_cu, int32_t *csr_idx, int64_t capacity);
 cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, const void *v_pages,
                              const int32_t *csr_cu, const int32_t *csr_idx, int64_t capacity, const void *kbar_op,

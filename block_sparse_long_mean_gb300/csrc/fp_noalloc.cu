@@ -95,7 +95,7 @@ extern "C" fp_status fp_select_noalloc(const fp_problem *p, const void *q, const
     cudaError_t e = cudaMemsetAsync(c.status(), 0, 64 * 4, c.stream);
     if (e == cudaSuccess) e = launch_prep(c);
     if (e == cudaSuccess && s.nblocks > 0) e = launch_pool(c, k_pages, v_pages, kbar, vbar, kbar_op, vbar_op);
-    if (e == cudaSuccess && s.nseg > 0) e = launch_score(c, q, kbar, alpha, sink_blocks, window_blocks);
+    if (e == cudaSuccess && s.nseg > 0) e = launch_score(c, q, kbar, kbar_op, alpha, sink_blocks, window_blocks);
     if (e == cudaSuccess) e = launch_csr(c, csr_cu, csr_idx, csr_idx_capacity);
     if (e == cudaSuccess && device_status)
         e = cudaMemcpyAsync(device_status, c.status(), sizeof(int32_t), cudaMemcpyDeviceToDevice, c.stream);

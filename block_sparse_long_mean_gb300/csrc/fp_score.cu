@@ -1,0 +1,475 @@
+// Stage 1 scoring + selection on the tensor cores (FlashPrefill V2 Sec.3.3
+// "Single-Pass Score and Selection", Eq.19-20; Sec.3.1 Eq.1-3).
+//
+// One persistent CTA per SM walks the packed query tiles. For a tile of
+// (request b, KV head h, tile t) with diagonal block D it computes, chunk by
+// chunk of 128 pooled keys, S[J][r] = kbar_J . q_r on tcgen05 (pooled keys on
+// the 128 TMEM lanes, the tile's 128 packed rows on 128 columns), so each
+// reduction thread owns one block J and reduces its row of S without any
+// cross-thread traffic:
+//     lE_J = ln sum_r exp(s_rJ),   s_rJ = kbar_J . q_r / sqrt(d)
+// (Eq.19's E_J up to the common factor exp(-M), which cancels in Eq.20).
+// Block J is kept iff lE_J >= ln(alpha) + max_J' lE_J' or J is forced.
+//
+// Exactness. The tensor core sees kbar rounded to the operand format (bf16 or
+// e4m3). Per (block, head) the pooling kernel records |kbar - kbar_op|_2 and
+// |kbar|_2, so |s_rJ(screen) - s_rJ(exact)| <= eps_J = max_r |q_r| (|kbar -
+// kbar_op| + 2^-12 |kbar|) / sqrt(d) + 2e-4 (Cauchy-Schwarz; the second term
+// covers fp32 accumulation and the exp/log approximations), hence
+// |lE_J(screen) - lE_J| <= eps_J. Every block whose decision (or whose claim
+// to the maximum) is not settled by these bounds is recomputed in fp32 from
+// the fp32 means, so the CSR matches an exact evaluation except for blocks
+// within fp32 rounding of the threshold.
+//
+// Exp work is skipped for blocks that cannot matter: chunks run from the
+// diagonal block down, and a block whose upper bound
+// max_r s_rJ + ln(rows) + eps_J lies below ln(alpha) + (a proven lower bound of
+// the maximum) is certainly pruned and certainly not the maximum.
+#include <math.h>
+
+#include "fp_internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace fp {
+namespace {
+
+using namespace sm100;
+
+constexpr int kSWarps = 6;  // warp 0: TMA, warp 1: MMA + TMEM, warps 2-5: reduction / selection
+constexpr int kSThreads = 32 * kSWarps;
+constexpr int kSStages = 3;  // pooled-key chunk stages
+constexpr int kRedThreads = 128;
+constexpr int kRefineList = 256;
+
+enum ScoreMode { kModeScore = 0, kModeAll = 1, kModeForced = 2 };
+
+template <int kDtype>
+struct SCfg {
+    static constexpr int kEb = Elem<kDtype>::kBytes;
+    static constexpr int kTile = 128 * 128 * kEb;  // bytes of a Q tile or of a chunk of 128 pooled keys
+    static constexpr int kKStep = 32 / kEb;         // K elements per MMA (32 bytes)
+    static constexpr int kNumK = 128 / kKStep;      // MMAs per chunk
+    static constexpr int kBoxElems = 128 / kEb;     // elements per 128-byte TMA box row
+    static constexpr int kBoxes = 128 / kBoxElems;  // boxes along d
+    static constexpr uint32_t kIdesc =
+        instr_desc(kDtype == FP_DTYPE_BF16 ? 1u : 0u, kDtype == FP_DTYPE_BF16 ? 1u : 0u, false, false, 128, 128);
+};
+
+template <int kDtype>
+struct ScoreSmem {
+    alignas(1024) uint8_t q[2][SCfg<kDtype>::kTile];
+    alignas(1024) uint8_t k[kSStages][SCfg<kDtype>::kTile];
+    float lE[kMaxBlocks];       // screened log-energy, upper bound, or refined value
+    uint8_t state[kMaxBlocks];  // see kSt* below
+    int32_t list[kRefineList];
+    uint64_t q_full[2], q_empty[2], k_full[kSStages], k_empty[kSStages], s_full[2], s_empty[2];
+    uint32_t tmem_base;
+    int abort;
+    float red[2][4];
+    int ired[4];
+    int nlist;
+    int any;
+};
+
+// state bits
+constexpr uint8_t kStSkipped = 1;    // lE holds an upper bound (eps included), no screened value
+constexpr uint8_t kStUncertain = 2;  // decision not settled by the bounds
+constexpr uint8_t kStMaxCand = 4;    // may hold the maximum
+constexpr uint8_t kStRefined = 8;    // lE is the fp32 recomputation
+constexpr uint8_t kStSelected = 0x80;
+
+__device__ __forceinline__ void red_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ float warp_max(float v) {
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Max over the 128 reduction threads (warps 2-5); slot selects the smem buffer.
+template <typename S>
+__device__ __forceinline__ float red_max(S &sm, float v, int slot) {
+    v = warp_max(v);
+    const int w = (threadIdx.x >> 5) - 2;
+    if ((threadIdx.x & 31) == 0) sm.red[slot][w] = v;
+    red_bar();
+    const float r = fmaxf(fmaxf(sm.red[slot][0], sm.red[slot][1]), fmaxf(sm.red[slot][2], sm.red[slot][3]));
+    return r;
+}
+template <typename S>
+__device__ __forceinline__ float red_sum(S &sm, float v, int slot) {
+    v = warp_sum(v);
+    const int w = (threadIdx.x >> 5) - 2;
+    if ((threadIdx.x & 31) == 0) sm.red[slot][w] = v;
+    red_bar();
+    return (sm.red[slot][0] + sm.red[slot][1]) + (sm.red[slot][2] + sm.red[slot][3]);
+}
+
+// Element (row r, column c) of a 128x128 tile stored by TMA with 128-byte swizzling.
+template <int kDtype>
+__device__ __forceinline__ float q_elem(const uint8_t *tile, int r, int c) {
+    if (kDtype == FP_DTYPE_BF16) {
+        const int off = (c >> 6) * 16384 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + ((c & 7) << 1);
+        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off));
+    } else {
+        const int off = r * 128 + (((c >> 4) ^ (r & 7)) << 4) + (c & 15);
+        return float(*reinterpret_cast<const __nv_fp8_e4m3 *>(tile + off));
+    }
+}
+
+template <int kDtype>
+__global__ void __launch_bounds__(kSThreads, 1)
+    score_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const float *__restrict__ kbar, const float2 *__restrict__ kstat,
+                    const ReqInfo *__restrict__ req, int batch, int hkv, int g, int mode, float log_alpha, int sink,
+                    int window, float qscale, float kscale, int32_t nseg, int32_t *__restrict__ seg_count,
+                    uint32_t *__restrict__ mask, int32_t *__restrict__ status) {
+    using C = SCfg<kDtype>;
+    extern __shared__ uint8_t smem_raw[];
+    ScoreSmem<kDtype> &sm = *reinterpret_cast<ScoreSmem<kDtype> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (status_bad(status)) return;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.q_full[i], 1);
+            mbar_init(&sm.q_empty[i], 2);  // MMA commit + reduction warps done with Q
+            mbar_init(&sm.s_full[i], 1);
+            mbar_init(&sm.s_empty[i], 4);  // one arrival per reduction warp
+        }
+        for (int i = 0; i < kSStages; ++i) {
+            mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.k_empty[i], 1);
+        }
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(&sm.tmem_base, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const Abort ab{&sm.abort};
+    const uint32_t tmem = sm.tmem_base;
+    const bool scoring = mode == kModeScore;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && scoring) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            uint32_t tile_it = 0, chunk_it = 0;
+            for (int w = blockIdx.x; w < nseg; w += gridDim.x, ++tile_it) {
+                const SegCoord sc = decode_seg(req, batch, g, nseg - 1 - w);
+                const ReqInfo r = req[sc.b];
+                const int qb = tile_it & 1;
+                if (!mbar_wait(&sm.q_empty[qb], ((tile_it >> 1) & 1) ^ 1, ab)) break;
+                mbar_arrive_expect_tx(&sm.q_full[qb], C::kTile);
+                const int pos0 = r.q_start + (sc.t * kTileRows) / g;
+                for (int i = 0; i < C::kBoxes; ++i)
+                    tma_load_4d(sm.q[qb] + i * 16384, &tm_q, &sm.q_full[qb], i * C::kBoxElems, 0, sc.h, pos0);
+                const int nch = sc.D / 128 + 1;
+                bool ok = true;
+                for (int cc = 0; cc < nch && ok; ++cc, ++chunk_it) {
+                    const int c = nch - 1 - cc;
+                    const int st = chunk_it % kSStages;
+                    if (!(ok = mbar_wait(&sm.k_empty[st], ((chunk_it / kSStages) & 1) ^ 1, ab))) break;
+                    mbar_arrive_expect_tx(&sm.k_full[st], C::kTile);
+                    for (int i = 0; i < C::kBoxes; ++i)
+                        tma_load_3d(sm.k[st] + i * 16384, &tm_k, &sm.k_full[st], i * C::kBoxElems, sc.h,
+                                    r.blk_base + 128 * c);
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------------------- MMA issue
+        if (lane == 0 && scoring) {
+            uint32_t tile_it = 0, chunk_it = 0;
+            for (int w = blockIdx.x; w < nseg; w += gridDim.x, ++tile_it) {
+                const SegCoord sc = decode_seg(req, batch, g, nseg - 1 - w);
+                const int qb = tile_it & 1;
+                if (!mbar_wait(&sm.q_full[qb], (tile_it >> 1) & 1, ab)) break;
+                const int nch = sc.D / 128 + 1;
+                bool ok = true;
+                for (int cc = 0; cc < nch; ++cc, ++chunk_it) {
+                    const int st = chunk_it % kSStages;
+                    const int sb = chunk_it & 1;
+                    if (!(ok = mbar_wait(&sm.k_full[st], (chunk_it / kSStages) & 1, ab))) break;
+                    if (!(ok = mbar_wait(&sm.s_empty[sb], ((chunk_it >> 1) & 1) ^ 1, ab))) break;
+                    tc_fence_after();
+                    const uint32_t abase = smem_addr(sm.k[st]), bbase = smem_addr(sm.q[qb]);
+#pragma unroll
+                    for (int k = 0; k < C::kNumK; ++k) {
+                        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                        const uint64_t ad = sw128_desc(abase + off, 16, 1024);
+                        const uint64_t bd = sw128_desc(bbase + off, 16, 1024);
+                        if (kDtype == FP_DTYPE_BF16)
+                            umma_f16_ss(tmem + sb * 128, ad, bd, C::kIdesc, k > 0);
+                        else
+                            umma_f8_ss(tmem + sb * 128, ad, bd, C::kIdesc, k > 0);
+                    }
+                    umma_commit(&sm.k_empty[st]);
+                    umma_commit(&sm.s_full[sb]);
+                }
+                if (!ok) break;
+                umma_commit(&sm.q_empty[qb]);
+            }
+        }
+    } else {
+        // --------------------------------------------------- reduction / selection
+        const int rt = threadIdx.x - 64;              // 0..127 across warps 2-5
+        const int j = 32 * (warp & 3) + lane;         // TMEM lane = block in chunk = tile row
+        const uint32_t tlane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        const float inv_sqrt_d = rsqrtf((float)kHeadDim);
+        const float scale = qscale * kscale * inv_sqrt_d;  // raw MMA dot -> logit
+        const float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
+        uint32_t tile_it = 0, chunk_it = 0;
+        for (int w = blockIdx.x; w < nseg; w += gridDim.x, ++tile_it) {
+            const int seg = nseg - 1 - w;
+            const SegCoord sc = decode_seg(req, batch, g, seg);
+            const ReqInfo r = req[sc.b];
+            const int D = sc.D, rows = sc.rows;
+            const int qb = tile_it & 1;
+            const int nch = D / 128 + 1;
+            bool ok = true;
+            float qmax = 0.f;
+            if (scoring) {
+                if (!(ok = mbar_wait(&sm.q_full[qb], (tile_it >> 1) & 1, ab))) break;
+                float n2 = 0.f;
+                if (j < rows)
+                    for (int c = 0; c < kHeadDim; ++c) {
+                        const float x = q_elem<kDtype>(sm.q[qb], j, c) * qscale;
+                        n2 = fmaf(x, x, n2);
+                    }
+                qmax = sqrtf(red_max(sm, n2, 0));
+                float m_run = -INFINITY;  // proven lower bound of max_J lE_J
+                for (int cc = 0; cc < nch; ++cc, ++chunk_it) {
+                    const int c = nch - 1 - cc;
+                    const int sb = chunk_it & 1;
+                    if (!(ok = mbar_wait(&sm.s_full[sb], (chunk_it >> 1) & 1, ab))) break;
+                    tc_fence_after();
+                    float v[128];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t raw[32];
+                        tmem_ld32(tmem + tlane + sb * 128 + q4 * 32, raw);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) v[q4 * 32 + x] = __uint_as_float(raw[x]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
+                    const int J = 128 * c + j;
+                    const bool valid = J <= D;
+                    float m = -INFINITY;
+#pragma unroll
+                    for (int x = 0; x < 128; ++x) m = fmaxf(m, x < rows ? v[x] : -INFINITY);
+                    float eps = 0.f;
+                    if (valid) {
+                        const float2 ks = kstat[(int64_t)(r.blk_base + J) * hkv + sc.h];
+                        eps = qmax * (ks.x + 2.44140625e-4f * ks.y) * inv_sqrt_d + 2e-4f;
+                    }
+                    const float ms = m * scale;
+                    const float lo = valid ? ms - eps : -INFINITY;
+                    m_run = fmaxf(m_run, red_max(sm, lo, (cc & 1)));
+                    if (valid) {
+                        const float hi = ms + logf((float)rows) + eps;
+                        if (hi >= log_alpha + m_run) {
+                            const float k2 = scale * LOG2E;
+                            float s = 0.f;
+#pragma unroll
+                            for (int x = 0; x < 128; ++x)
+                                if (x < rows) s += exp2f((v[x] - m) * k2);
+                            sm.lE[J] = ms + log2f(s) * LN2;
+                            sm.state[J] = 0;
+                        } else {
+                            sm.lE[J] = hi;
+                            sm.state[J] = kStSkipped;
+                        }
+                    }
+                }
+                if (!ok) break;
+            }
+            red_bar();
+            {
+                // ---------------------------------------------------- selection
+                int cnt = 0;
+                if (mode == kModeAll || mode == kModeForced) {
+                    for (int J = rt; J <= D; J += kRedThreads) {
+                        const bool forced = J < sink || (J >= D - window && J < D) || J == D;
+                        sm.state[J] = (mode == kModeAll || forced) ? kStSelected : 0;
+                    }
+                } else {
+                    auto eps_of = [&](int J) {
+                        const float2 ks = kstat[(int64_t)(r.blk_base + J) * hkv + sc.h];
+                        return qmax * (ks.x + 2.44140625e-4f * ks.y) * inv_sqrt_d + 2e-4f;
+                    };
+                    float mlo = -INFINITY, mhi = -INFINITY;
+                    for (int J = rt; J <= D; J += kRedThreads) {
+                        const uint8_t st = sm.state[J];
+                        const float e = eps_of(J);
+                        const float lo = (st & kStSkipped) ? -INFINITY : sm.lE[J] - e;
+                        const float hi = (st & kStSkipped) ? sm.lE[J] : sm.lE[J] + e;
+                        mlo = fmaxf(mlo, lo);
+                        mhi = fmaxf(mhi, hi);
+                    }
+                    mlo = red_max(sm, mlo, 0);
+                    mhi = red_max(sm, mhi, 1);
+                    const float thr_lo = log_alpha + mlo, thr_hi = log_alpha + mhi;
+                    if (rt == 0) sm.any = 0;
+                    red_bar();
+                    int any = 0;
+                    for (int J = rt; J <= D; J += kRedThreads) {
+                        const uint8_t st = sm.state[J];
+                        const float e = eps_of(J);
+                        const float lo = (st & kStSkipped) ? -INFINITY : sm.lE[J] - e;
+                        const float hi = (st & kStSkipped) ? sm.lE[J] : sm.lE[J] + e;
+                        const bool forced = J < sink || (J >= D - window && J < D) || J == D;
+                        uint8_t ns = st;
+                        if (forced || lo >= thr_hi) ns |= kStSelected;
+                        else if (!(hi < thr_lo)) { ns |= kStUncertain; any = 1; }
+                        if (hi >= mlo) ns |= kStMaxCand;
+                        sm.state[J] = ns;
+                    }
+                    if (any) sm.any = 1;
+                    red_bar();
+                    if (sm.any) {
+                        // fp32 recomputation of every max candidate and every unsettled block
+                        float qr[kHeadDim];
+#pragma unroll
+                        for (int c = 0; c < kHeadDim; ++c) qr[c] = j < rows ? q_elem<kDtype>(sm.q[qb], j, c) * qscale : 0.f;
+                        for (;;) {
+                            if (rt == 0) sm.nlist = 0;
+                            red_bar();
+                            // collect up to kRefineList pending candidates with J >= start, in order
+                            for (int J0 = 0; J0 <= D; J0 += kRedThreads) {
+                                const int J = J0 + rt;
+                                const bool need = J <= D && (sm.state[J] & (kStUncertain | kStMaxCand)) &&
+                                                  !(sm.state[J] & kStRefined);
+                                const unsigned bal = __ballot_sync(0xffffffffu, need);
+                                int base = 0;
+                                if (lane == 0 && bal) base = atomicAdd(&sm.nlist, __popc(bal));
+                                base = __shfl_sync(0xffffffffu, base, 0);
+                                if (need) {
+                                    const int slot = base + __popc(bal & ((1u << lane) - 1u));
+                                    if (slot < kRefineList) sm.list[slot] = J;
+                                }
+                                red_bar();
+                                if (sm.nlist >= kRefineList) break;
+                            }
+                            const int n = min(sm.nlist, kRefineList);
+                            if (n == 0) break;
+                            for (int i = 0; i < n; ++i) {
+                                const int J = sm.list[i];
+                                const float *kb = kbar + ((int64_t)(r.blk_base + J) * hkv + sc.h) * kHeadDim;
+                                float dot = 0.f;
+#pragma unroll
+                                for (int c = 0; c < kHeadDim; c += 4) {
+                                    const float4 k4 = __ldg(reinterpret_cast<const float4 *>(kb + c));
+                                    dot = fmaf(qr[c], k4.x, dot);
+                                    dot = fmaf(qr[c + 1], k4.y, dot);
+                                    dot = fmaf(qr[c + 2], k4.z, dot);
+                                    dot = fmaf(qr[c + 3], k4.w, dot);
+                                }
+                                const float s = j < rows ? dot * inv_sqrt_d : -INFINITY;
+                                const float mx = red_max(sm, s, 0);
+                                const float e = j < rows ? expf(s - mx) : 0.f;
+                                const float sum = red_sum(sm, e, 1);
+                                if (rt == 0) {
+                                    sm.lE[J] = mx + logf(sum);
+                                    sm.state[J] = (sm.state[J] & ~kStSkipped) | kStRefined;
+                                }
+                                red_bar();
+                            }
+                            red_bar();
+                        }
+                        float mex = -INFINITY;
+                        for (int J = rt; J <= D; J += kRedThreads)
+                            if (sm.state[J] & kStMaxCand) mex = fmaxf(mex, sm.lE[J]);
+                        mex = red_max(sm, mex, 0);
+                        const float thr = log_alpha + mex;
+                        for (int J = rt; J <= D; J += kRedThreads) {
+                            const uint8_t st = sm.state[J];
+                            if ((st & kStUncertain) && sm.lE[J] >= thr) sm.state[J] = st | kStSelected;
+                        }
+                    }
+                }
+                red_bar();
+                const int64_t wbase = (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
+                for (int wd = rt; wd < r.words; wd += kRedThreads) {
+                    uint32_t bits = 0;
+                    for (int k = 0; k < 32; ++k) {
+                        const int J = 32 * wd + k;
+                        if (J > D) break;
+                        if (sm.state[J] & kStSelected) bits |= 1u << k;
+                    }
+                    mask[wbase + wd] = bits;
+                    cnt += __popc(bits);
+                }
+                cnt = (int)red_sum(sm, (float)cnt, 0);
+                if (rt == 0) seg_count[seg] = cnt;
+                red_bar();
+                if (scoring && rt == 0) mbar_arrive(&sm.q_empty[qb]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (sm.abort && threadIdx.x == 0) set_status(status, FP_ERR_DEVICE_TIMEOUT, blockIdx.x);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_score(const Ctx &c, const void *q, const float *kbar, const void *kbar_op, float alpha, int sink,
+                         int window) {
+    const int mode = alpha == 0.f ? kModeAll : (alpha > 1.f ? kModeForced : kModeScore);
+    const float log_alpha = alpha > 0.f ? logf(alpha) : -INFINITY;
+    const bool fp8 = c.p.dtype == FP_DTYPE_E4M3;
+    const int eb = fp8 ? 1 : 2;
+    const int g = c.s.g, hkv = c.p.num_kv_heads, hq = c.p.num_q_heads;
+    CUtensorMap tm_q, tm_k;
+    {
+        const uint64_t dims[4] = {128, (uint64_t)g, (uint64_t)hkv, (uint64_t)c.s.total_tokens};
+        const uint64_t strides[3] = {(uint64_t)128 * eb, (uint64_t)g * 128 * eb, (uint64_t)hq * 128 * eb};
+        const uint32_t box[4] = {(uint32_t)(128 / eb), (uint32_t)g, 1, (uint32_t)(kTileRows / g)};
+        if (!make_tmap(&tm_q, q, fp8, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t dims[3] = {128, (uint64_t)hkv, (uint64_t)c.s.nblocks};
+        const uint64_t strides[2] = {(uint64_t)128 * eb, (uint64_t)hkv * 128 * eb};
+        const uint32_t box[3] = {(uint32_t)(128 / eb), 1, 128};
+        if (!make_tmap(&tm_k, kbar_op, fp8, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    const int grid = (int)(c.s.nseg < num_sms() ? c.s.nseg : num_sms());
+    cudaError_t e;
+    if (fp8) {
+        const size_t smem = sizeof(ScoreSmem<FP_DTYPE_E4M3>) + 1024;
+        e = cudaFuncSetAttribute(score_tc_kernel<FP_DTYPE_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        score_tc_kernel<FP_DTYPE_E4M3><<<grid, kSThreads, smem, c.stream>>>(
+            tm_q, tm_k, kbar, c.kstat(), c.req(), c.p.batch, hkv, g, mode, log_alpha, sink, window, c.p.c_q,
+            c.p.c_k, (int32_t)c.s.nseg, c.seg_count(), c.mask(), c.status());
+    } else {
+        const size_t smem = sizeof(ScoreSmem<FP_DTYPE_BF16>) + 1024;
+        e = cudaFuncSetAttribute(score_tc_kernel<FP_DTYPE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        score_tc_kernel<FP_DTYPE_BF16><<<grid, kSThreads, smem, c.stream>>>(
+            tm_q, tm_k, kbar, c.kstat(), c.req(), c.p.batch, hkv, g, mode, log_alpha, sink, window, 1.f, 1.f,
+            (int32_t)c.s.nseg, c.seg_count(), c.mask(), c.status());
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace fp

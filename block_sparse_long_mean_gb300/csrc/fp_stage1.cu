@@ -120,12 +120,14 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ k
                                                    int batch, int hkv, float c_k, float c_v,
                                                    float *__restrict__ kbar, float *__restrict__ vbar,
                                                    void *__restrict__ kbar_op, void *__restrict__ vbar_op,
-                                                   int32_t *__restrict__ status) {
+                                                   float2 *__restrict__ kstat, int32_t *__restrict__ status) {
     using E = Elem<kDtype>;
     constexpr int kEb = E::kBytes;
     constexpr int kEpv = 16 / kEb;  // elements per 16-byte vector
     __shared__ float red[2][256 * kEpv];
+    __shared__ float kst[2][64];  // per KV head: squared rounding error and squared norm of kbar
     if (status_bad(status)) return;
+    if (threadIdx.x < 64) kst[0][threadIdx.x] = kst[1][threadIdx.x] = 0.f;
     const int gb = blockIdx.x;
     const int b = find_req_by_block(req, batch, gb);
     const ReqInfo r = req[b];
@@ -183,124 +185,26 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ k
             const int64_t oi = (int64_t)gb * hkv * kHeadDim + (int64_t)colx * kEpv + e;
             kbar[oi] = mk;
             vbar[oi] = mv;
+            float kq;  // the operand-format value as the tensor core sees it, in real units
             if (kDtype == FP_DTYPE_E4M3) {
-                reinterpret_cast<__nv_fp8_e4m3 *>(kbar_op)[oi] = __nv_fp8_e4m3(mk / c_k);
+                const __nv_fp8_e4m3 k8(mk / c_k);
+                reinterpret_cast<__nv_fp8_e4m3 *>(kbar_op)[oi] = k8;
                 reinterpret_cast<__nv_fp8_e4m3 *>(vbar_op)[oi] = __nv_fp8_e4m3(mv / c_v);
+                kq = float(k8) * c_k;
             } else {
-                reinterpret_cast<__nv_bfloat16 *>(kbar_op)[oi] = __float2bfloat16_rn(mk);
+                const __nv_bfloat16 k16 = __float2bfloat16_rn(mk);
+                reinterpret_cast<__nv_bfloat16 *>(kbar_op)[oi] = k16;
                 reinterpret_cast<__nv_bfloat16 *>(vbar_op)[oi] = __float2bfloat16_rn(mv);
+                kq = __bfloat162float(k16);
             }
+            const int head = (colx * kEpv + e) / kHeadDim;
+            atomicAdd(&kst[0][head], (mk - kq) * (mk - kq));
+            atomicAdd(&kst[1][head], mk * mk);
         }
         __syncthreads();
     }
-}
-
-// ---------------------------------------------------------------- score kernel
-
-// One CTA per segment (request b, KV head h, packed tile t), 128 threads.
-// Thread i owns block J = 128 c + i of chunk c and reduces its logits
-// s_rJ = q_r . kbar_J / sqrt(d) over the tile's rows r into the log-energy
-// lE_J = ln sum_r exp(s_rJ) with an online max (Eq.19 up to the common
-// factor exp(-M), which cancels in Eq.20). Selection (Eq.20):
-//   J kept  <=>  lE_J >= ln(alpha) + max_J' lE_J'  or J forced.
-// The result is a bitmask over J in [0, D] and the segment's count.
-constexpr int kScoreThreads = 128;
-constexpr int kKPad = kHeadDim + 1;
-constexpr size_t kScoreSmem = sizeof(float) * (kTileRows * kHeadDim + 128 * kKPad + kMaxBlocks);
-
-template <int kDtype>
-__global__ void __launch_bounds__(kScoreThreads) score_kernel(
-    const typename Elem<kDtype>::T *__restrict__ q, const float *__restrict__ kbar, const ReqInfo *__restrict__ req,
-    int batch, int hq, int hkv, int g, float log_alpha, int sink, int window, float c_q, int32_t nseg,
-    int32_t *__restrict__ seg_count, uint32_t *__restrict__ mask, int32_t *__restrict__ status) {
-    using E = Elem<kDtype>;
-    extern __shared__ float smem[];
-    float *qs = smem;                          // [128][128]
-    float *ks = qs + kTileRows * kHeadDim;     // [128][129]
-    float *lE = ks + 128 * kKPad;              // [kMaxBlocks]
-    __shared__ float red[kScoreThreads / 32];
-    __shared__ int cnt_red[kScoreThreads / 32];
-    if (status_bad(status)) return;
-    const int seg = nseg - 1 - blockIdx.x;  // heavier tiles (larger t) first
-    const SegCoord sc = decode_seg(req, batch, g, seg);
-    const ReqInfo r = req[sc.b];
-    const int r0 = sc.t * kTileRows;
-    const float qscale = kDtype == FP_DTYPE_E4M3 ? c_q : 1.f;
-    for (int e = threadIdx.x; e < kTileRows * kHeadDim; e += kScoreThreads) {
-        const int row = e / kHeadDim, c = e % kHeadDim;
-        float v = 0.f;
-        if (row < sc.rows) {
-            const int gr = r0 + row;
-            const int pos = gr / g, head = sc.h * g + gr % g;
-            v = E::to_float(q[((int64_t)(r.q_start + pos) * hq + head) * kHeadDim + c]) * qscale;
-        }
-        qs[e] = v;
-    }
-    const float inv_sqrt_d = 1.f / sqrtf((float)kHeadDim);
-    for (int c0 = 0; c0 <= sc.D; c0 += 128) {
-        __syncthreads();
-        for (int e = threadIdx.x; e < 128 * kHeadDim; e += kScoreThreads) {
-            const int i = e / kHeadDim, c = e % kHeadDim;
-            const int J = c0 + i;
-            ks[i * kKPad + c] = J <= sc.D ? kbar[((int64_t)(r.blk_base + J) * hkv + sc.h) * kHeadDim + c] : 0.f;
-        }
-        __syncthreads();
-        const int J = c0 + threadIdx.x;
-        if (J <= sc.D) {
-            const float *kr = ks + threadIdx.x * kKPad;
-            float m = -INFINITY, l = 0.f;
-            for (int row = 0; row < sc.rows; row += 4) {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int c = 0; c < kHeadDim; ++c) {
-                    const float kv = kr[c];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) acc[u] = fmaf(qs[(row + u) * kHeadDim + c], kv, acc[u]);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    if (row + u >= sc.rows) break;
-                    const float s = acc[u] * inv_sqrt_d;
-                    if (s > m) {
-                        l = l * expf(m - s) + 1.f;
-                        m = s;
-                    } else {
-                        l += expf(s - m);
-                    }
-                }
-            }
-            lE[J] = m + logf(l);
-        }
-    }
-    __syncthreads();
-    float mx = -INFINITY;
-    for (int J = threadIdx.x; J <= sc.D; J += kScoreThreads) mx = fmaxf(mx, lE[J]);
-    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-    __syncthreads();
-    mx = red[0];
-    for (int w = 1; w < kScoreThreads / 32; ++w) mx = fmaxf(mx, red[w]);
-    const float thr = log_alpha + mx;
-    const int64_t wbase = (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
-    int cnt = 0;
-    for (int w = threadIdx.x; w < r.words; w += kScoreThreads) {
-        uint32_t bits = 0;
-        for (int k = 0; k < 32; ++k) {
-            const int J = 32 * w + k;
-            if (J > sc.D) break;
-            const bool forced = J < sink || (J >= sc.D - window && J < sc.D) || J == sc.D;
-            if (forced || lE[J] >= thr) bits |= 1u << k;
-        }
-        mask[wbase + w] = bits;
-        cnt += __popc(bits);
-    }
-    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if ((threadIdx.x & 31) == 0) cnt_red[threadIdx.x >> 5] = cnt;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int tot = 0;
-        for (int w = 0; w < kScoreThreads / 32; ++w) tot += cnt_red[w];
-        seg_count[seg] = tot;
-    }
+    if (threadIdx.x < hkv)
+        kstat[(int64_t)gb * hkv + threadIdx.x] = make_float2(sqrtf(kst[0][threadIdx.x]), sqrtf(kst[1][threadIdx.x]));
 }
 
 // ------------------------------------------------------------------ CSR kernels
@@ -385,34 +289,12 @@ cudaError_t launch_pool(const Ctx &c, const void *k_pages, const void *v_pages, 
         pool_kernel<FP_DTYPE_E4M3><<<grid, 256, 0, c.stream>>>(
             (const uint8_t *)k_pages, (const uint8_t *)v_pages, c.p.page_table, c.p.page_table_stride,
             c.p.num_pages, c.p.page_size, c.req(), c.p.batch, c.p.num_kv_heads, c.p.c_k, c.p.c_v, kbar, vbar,
-            kbar_op, vbar_op, c.status());
+            kbar_op, vbar_op, c.kstat(), c.status());
     else
         pool_kernel<FP_DTYPE_BF16><<<grid, 256, 0, c.stream>>>(
             (const uint8_t *)k_pages, (const uint8_t *)v_pages, c.p.page_table, c.p.page_table_stride,
             c.p.num_pages, c.p.page_size, c.req(), c.p.batch, c.p.num_kv_heads, 1.f, 1.f, kbar, vbar, kbar_op,
-            vbar_op, c.status());
-    return cudaGetLastError();
-}
-
-cudaError_t launch_score(const Ctx &c, const void *q, const float *kbar, float alpha, int sink, int window) {
-    const float log_alpha = alpha > 0.f ? logf(alpha) : -INFINITY;
-    const dim3 grid((unsigned)c.s.nseg);
-    cudaError_t e;
-    if (c.p.dtype == FP_DTYPE_E4M3) {
-        e = cudaFuncSetAttribute(score_kernel<FP_DTYPE_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kScoreSmem);
-        if (e != cudaSuccess) return e;
-        score_kernel<FP_DTYPE_E4M3><<<grid, kScoreThreads, kScoreSmem, c.stream>>>(
-            (const __nv_fp8_e4m3 *)q, kbar, c.req(), c.p.batch, c.p.num_q_heads, c.p.num_kv_heads, c.s.g,
-            log_alpha, sink, window, c.p.c_q, (int32_t)c.s.nseg, c.seg_count(), c.mask(), c.status());
-    } else {
-        e = cudaFuncSetAttribute(score_kernel<FP_DTYPE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kScoreSmem);
-        if (e != cudaSuccess) return e;
-        score_kernel<FP_DTYPE_BF16><<<grid, kScoreThreads, kScoreSmem, c.stream>>>(
-            (const __nv_bfloat16 *)q, kbar, c.req(), c.p.batch, c.p.num_q_heads, c.p.num_kv_heads, c.s.g,
-            log_alpha, sink, window, 1.f, (int32_t)c.s.nseg, c.seg_count(), c.mask(), c.status());
-    }
+            vbar_op, c.kstat(), c.status());
     return cudaGetLastError();
 }
 
