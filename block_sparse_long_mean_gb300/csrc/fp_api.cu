@@ -62,9 +62,10 @@ WsLayout layout(const fp_problem *p, const Sizes &s) {
     w.seg_count = o; o = align256(o + 4 * (s.nseg + 1));
     w.mask = o; o = align256(o + 4 * (s.mask_words + 1));
     w.work = o; o = align256(o + 4 * (s.nseg + 1));
-    w.hist = o; o = align256(o + 4 * (int64_t)(kMaxBlocks + 2));
+    w.hist = o; o = align256(o + 4 * (int64_t)(kCostBuckets + 2));
     w.counters = o; o = align256(o + 4 * 64);
     w.kstat = o; o = align256(o + 8 * (s.nblocks * p->num_kv_heads + 1));
+    w.meta = o; o = align256(o + (int64_t)sizeof(SegMeta) * (s.nseg + 1));
     w.total = o;
     return w;
 }

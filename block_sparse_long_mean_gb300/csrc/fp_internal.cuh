@@ -17,6 +17,16 @@ constexpr int kBlock = 128;       // B, tokens per selection block
 constexpr int kTileRows = 128;    // packed query rows per tile (PackGQA M-tile)
 constexpr int kMaxLen = 1 << 20;  // longest request
 constexpr int kMaxBlocks = kMaxLen / kBlock;
+constexpr int kMaxChunks = kMaxBlocks / 128;          // 128-block correction chunks per tile (64)
+constexpr int kCostBuckets = kMaxBlocks + kMaxChunks + 2;
+
+// Per-segment Stage 2 schedule entry: iterations and correction chunks.
+struct SegMeta {
+    int32_t n_exact;      // selected blocks walked exactly, -1 if the segment's CSR is malformed
+    int32_t n_chunks;     // correction chunks holding at least one pruned block
+    uint32_t chunk_lo;    // bit c: chunk c (blocks 128c .. 128c+127) needs correction, c < 32
+    uint32_t chunk_hi;    // same for c in [32, 64)
+};
 
 // Per-request table, built on the device from cu_seqlens at the start of each
 // call (the host mirrors it from host_cu_seqlens only to size buffers).
@@ -36,7 +46,7 @@ enum StatusSlot { kStatusCode = 0, kStatusDetail = 1 };
 
 // Byte offsets of the workspace regions, derived on the host from the sizes.
 struct WsLayout {
-    int64_t status, req, seg_count, mask, work, hist, counters, kstat, total;
+    int64_t status, req, seg_count, mask, work, hist, counters, kstat, meta, total;
 };
 
 struct Sizes {
@@ -60,6 +70,7 @@ struct Ctx {
     int32_t *counters() const { return reinterpret_cast<int32_t *>(wsbase + ws.counters); }
     // per (pooled block, KV head): {|kbar - operand-format kbar|_2, |kbar|_2}
     float2 *kstat() const { return reinterpret_cast<float2 *>(wsbase + ws.kstat); }
+    SegMeta *meta() const { return reinterpret_cast<SegMeta *>(wsbase + ws.meta); }
 };
 
 // ----------------------------------------------------------------- device helpers
