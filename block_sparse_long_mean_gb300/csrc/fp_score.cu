@@ -21,10 +21,13 @@
 // the fp32 means, so the CSR matches an exact evaluation except for blocks
 // within fp32 rounding of the threshold.
 //
-// Exp work is skipped for blocks that cannot matter: chunks run from the
-// diagonal block down, and a block whose upper bound
-// max_r s_rJ + ln(rows) + eps_J lies below ln(alpha) + (a proven lower bound of
-// the maximum) is certainly pruned and certainly not the maximum.
+// Exponentials are computed only for blocks that can matter. A block's
+// maximum logit ms_J over the tile's rows bounds its log-energy from both
+// sides, ms_J <= lE_J <= ms_J + ln(rows); the first chunk processed holds the
+// diagonal block, and one block-wide maximum there gives a proven lower bound
+// of max_J lE_J. A later block whose upper bound lies below ln(alpha) plus that
+// bound is certainly pruned and certainly not the maximum, so it needs no
+// exponentials.
 #include <math.h>
 
 #include "fp_internal.cuh"
@@ -72,13 +75,19 @@ struct ScoreSmem {
 };
 
 // state bits
-constexpr uint8_t kStSkipped = 1;    // lE holds an upper bound (eps included), no screened value
+constexpr uint8_t kStBound = 1;      // lE holds only an upper bound (block certainly pruned)
 constexpr uint8_t kStUncertain = 2;  // decision not settled by the bounds
 constexpr uint8_t kStMaxCand = 4;    // may hold the maximum
 constexpr uint8_t kStRefined = 8;    // lE is the fp32 recomputation
 constexpr uint8_t kStSelected = 0x80;
 
 __device__ __forceinline__ void red_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ float warp_max(float v) {
     for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -221,6 +230,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
     } else {
         // --------------------------------------------------- reduction / selection
+        // Chunk pass: thread j keeps only the screened maximum logit ms_J of its block J, which bounds the
+        // log-energy lE_J = ln sum_r exp(s_rJ) on both sides: ms_J - eps_J <= lE_J <= ms_J + ln(rows) + eps_J.
+        // Selection settles every block these bounds decide; blocks they leave open (and the candidates for
+        // the maximum) are recomputed exactly in fp32.
         const int rt = threadIdx.x - 64;              // 0..127 across warps 2-5
         const int j = 32 * (warp & 3) + lane;         // TMEM lane = block in chunk = tile row
         const uint32_t tlane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
@@ -228,190 +241,222 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const float scale = qscale * kscale * inv_sqrt_d;  // raw MMA dot -> logit
         const float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
         uint32_t tile_it = 0, chunk_it = 0;
-        for (int w = blockIdx.x; w < nseg; w += gridDim.x, ++tile_it) {
+        bool ok = true;
+        for (int w = blockIdx.x; w < nseg && ok; w += gridDim.x, ++tile_it) {
             const int seg = nseg - 1 - w;
             const SegCoord sc = decode_seg(req, batch, g, seg);
             const ReqInfo r = req[sc.b];
             const int D = sc.D, rows = sc.rows;
             const int qb = tile_it & 1;
             const int nch = D / 128 + 1;
-            bool ok = true;
-            float qmax = 0.f;
+            const float2 *ks_base = kstat + (int64_t)r.blk_base * hkv + sc.h;
+            const float lnrows = logf((float)rows);
+            float eps_tile = 0.f;                    // largest per-block logit error bound of the tile
+            float mlo = -INFINITY, mhi = -INFINITY;  // this thread's bounds of max_J lE_J
+            float m_run = -INFINITY;                 // proven lower bound of max_J lE_J
             if (scoring) {
                 if (!(ok = mbar_wait(&sm.q_full[qb], (tile_it >> 1) & 1, ab))) break;
-                float n2 = 0.f;
-                if (j < rows)
-                    for (int c = 0; c < kHeadDim; ++c) {
-                        const float x = q_elem<kDtype>(sm.q[qb], j, c) * qscale;
-                        n2 = fmaf(x, x, n2);
+                // |q_j|_2 of this thread's row, read 16 bytes at a time from the swizzled tile
+                float n2[4] = {0.f, 0.f, 0.f, 0.f};
+                if (j < rows) {
+#pragma unroll
+                    for (int ch = 0; ch < 128 * SCfg<kDtype>::kEb / 16; ++ch) {
+                        const int atom = ch >> 3, c16 = ch & 7;
+                        const uint4 u = *reinterpret_cast<const uint4 *>(sm.q[qb] + atom * 16384 + j * 128 +
+                                                                         ((c16 ^ (j & 7)) << 4));
+                        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (kDtype == FP_DTYPE_BF16) {
+                                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv[q]));
+                                n2[q] = fmaf(f.x, f.x, fmaf(f.y, f.y, n2[q]));
+                            } else {
+                                const __nv_fp8x2_e4m3 *p2 = reinterpret_cast<const __nv_fp8x2_e4m3 *>(&wv[q]);
+                                const float2 a = float2(p2[0]), b = float2(p2[1]);
+                                n2[q] = fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(b.x, b.x, fmaf(b.y, b.y, n2[q]))));
+                            }
+                        }
                     }
-                qmax = sqrtf(red_max(sm, n2, 0));
-                float m_run = -INFINITY;  // proven lower bound of max_J lE_J
+                }
+                const float qmax = sqrtf(red_max(sm, (n2[0] + n2[1]) + (n2[2] + n2[3]), 0)) * qscale;
                 for (int cc = 0; cc < nch; ++cc, ++chunk_it) {
                     const int c = nch - 1 - cc;
                     const int sb = chunk_it & 1;
+                    const int J = 128 * c + j;
+                    const bool valid = J <= D;
+                    const float2 ks = valid ? __ldg(ks_base + (int64_t)J * hkv) : make_float2(0.f, 0.f);
                     if (!(ok = mbar_wait(&sm.s_full[sb], (chunk_it >> 1) & 1, ab))) break;
                     tc_fence_after();
-                    float v[128];
+                    uint32_t v[4][32];
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t raw[32];
-                        tmem_ld32(tmem + tlane + sb * 128 + q4 * 32, raw);
-                        tmem_ld_wait();
+                    for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tmem + tlane + sb * 128 + q4 * 32, v[q4]);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int x = 0; x < 32; ++x) v[q4 * 32 + x] = __uint_as_float(raw[x]);
-                    }
+                    for (int q4 = 0; q4 < 4; ++q4) reg_fence32(v[q4]);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
-                    const int J = 128 * c + j;
-                    const bool valid = J <= D;
-                    float m = -INFINITY;
+                    float pm[8];
 #pragma unroll
-                    for (int x = 0; x < 128; ++x) m = fmaxf(m, x < rows ? v[x] : -INFINITY);
-                    float eps = 0.f;
-                    if (valid) {
-                        const float2 ks = kstat[(int64_t)(r.blk_base + J) * hkv + sc.h];
-                        eps = qmax * (ks.x + 2.44140625e-4f * ks.y) * inv_sqrt_d + 2e-4f;
+                    for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+                    if (rows == 128) {
+#pragma unroll
+                        for (int x = 0; x < 128; ++x) pm[x & 7] = fmaxf(pm[x & 7], __uint_as_float(v[x >> 5][x & 31]));
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 128; ++x)
+                            pm[x & 7] = fmaxf(pm[x & 7], x < rows ? __uint_as_float(v[x >> 5][x & 31]) : -INFINITY);
                     }
+                    const float m = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                          fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+                    const float eps = valid ? qmax * (ks.x + 2.44140625e-4f * ks.y) * inv_sqrt_d + 2e-4f : 0.f;
                     const float ms = m * scale;
-                    const float lo = valid ? ms - eps : -INFINITY;
-                    m_run = fmaxf(m_run, red_max(sm, lo, (cc & 1)));
+                    // the first chunk holds the diagonal block (usually the maximum): one block-wide max of the
+                    // lower bounds there gives m_run, a proven lower bound of max_J lE_J for the whole tile
+                    if (cc == 0) m_run = red_max(sm, valid ? ms - eps : -INFINITY, 1);
                     if (valid) {
-                        const float hi = ms + logf((float)rows) + eps;
+                        eps_tile = fmaxf(eps_tile, eps);
+                        const float hi = ms + lnrows + eps;
                         if (hi >= log_alpha + m_run) {
+                            // the block may matter: screened log-energy (operand-format kbar, fp32 sums)
                             const float k2 = scale * LOG2E;
-                            float s = 0.f;
+                            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+                            if (rows == 128) {
 #pragma unroll
-                            for (int x = 0; x < 128; ++x)
-                                if (x < rows) s += exp2f((v[x] - m) * k2);
-                            sm.lE[J] = ms + log2f(s) * LN2;
+                                for (int x = 0; x < 128; ++x)
+                                    ps[x & 3] += ex2((__uint_as_float(v[x >> 5][x & 31]) - m) * k2);
+                            } else {
+#pragma unroll
+                                for (int x = 0; x < 128; ++x)
+                                    if (x < rows) ps[x & 3] += ex2((__uint_as_float(v[x >> 5][x & 31]) - m) * k2);
+                            }
+                            const float lE = ms + log2f((ps[0] + ps[1]) + (ps[2] + ps[3])) * LN2;
+                            sm.lE[J] = lE;
                             sm.state[J] = 0;
+                            mlo = fmaxf(mlo, lE - eps);
+                            mhi = fmaxf(mhi, lE + eps);
                         } else {
+                            // certainly pruned and certainly not the maximum: hi < ln(alpha) + m_run
                             sm.lE[J] = hi;
-                            sm.state[J] = kStSkipped;
+                            sm.state[J] = kStBound;
+                            mhi = fmaxf(mhi, hi);
                         }
                     }
                 }
                 if (!ok) break;
             }
-            red_bar();
+            // ------------------------------------------------------------ selection
             {
-                // ---------------------------------------------------- selection
-                int cnt = 0;
-                if (mode == kModeAll || mode == kModeForced) {
-                    for (int J = rt; J <= D; J += kRedThreads) {
-                        const bool forced = J < sink || (J >= D - window && J < D) || J == D;
-                        sm.state[J] = (mode == kModeAll || forced) ? kStSelected : 0;
-                    }
-                } else {
-                    auto eps_of = [&](int J) {
-                        const float2 ks = kstat[(int64_t)(r.blk_base + J) * hkv + sc.h];
-                        return qmax * (ks.x + 2.44140625e-4f * ks.y) * inv_sqrt_d + 2e-4f;
-                    };
-                    float mlo = -INFINITY, mhi = -INFINITY;
-                    for (int J = rt; J <= D; J += kRedThreads) {
-                        const uint8_t st = sm.state[J];
-                        const float e = eps_of(J);
-                        const float lo = (st & kStSkipped) ? -INFINITY : sm.lE[J] - e;
-                        const float hi = (st & kStSkipped) ? sm.lE[J] : sm.lE[J] + e;
-                        mlo = fmaxf(mlo, lo);
-                        mhi = fmaxf(mhi, hi);
-                    }
-                    mlo = red_max(sm, mlo, 0);
-                    mhi = red_max(sm, mhi, 1);
-                    const float thr_lo = log_alpha + mlo, thr_hi = log_alpha + mhi;
-                    if (rt == 0) sm.any = 0;
-                    red_bar();
-                    int any = 0;
-                    for (int J = rt; J <= D; J += kRedThreads) {
-                        const uint8_t st = sm.state[J];
-                        const float e = eps_of(J);
-                        const float lo = (st & kStSkipped) ? -INFINITY : sm.lE[J] - e;
-                        const float hi = (st & kStSkipped) ? sm.lE[J] : sm.lE[J] + e;
-                        const bool forced = J < sink || (J >= D - window && J < D) || J == D;
-                        uint8_t ns = st;
-                        if (forced || lo >= thr_hi) ns |= kStSelected;
-                        else if (!(hi < thr_lo)) { ns |= kStUncertain; any = 1; }
-                        if (hi >= mlo) ns |= kStMaxCand;
-                        sm.state[J] = ns;
-                    }
-                    if (any) sm.any = 1;
-                    red_bar();
-                    if (sm.any) {
-                        // fp32 recomputation of every max candidate and every unsettled block
-                        float qr[kHeadDim];
-#pragma unroll
-                        for (int c = 0; c < kHeadDim; ++c) qr[c] = j < rows ? q_elem<kDtype>(sm.q[qb], j, c) * qscale : 0.f;
-                        for (;;) {
-                            if (rt == 0) sm.nlist = 0;
-                            red_bar();
-                            // collect up to kRefineList pending candidates with J >= start, in order
-                            for (int J0 = 0; J0 <= D; J0 += kRedThreads) {
-                                const int J = J0 + rt;
-                                const bool need = J <= D && (sm.state[J] & (kStUncertain | kStMaxCand)) &&
-                                                  !(sm.state[J] & kStRefined);
-                                const unsigned bal = __ballot_sync(0xffffffffu, need);
-                                int base = 0;
-                                if (lane == 0 && bal) base = atomicAdd(&sm.nlist, __popc(bal));
-                                base = __shfl_sync(0xffffffffu, base, 0);
-                                if (need) {
-                                    const int slot = base + __popc(bal & ((1u << lane) - 1u));
-                                    if (slot < kRefineList) sm.list[slot] = J;
-                                }
-                                red_bar();
-                                if (sm.nlist >= kRefineList) break;
-                            }
-                            const int n = min(sm.nlist, kRefineList);
-                            if (n == 0) break;
-                            for (int i = 0; i < n; ++i) {
-                                const int J = sm.list[i];
-                                const float *kb = kbar + ((int64_t)(r.blk_base + J) * hkv + sc.h) * kHeadDim;
-                                float dot = 0.f;
-#pragma unroll
-                                for (int c = 0; c < kHeadDim; c += 4) {
-                                    const float4 k4 = __ldg(reinterpret_cast<const float4 *>(kb + c));
-                                    dot = fmaf(qr[c], k4.x, dot);
-                                    dot = fmaf(qr[c + 1], k4.y, dot);
-                                    dot = fmaf(qr[c + 2], k4.z, dot);
-                                    dot = fmaf(qr[c + 3], k4.w, dot);
-                                }
-                                const float s = j < rows ? dot * inv_sqrt_d : -INFINITY;
-                                const float mx = red_max(sm, s, 0);
-                                const float e = j < rows ? expf(s - mx) : 0.f;
-                                const float sum = red_sum(sm, e, 1);
-                                if (rt == 0) {
-                                    sm.lE[J] = mx + logf(sum);
-                                    sm.state[J] = (sm.state[J] & ~kStSkipped) | kStRefined;
-                                }
-                                red_bar();
-                            }
-                            red_bar();
-                        }
-                        float mex = -INFINITY;
-                        for (int J = rt; J <= D; J += kRedThreads)
-                            if (sm.state[J] & kStMaxCand) mex = fmaxf(mex, sm.lE[J]);
-                        mex = red_max(sm, mex, 0);
-                        const float thr = log_alpha + mex;
-                        for (int J = rt; J <= D; J += kRedThreads) {
-                            const uint8_t st = sm.state[J];
-                            if ((st & kStUncertain) && sm.lE[J] >= thr) sm.state[J] = st | kStSelected;
-                        }
-                    }
-                }
-                red_bar();
                 const int64_t wbase = (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
-                for (int wd = rt; wd < r.words; wd += kRedThreads) {
-                    uint32_t bits = 0;
-                    for (int k = 0; k < 32; ++k) {
-                        const int J = 32 * wd + k;
-                        if (J > D) break;
-                        if (sm.state[J] & kStSelected) bits |= 1u << k;
+                float thr_lo = 0.f, thr_hi = 0.f;
+                bool any = false;
+                if (scoring) {
+                    eps_tile = red_max(sm, eps_tile, 0);
+                    mlo = red_max(sm, mlo, 1);
+                    mhi = red_max(sm, mhi, 0);
+                    thr_lo = log_alpha + mlo;
+                    thr_hi = log_alpha + mhi;
+                    // does any screened block's interval straddle the threshold?
+                    int un = 0;
+                    for (int J = rt; J <= D; J += kRedThreads) {
+                        const bool forced = J < sink || (J >= D - window && J < D) || J == D;
+                        const float lE = sm.lE[J];
+                        un |= (!forced && !(sm.state[J] & kStBound) && lE - eps_tile < thr_hi &&
+                               lE + eps_tile >= thr_lo) ? 1 : 0;
                     }
-                    mask[wbase + wd] = bits;
+                    any = red_max(sm, (float)un, 1) > 0.f;
+                }
+                if (any) {
+                    // fp32 recomputation of every unsettled block and every candidate for the maximum
+                    for (int J = rt; J <= D; J += kRedThreads) {
+                        const bool forced = J < sink || (J >= D - window && J < D) || J == D;
+                        const bool bound = sm.state[J] & kStBound;
+                        const float lo = bound ? -INFINITY : sm.lE[J] - eps_tile;
+                        const float hi = bound ? sm.lE[J] : sm.lE[J] + eps_tile;
+                        uint8_t st = 0;
+                        if (forced || lo >= thr_hi) st |= kStSelected;
+                        else if (!(hi < thr_lo)) st |= kStUncertain;
+                        if (hi >= mlo) st |= kStMaxCand;
+                        sm.state[J] = st;
+                    }
+                    float qr[kHeadDim];
+#pragma unroll
+                    for (int c = 0; c < kHeadDim; ++c) qr[c] = j < rows ? q_elem<kDtype>(sm.q[qb], j, c) * qscale : 0.f;
+                    for (;;) {
+                        if (rt == 0) sm.nlist = 0;
+                        red_bar();
+                        // collect up to kRefineList pending candidates, in order
+                        for (int J0 = 0; J0 <= D; J0 += kRedThreads) {
+                            const int J = J0 + rt;
+                            const bool need = J <= D && (sm.state[J] & (kStUncertain | kStMaxCand)) &&
+                                              !(sm.state[J] & kStRefined);
+                            const unsigned bal = __ballot_sync(0xffffffffu, need);
+                            int base = 0;
+                            if (lane == 0 && bal) base = atomicAdd(&sm.nlist, __popc(bal));
+                            base = __shfl_sync(0xffffffffu, base, 0);
+                            if (need) {
+                                const int slot = base + __popc(bal & ((1u << lane) - 1u));
+                                if (slot < kRefineList) sm.list[slot] = J;
+                            }
+                            red_bar();
+                            if (sm.nlist >= kRefineList) break;
+                        }
+                        const int n = min(sm.nlist, kRefineList);
+                        if (n == 0) break;
+                        for (int i = 0; i < n; ++i) {
+                            const int J = sm.list[i];
+                            const float *kb = kbar + ((int64_t)(r.blk_base + J) * hkv + sc.h) * kHeadDim;
+                            float dot = 0.f;
+#pragma unroll
+                            for (int c = 0; c < kHeadDim; c += 4) {
+                                const float4 k4 = __ldg(reinterpret_cast<const float4 *>(kb + c));
+                                dot = fmaf(qr[c], k4.x, dot);
+                                dot = fmaf(qr[c + 1], k4.y, dot);
+                                dot = fmaf(qr[c + 2], k4.z, dot);
+                                dot = fmaf(qr[c + 3], k4.w, dot);
+                            }
+                            const float s = j < rows ? dot * inv_sqrt_d : -INFINITY;
+                            const float mx = red_max(sm, s, 0);
+                            const float e = j < rows ? expf(s - mx) : 0.f;
+                            const float sum = red_sum(sm, e, 1);
+                            if (rt == 0) {
+                                sm.lE[J] = mx + logf(sum);
+                                sm.state[J] |= kStRefined;
+                            }
+                            red_bar();
+                        }
+                        red_bar();
+                    }
+                    // every candidate for the maximum is now exact
+                    float mex = -INFINITY;
+                    for (int J = rt; J <= D; J += kRedThreads)
+                        if (sm.state[J] & kStMaxCand) mex = fmaxf(mex, sm.lE[J]);
+                    mex = red_max(sm, mex, 0);
+                    const float thr = log_alpha + mex;
+                    for (int J = rt; J <= D; J += kRedThreads) {
+                        const uint8_t st = sm.state[J];
+                        if ((st & kStUncertain) && sm.lE[J] >= thr) sm.state[J] = st | kStSelected;
+                    }
+                    red_bar();
+                }
+                // mask words: 32 consecutive blocks per ballot, one warp per word
+                int cnt = 0;
+                for (int J0 = 32 * (warp & 3); J0 < 32 * r.words; J0 += kRedThreads) {
+                    const int J = J0 + lane;
+                    bool sel = false;
+                    if (J <= D) {
+                        const bool forced = J < sink || (J >= D - window && J < D) || J == D;
+                        if (mode == kModeAll || forced) sel = true;
+                        else if (mode == kModeScore) {
+                            if (any) sel = sm.state[J] & kStSelected;
+                            else sel = !(sm.state[J] & kStBound) && sm.lE[J] - eps_tile >= thr_hi;
+                        }
+                    }
+                    const unsigned bits = __ballot_sync(0xffffffffu, sel);
+                    if (lane == 0) mask[wbase + (J0 >> 5)] = bits;
                     cnt += __popc(bits);
                 }
-                cnt = (int)red_sum(sm, (float)cnt, 0);
+                cnt = (int)red_sum(sm, lane == 0 ? (float)cnt : 0.f, 0);
                 if (rt == 0) seg_count[seg] = cnt;
                 red_bar();
                 if (scoring && rt == 0) mbar_arrive(&sm.q_empty[qb]);
