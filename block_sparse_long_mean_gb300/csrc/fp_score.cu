@@ -43,6 +43,7 @@ constexpr int kSThreads = 32 * kSWarps;
 constexpr int kSStages = 3;  // pooled-key chunk stages
 constexpr int kRedThreads = 128;
 constexpr int kRefineList = 256;
+constexpr int kCand = 128;  // candidates per tile settled without the exact path
 
 enum ScoreMode { kModeScore = 0, kModeAll = 1, kModeForced = 2 };
 
@@ -65,13 +66,16 @@ struct ScoreSmem {
     float lE[kMaxBlocks];       // screened log-energy, upper bound, or refined value
     uint8_t state[kMaxBlocks];  // see kSt* below
     int32_t list[kRefineList];
+    uint32_t words[kMaxBlocks / 32];  // selection mask of the current tile
+    int32_t cand[kCand];              // blocks with a screened log-energy
     uint64_t q_full[2], q_empty[2], k_full[kSStages], k_empty[kSStages], s_full[2], s_empty[2];
     uint32_t tmem_base;
     int abort;
     float red[2][4];
-    int ired[4];
-    int nlist;
+    float red3[3][4];
+    int nlist, ncand, nsel;
     int any;
+    int any2[2];  // per tile parity: some candidate was left open (read after the tile's last barrier)
 };
 
 // state bits
@@ -230,55 +234,79 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
     } else {
         // --------------------------------------------------- reduction / selection
-        // Chunk pass: thread j keeps only the screened maximum logit ms_J of its block J, which bounds the
-        // log-energy lE_J = ln sum_r exp(s_rJ) on both sides: ms_J - eps_J <= lE_J <= ms_J + ln(rows) + eps_J.
-        // Selection settles every block these bounds decide; blocks they leave open (and the candidates for
-        // the maximum) are recomputed exactly in fp32.
+        // Thread j owns block J = 128 c + j of each chunk c. Its screened maximum logit ms_J bounds the
+        // block's log-energy, ms_J - eps_J <= lE_J <= ms_J + ln(rows) + eps_J. Blocks whose upper bound
+        // falls below ln(alpha) plus a proven lower bound of the maximum are certainly pruned; the few
+        // others ("candidates") get a screened log-energy and are settled at the end of the tile against
+        // the threshold interval, and any candidate the interval cannot settle sends the tile through the
+        // exact fp32 path. Mask words start from the forced blocks (sink, window, diagonal).
         const int rt = threadIdx.x - 64;              // 0..127 across warps 2-5
         const int j = 32 * (warp & 3) + lane;         // TMEM lane = block in chunk = tile row
         const uint32_t tlane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         const float inv_sqrt_d = rsqrtf((float)kHeadDim);
         const float scale = qscale * kscale * inv_sqrt_d;  // raw MMA dot -> logit
         const float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
+        // bits of the blocks [lo, hi) that fall in mask word k
+        auto range_bits = [](int k, int lo, int hi) -> uint32_t {
+            lo = max(lo - 32 * k, 0);
+            hi = min(hi - 32 * k, 32);
+            if (hi <= lo) return 0u;
+            const uint32_t up = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+            return up & ~((1u << lo) - 1u);
+        };
         uint32_t tile_it = 0, chunk_it = 0;
         bool ok = true;
+        SegCoord sc_next = decode_seg(req, batch, g, nseg - 1 - (int)blockIdx.x);
         for (int w = blockIdx.x; w < nseg && ok; w += gridDim.x, ++tile_it) {
             const int seg = nseg - 1 - w;
-            const SegCoord sc = decode_seg(req, batch, g, seg);
+            const SegCoord sc = sc_next;
+            if (w + (int)gridDim.x < nseg) sc_next = decode_seg(req, batch, g, nseg - 1 - (w + (int)gridDim.x));
             const ReqInfo r = req[sc.b];
             const int D = sc.D, rows = sc.rows;
             const int qb = tile_it & 1;
             const int nch = D / 128 + 1;
             const float2 *ks_base = kstat + (int64_t)r.blk_base * hkv + sc.h;
             const float lnrows = logf((float)rows);
+            const int s_end = min(sink, D + 1), w_lo = max(D - window, 0);
+            // mask words of this tile start as the forced set; thread k owns word k
+            for (int k = rt; k < r.words; k += kRedThreads)
+                sm.words[k] = range_bits(k, 0, s_end) | range_bits(k, w_lo, D) | range_bits(k, D, D + 1);
+            if (rt == 0) {
+                sm.ncand = 0;
+                sm.nsel = 0;
+                sm.any2[tile_it & 1] = 0;
+            }
             float eps_tile = 0.f;                    // largest per-block logit error bound of the tile
             float mlo = -INFINITY, mhi = -INFINITY;  // this thread's bounds of max_J lE_J
             float m_run = -INFINITY;                 // proven lower bound of max_J lE_J
             if (scoring) {
                 if (!(ok = mbar_wait(&sm.q_full[qb], (tile_it >> 1) & 1, ab))) break;
-                // |q_j|_2 of this thread's row, read 16 bytes at a time from the swizzled tile
-                float n2[4] = {0.f, 0.f, 0.f, 0.f};
+                // |q_r|_2 <= sqrt(d) max_i |q_ri|: the largest element magnitude of this thread's row,
+                // an integer maximum over the magnitude bits of the 16-byte chunks of the swizzled tile
+                uint32_t mx = 0;
                 if (j < rows) {
 #pragma unroll
                     for (int ch = 0; ch < 128 * SCfg<kDtype>::kEb / 16; ++ch) {
                         const int atom = ch >> 3, c16 = ch & 7;
                         const uint4 u = *reinterpret_cast<const uint4 *>(sm.q[qb] + atom * 16384 + j * 128 +
                                                                          ((c16 ^ (j & 7)) << 4));
-                        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if (kDtype == FP_DTYPE_BF16) {
-                                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wv[q]));
-                                n2[q] = fmaf(f.x, f.x, fmaf(f.y, f.y, n2[q]));
-                            } else {
-                                const __nv_fp8x2_e4m3 *p2 = reinterpret_cast<const __nv_fp8x2_e4m3 *>(&wv[q]);
-                                const float2 a = float2(p2[0]), b = float2(p2[1]);
-                                n2[q] = fmaf(a.x, a.x, fmaf(a.y, a.y, fmaf(b.x, b.x, fmaf(b.y, b.y, n2[q]))));
-                            }
+                        if (kDtype == FP_DTYPE_BF16) {
+                            mx = __vmaxu2(mx, __vmaxu2(u.x & 0x7fff7fffu, u.y & 0x7fff7fffu));
+                            mx = __vmaxu2(mx, __vmaxu2(u.z & 0x7fff7fffu, u.w & 0x7fff7fffu));
+                        } else {
+                            mx = __vmaxu4(mx, __vmaxu4(u.x & 0x7f7f7f7fu, u.y & 0x7f7f7f7fu));
+                            mx = __vmaxu4(mx, __vmaxu4(u.z & 0x7f7f7f7fu, u.w & 0x7f7f7f7fu));
                         }
                     }
                 }
-                const float qmax = sqrtf(red_max(sm, (n2[0] + n2[1]) + (n2[2] + n2[3]), 0)) * qscale;
+                float amax;
+                if (kDtype == FP_DTYPE_BF16) {
+                    amax = __uint_as_float(max(mx & 0xffffu, mx >> 16) << 16);
+                } else {
+                    const uint32_t b = max(max(mx & 0xffu, (mx >> 8) & 0xffu), max((mx >> 16) & 0xffu, mx >> 24));
+                    amax = float(*reinterpret_cast<const __nv_fp8_e4m3 *>(&b));
+                }
+                const float qmax = red_max(sm, amax, 0) * qscale * sqrtf((float)kHeadDim);
                 for (int cc = 0; cc < nch; ++cc, ++chunk_it) {
                     const int c = nch - 1 - cc;
                     const int sb = chunk_it & 1;
@@ -318,7 +346,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                         eps_tile = fmaxf(eps_tile, eps);
                         const float hi = ms + lnrows + eps;
                         if (hi >= log_alpha + m_run) {
-                            // the block may matter: screened log-energy (operand-format kbar, fp32 sums)
+                            // a candidate: screened log-energy (operand-format kbar, fp32 sums)
                             const float k2 = scale * LOG2E;
                             float ps[4] = {0.f, 0.f, 0.f, 0.f};
                             if (rows == 128) {
@@ -335,6 +363,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
                             sm.state[J] = 0;
                             mlo = fmaxf(mlo, lE - eps);
                             mhi = fmaxf(mhi, lE + eps);
+                            const int slot = atomicAdd(&sm.ncand, 1);
+                            if (slot < kCand) sm.cand[slot] = J;
                         } else {
                             // certainly pruned and certainly not the maximum: hi < ln(alpha) + m_run
                             sm.lE[J] = hi;
@@ -346,112 +376,123 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 if (!ok) break;
             }
             // ------------------------------------------------------------ selection
-            {
-                const int64_t wbase = (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
-                float thr_lo = 0.f, thr_hi = 0.f;
-                bool any = false;
-                if (scoring) {
-                    eps_tile = red_max(sm, eps_tile, 0);
-                    mlo = red_max(sm, mlo, 1);
-                    mhi = red_max(sm, mhi, 0);
-                    thr_lo = log_alpha + mlo;
-                    thr_hi = log_alpha + mhi;
-                    // does any screened block's interval straddle the threshold?
-                    int un = 0;
-                    for (int J = rt; J <= D; J += kRedThreads) {
+            const int64_t wbase = (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
+            float thr_lo = 0.f, thr_hi = 0.f;
+            if (scoring) {
+                // one barrier for the three tile-wide maxima
+                float e3[3] = {eps_tile, mlo, mhi};
+#pragma unroll
+                for (int o = 16; o; o >>= 1)
+#pragma unroll
+                    for (int q = 0; q < 3; ++q) e3[q] = fmaxf(e3[q], __shfl_xor_sync(0xffffffffu, e3[q], o));
+                if (lane == 0)
+                    for (int q = 0; q < 3; ++q) sm.red3[q][warp - 2] = e3[q];
+                red_bar();
+#pragma unroll
+                for (int q = 0; q < 3; ++q)
+                    e3[q] = fmaxf(fmaxf(sm.red3[q][0], sm.red3[q][1]), fmaxf(sm.red3[q][2], sm.red3[q][3]));
+                eps_tile = e3[0];
+                mlo = e3[1];
+                mhi = e3[2];
+                thr_lo = log_alpha + mlo;
+                thr_hi = log_alpha + mhi;
+                // settle the candidates against the threshold interval
+                const int nc = sm.ncand;
+                if (nc > kCand) {
+                    if (rt == 0) sm.any2[tile_it & 1] = 1;
+                } else {
+                    for (int i = rt; i < nc; i += kRedThreads) {
+                        const int J = sm.cand[i];
                         const bool forced = J < sink || (J >= D - window && J < D) || J == D;
+                        if (forced) continue;
                         const float lE = sm.lE[J];
-                        un |= (!forced && !(sm.state[J] & kStBound) && lE - eps_tile < thr_hi &&
-                               lE + eps_tile >= thr_lo) ? 1 : 0;
+                        if (lE - eps_tile >= thr_hi) {
+                            atomicOr(&sm.words[J >> 5], 1u << (J & 31));
+                            atomicAdd(&sm.nsel, 1);
+                        } else if (lE + eps_tile >= thr_lo) {
+                            sm.any2[tile_it & 1] = 1;
+                        }
                     }
-                    any = red_max(sm, (float)un, 1) > 0.f;
                 }
-                if (any) {
-                    // fp32 recomputation of every unsettled block and every candidate for the maximum
-                    for (int J = rt; J <= D; J += kRedThreads) {
-                        const bool forced = J < sink || (J >= D - window && J < D) || J == D;
-                        const bool bound = sm.state[J] & kStBound;
-                        const float lo = bound ? -INFINITY : sm.lE[J] - eps_tile;
-                        const float hi = bound ? sm.lE[J] : sm.lE[J] + eps_tile;
-                        uint8_t st = 0;
-                        if (forced || lo >= thr_hi) st |= kStSelected;
-                        else if (!(hi < thr_lo)) st |= kStUncertain;
-                        if (hi >= mlo) st |= kStMaxCand;
-                        sm.state[J] = st;
-                    }
-                    float qr[kHeadDim];
+                red_bar();
+            }
+            if (scoring && sm.any2[tile_it & 1]) {
+                // fp32 recomputation of every unsettled block and every candidate for the maximum
+                for (int J = rt; J <= D; J += kRedThreads) {
+                    const bool forced = J < sink || (J >= D - window && J < D) || J == D;
+                    const bool bound = sm.state[J] & kStBound;
+                    const float lo = bound ? -INFINITY : sm.lE[J] - eps_tile;
+                    const float hi = bound ? sm.lE[J] : sm.lE[J] + eps_tile;
+                    uint8_t st = 0;
+                    if (forced || lo >= thr_hi) st |= kStSelected;
+                    else if (!(hi < thr_lo)) st |= kStUncertain;
+                    if (hi >= mlo) st |= kStMaxCand;
+                    sm.state[J] = st;
+                }
+                float qr[kHeadDim];
 #pragma unroll
-                    for (int c = 0; c < kHeadDim; ++c) qr[c] = j < rows ? q_elem<kDtype>(sm.q[qb], j, c) * qscale : 0.f;
-                    for (;;) {
-                        if (rt == 0) sm.nlist = 0;
-                        red_bar();
-                        // collect up to kRefineList pending candidates, in order
-                        for (int J0 = 0; J0 <= D; J0 += kRedThreads) {
-                            const int J = J0 + rt;
-                            const bool need = J <= D && (sm.state[J] & (kStUncertain | kStMaxCand)) &&
-                                              !(sm.state[J] & kStRefined);
-                            const unsigned bal = __ballot_sync(0xffffffffu, need);
-                            int base = 0;
-                            if (lane == 0 && bal) base = atomicAdd(&sm.nlist, __popc(bal));
-                            base = __shfl_sync(0xffffffffu, base, 0);
-                            if (need) {
-                                const int slot = base + __popc(bal & ((1u << lane) - 1u));
-                                if (slot < kRefineList) sm.list[slot] = J;
-                            }
-                            red_bar();
-                            if (sm.nlist >= kRefineList) break;
-                        }
-                        const int n = min(sm.nlist, kRefineList);
-                        if (n == 0) break;
-                        for (int i = 0; i < n; ++i) {
-                            const int J = sm.list[i];
-                            const float *kb = kbar + ((int64_t)(r.blk_base + J) * hkv + sc.h) * kHeadDim;
-                            float dot = 0.f;
-#pragma unroll
-                            for (int c = 0; c < kHeadDim; c += 4) {
-                                const float4 k4 = __ldg(reinterpret_cast<const float4 *>(kb + c));
-                                dot = fmaf(qr[c], k4.x, dot);
-                                dot = fmaf(qr[c + 1], k4.y, dot);
-                                dot = fmaf(qr[c + 2], k4.z, dot);
-                                dot = fmaf(qr[c + 3], k4.w, dot);
-                            }
-                            const float s = j < rows ? dot * inv_sqrt_d : -INFINITY;
-                            const float mx = red_max(sm, s, 0);
-                            const float e = j < rows ? expf(s - mx) : 0.f;
-                            const float sum = red_sum(sm, e, 1);
-                            if (rt == 0) {
-                                sm.lE[J] = mx + logf(sum);
-                                sm.state[J] |= kStRefined;
-                            }
-                            red_bar();
+                for (int c = 0; c < kHeadDim; ++c) qr[c] = j < rows ? q_elem<kDtype>(sm.q[qb], j, c) * qscale : 0.f;
+                for (;;) {
+                    if (rt == 0) sm.nlist = 0;
+                    red_bar();
+                    // collect up to kRefineList pending candidates, in order
+                    for (int J0 = 0; J0 <= D; J0 += kRedThreads) {
+                        const int J = J0 + rt;
+                        const bool need = J <= D && (sm.state[J] & (kStUncertain | kStMaxCand)) &&
+                                          !(sm.state[J] & kStRefined);
+                        const unsigned bal = __ballot_sync(0xffffffffu, need);
+                        int base = 0;
+                        if (lane == 0 && bal) base = atomicAdd(&sm.nlist, __popc(bal));
+                        base = __shfl_sync(0xffffffffu, base, 0);
+                        if (need) {
+                            const int slot = base + __popc(bal & ((1u << lane) - 1u));
+                            if (slot < kRefineList) sm.list[slot] = J;
                         }
                         red_bar();
+                        if (sm.nlist >= kRefineList) break;
                     }
-                    // every candidate for the maximum is now exact
-                    float mex = -INFINITY;
-                    for (int J = rt; J <= D; J += kRedThreads)
-                        if (sm.state[J] & kStMaxCand) mex = fmaxf(mex, sm.lE[J]);
-                    mex = red_max(sm, mex, 0);
-                    const float thr = log_alpha + mex;
-                    for (int J = rt; J <= D; J += kRedThreads) {
-                        const uint8_t st = sm.state[J];
-                        if ((st & kStUncertain) && sm.lE[J] >= thr) sm.state[J] = st | kStSelected;
+                    const int n = min(sm.nlist, kRefineList);
+                    if (n == 0) break;
+                    for (int i = 0; i < n; ++i) {
+                        const int J = sm.list[i];
+                        const float *kb = kbar + ((int64_t)(r.blk_base + J) * hkv + sc.h) * kHeadDim;
+                        float dot = 0.f;
+#pragma unroll
+                        for (int c = 0; c < kHeadDim; c += 4) {
+                            const float4 k4 = __ldg(reinterpret_cast<const float4 *>(kb + c));
+                            dot = fmaf(qr[c], k4.x, dot);
+                            dot = fmaf(qr[c + 1], k4.y, dot);
+                            dot = fmaf(qr[c + 2], k4.z, dot);
+                            dot = fmaf(qr[c + 3], k4.w, dot);
+                        }
+                        const float s = j < rows ? dot * inv_sqrt_d : -INFINITY;
+                        const float mxs = red_max(sm, s, 0);
+                        const float e = j < rows ? expf(s - mxs) : 0.f;
+                        const float sum = red_sum(sm, e, 1);
+                        if (rt == 0) {
+                            sm.lE[J] = mxs + logf(sum);
+                            sm.state[J] |= kStRefined;
+                        }
+                        red_bar();
                     }
                     red_bar();
                 }
-                // mask words: 32 consecutive blocks per ballot, one warp per word
+                // every candidate for the maximum is now exact
+                float mex = -INFINITY;
+                for (int J = rt; J <= D; J += kRedThreads)
+                    if (sm.state[J] & kStMaxCand) mex = fmaxf(mex, sm.lE[J]);
+                mex = red_max(sm, mex, 0);
+                const float thr = log_alpha + mex;
+                for (int J = rt; J <= D; J += kRedThreads) {
+                    const uint8_t st = sm.state[J];
+                    if ((st & kStUncertain) && sm.lE[J] >= thr) sm.state[J] = st | kStSelected;
+                }
+                red_bar();
+                // rebuild the mask words from the final states
                 int cnt = 0;
                 for (int J0 = 32 * (warp & 3); J0 < 32 * r.words; J0 += kRedThreads) {
                     const int J = J0 + lane;
-                    bool sel = false;
-                    if (J <= D) {
-                        const bool forced = J < sink || (J >= D - window && J < D) || J == D;
-                        if (mode == kModeAll || forced) sel = true;
-                        else if (mode == kModeScore) {
-                            if (any) sel = sm.state[J] & kStSelected;
-                            else sel = !(sm.state[J] & kStBound) && sm.lE[J] - eps_tile >= thr_hi;
-                        }
-                    }
+                    const bool sel = J <= D && (sm.state[J] & kStSelected);
                     const unsigned bits = __ballot_sync(0xffffffffu, sel);
                     if (lane == 0) mask[wbase + (J0 >> 5)] = bits;
                     cnt += __popc(bits);
@@ -459,8 +500,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 cnt = (int)red_sum(sm, lane == 0 ? (float)cnt : 0.f, 0);
                 if (rt == 0) seg_count[seg] = cnt;
                 red_bar();
-                if (scoring && rt == 0) mbar_arrive(&sm.q_empty[qb]);
+            } else {
+                // settled by bounds: forced blocks plus the selected candidates
+                if (!scoring) red_bar();  // the forced words are complete
+                for (int k = rt; k < r.words; k += kRedThreads) {
+                    uint32_t wv = sm.words[k];
+                    if (mode == kModeAll) wv = range_bits(k, 0, D + 1);
+                    mask[wbase + k] = wv;
+                }
+                if (rt == 0) {
+                    const int forced_cnt = s_end + max(0, D - max(w_lo, s_end)) + (D >= sink ? 1 : 0);
+                    seg_count[seg] = mode == kModeAll ? D + 1 : forced_cnt + (scoring ? sm.nsel : 0);
+                }
             }
+            if (scoring && rt == 0) mbar_arrive(&sm.q_empty[qb]);
         }
     }
 
