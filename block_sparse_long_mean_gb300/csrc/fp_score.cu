@@ -256,12 +256,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
         };
         uint32_t tile_it = 0, chunk_it = 0;
         bool ok = true;
+        // the next tile's coordinates and request record are fetched a tile ahead
         SegCoord sc_next = decode_seg(req, batch, g, nseg - 1 - (int)blockIdx.x);
+        ReqInfo r_next = req[sc_next.b];
         for (int w = blockIdx.x; w < nseg && ok; w += gridDim.x, ++tile_it) {
             const int seg = nseg - 1 - w;
             const SegCoord sc = sc_next;
-            if (w + (int)gridDim.x < nseg) sc_next = decode_seg(req, batch, g, nseg - 1 - (w + (int)gridDim.x));
-            const ReqInfo r = req[sc.b];
+            const ReqInfo r = r_next;
+            if (w + (int)gridDim.x < nseg) {
+                sc_next = decode_seg(req, batch, g, nseg - 1 - (w + (int)gridDim.x));
+                r_next = req[sc_next.b];
+            }
             const int D = sc.D, rows = sc.rows;
             const int qb = tile_it & 1;
             const int nch = D / 128 + 1;
@@ -307,12 +312,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     amax = float(*reinterpret_cast<const __nv_fp8_e4m3 *>(&b));
                 }
                 const float qmax = red_max(sm, amax, 0) * qscale * sqrtf((float)kHeadDim);
+                // rounding statistics of this thread's block, loaded one chunk ahead
+                float2 ks_next = (128 * (nch - 1) + j <= D) ? __ldg(ks_base + (int64_t)(128 * (nch - 1) + j) * hkv)
+                                                            : make_float2(0.f, 0.f);
                 for (int cc = 0; cc < nch; ++cc, ++chunk_it) {
                     const int c = nch - 1 - cc;
                     const int sb = chunk_it & 1;
                     const int J = 128 * c + j;
                     const bool valid = J <= D;
-                    const float2 ks = valid ? __ldg(ks_base + (int64_t)J * hkv) : make_float2(0.f, 0.f);
+                    const float2 ks = ks_next;
+                    if (c > 0) ks_next = __ldg(ks_base + (int64_t)(J - 128) * hkv);
                     if (!(ok = mbar_wait(&sm.s_full[sb], (chunk_it >> 1) & 1, ab))) break;
                     tc_fence_after();
                     uint32_t v[4][32];
@@ -329,7 +338,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
                     if (rows == 128) {
 #pragma unroll
-                        for (int x = 0; x < 128; ++x) pm[x & 7] = fmaxf(pm[x & 7], __uint_as_float(v[x >> 5][x & 31]));
+                        for (int x = 0; x < 128; x += 2)
+                            pm[(x >> 1) & 7] = fmax3(pm[(x >> 1) & 7], __uint_as_float(v[x >> 5][x & 31]),
+                                                     __uint_as_float(v[x >> 5][(x & 31) + 1]));
                     } else {
 #pragma unroll
                         for (int x = 0; x < 128; ++x)
