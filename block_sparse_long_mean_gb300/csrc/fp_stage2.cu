@@ -9,16 +9,13 @@
 //
 // Per segment (one 128-row packed query tile, Eq.12-13) the CTA runs one
 // pipeline iteration per selected block, in descending block order (Eq.17),
-// then one per correction chunk of 128 pooled means (Eq.6):
-//   warp 0      TMA producer: Q tile once; per iteration the block's K and V
-//               pages through the page table (Eq.22) or the chunk's means
-//   warp 1      MMA issuer (one thread): S = Q K^T into TMEM, then O += P V
-//               with P read from TMEM
-//   warps 2-5   softmax / epilogue, one thread per row: online softmax in the
-//               base-2 domain (causal mask on the diagonal block; the log2|B_J|
-//               = 7 shift and the todo mask on mean chunks), P written to TMEM,
-//               lazy rescaling of O, final O / l and the LSE
-// TMEM columns: S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512).
+// then one per correction chunk of 128 pooled means (Eq.6): TMA producers
+// bring the Q tile, the block's K and V pages through the page table (Eq.22)
+// or the chunk's means; one thread issues S = Q K^T and O += P V on tcgen05;
+// softmax warps keep one row per thread (online softmax in the base-2
+// domain, causal mask on the diagonal block, the log2|B_J| = 7 shift and the
+// correction mask on mean chunks, lazy rescaling of O); epilogue warps divide
+// by the denominator and write bf16 O and the LSE.
 // FP8 (Eq.15): Q, K, V and the means are E4M3, S = c_q c_k (Q~ K~^T),
 // P~ = e4m3(256 * 2^(x - m)) with the denominator summing P~, O = c_v ... / l.
 #include <math.h>
@@ -154,18 +151,22 @@ __global__ void __launch_bounds__(256) attn_scatter_kernel(const SegMeta *__rest
 // --------------------------------------------------------------- attention
 
 // Warp roles (three warpgroups; registers rebalanced with setmaxnreg):
-//   warp 0  K producer      warp 1  MMA issuer + TMEM owner
-//   warp 2  V producer      warp 3  Q producer (lane 0: slot 0, lane 1: slot 1)
-//   warps 4-7   softmax + epilogue of tile slot 0
-//   warps 8-11  softmax + epilogue of tile slot 1
-// Two query tiles ("slots") are in flight per CTA: while one slot's softmax
-// runs, the tensor core works on the other slot's QK^T and PV (ping-pong).
+//   warp 0      Q and K producer (TMA)     warp 1   MMA issuer + TMEM owner
+//   warp 2      V producer (TMA)           warp 3   idle
+//   warps 4-7   softmax, one thread per packed row
+//   warps 8-11  epilogue: O / l to bf16, LSE
+// TMEM: two S buffers (P of an iteration is written over its S), two O buffers.
+// The MMA warp issues QK^T of iteration i+1 before PV of iteration i, so the
+// tensor core computes the next scores while the softmax works on these.
+// Every tcgen05.mma of the CTA comes from one thread and executes in issue
+// order, so QK^T(i+2) may be issued right after PV(i), which read P(i) from
+// the same columns. O is double-buffered so one tile's epilogue overlaps the
+// next tile's PVs.
 constexpr int kAWarps = 12;
 constexpr int kAThreads = 32 * kAWarps;
 constexpr int kKStages = 3, kVStages = 2;
-// TMEM columns: S_X (P_X aliased on its first columns) at 128 X, O_X at 256 + 128 X
-constexpr uint32_t kColS = 0, kColO = 256;
-constexpr int kRegsProducer = 56, kRegsSoftmax = 224;  // 128 x 56 + 256 x 224 = 384 x 168
+constexpr uint32_t kColS = 0, kColO = 256;  // S_b at 128 b, O_o at 256 + 128 o
+constexpr int kRegsProducer = 56, kRegsSoftmax = 232, kRegsEpilogue = 160;  // 128 x (56 + 232 + 160) <= 384 x 168
 
 template <int kDtype>
 struct ACfg {
@@ -185,10 +186,11 @@ struct AttnSmem {
     alignas(1024) uint8_t q[2][ACfg<kDtype>::kTile];
     alignas(1024) uint8_t k[kKStages][ACfg<kDtype>::kTile];
     alignas(1024) uint8_t v[kVStages][ACfg<kDtype>::kTile];
+    float stat_m[2][128], stat_l[2][128];  // per O buffer: running max (log2) and denominator of each row
     uint64_t q_full[2], q_empty[2], k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages],
-        s_full[2], p_full[2], o_full[2], o_empty[2];
+        s_full[2], p_full[2], pv_done[2], o_full[2], o_empty[2], st_full[2];
     uint32_t tmem_base;
-    int abort;
+    int abort, skip;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -204,13 +206,6 @@ __device__ __forceinline__ void regs_inc() {
 template <uint32_t kRegs>
 __device__ __forceinline__ void regs_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-
-__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int c0, int c1, int c2, int c3) {
-    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-                 : "memory");
 }
 
 // Kernel arguments besides the tensor maps (read from the constant bank).
@@ -231,17 +226,17 @@ struct AttnParams {
     int32_t *status;
 };
 
-// One slot's walk over its tiles (work items blockIdx.x + (2k + slot) * gridDim.x,
-// skipping empty or malformed segments) and over each tile's iterations: the
-// selected blocks in descending order (Eq.17), then the correction chunks.
-struct SlotWalk {
+// Walk over this CTA's tiles (work items blockIdx.x + k gridDim.x, skipping
+// empty or malformed segments) and each tile's iterations: the selected blocks
+// in descending order (Eq.17), then the correction chunks.
+struct TileWalk {
     int w, seg, n, it, n_exact;
     SegCoord sc;
     int32_t end;
     uint64_t chunks;
     bool live;
-    __device__ __forceinline__ void start(const AttnParams &a, int slot) {
-        w = blockIdx.x + slot * gridDim.x - 2 * gridDim.x;
+    __device__ __forceinline__ void start(const AttnParams &a) {
+        w = (int)blockIdx.x - (int)gridDim.x;
         n = it = 0;
         live = true;
         next_tile(a);
@@ -249,7 +244,7 @@ struct SlotWalk {
     // moves to the next tile holding at least one iteration; live = false when none is left
     __device__ __forceinline__ void next_tile(const AttnParams &a) {
         for (;;) {
-            w += 2 * gridDim.x;
+            w += gridDim.x;
             if (w >= a.nseg) {
                 live = false;
                 return;
@@ -291,7 +286,6 @@ __global__ void __launch_bounds__(kAThreads, 1)
     const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
     AttnSmem<kDtype> &sm = *reinterpret_cast<AttnSmem<kDtype> *>(base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (status_bad(P.status)) return;
     if (base + sizeof(AttnSmem<kDtype>) > reinterpret_cast<uintptr_t>(smem_raw) + P.smem_bytes) {
         if (threadIdx.x == 0) set_status(P.status, FP_ERR_DEVICE_TIMEOUT, -1);
         return;
@@ -305,8 +299,10 @@ __global__ void __launch_bounds__(kAThreads, 1)
             mbar_init(&sm.q_empty[i], 1);
             mbar_init(&sm.s_full[i], 1);
             mbar_init(&sm.p_full[i], 4);
+            mbar_init(&sm.pv_done[i], 1);
             mbar_init(&sm.o_full[i], 1);
             mbar_init(&sm.o_empty[i], 4);
+            mbar_init(&sm.st_full[i], 4);
         }
         for (int i = 0; i < kKStages; ++i) {
             mbar_init(&sm.k_full[i], 1);
@@ -317,6 +313,8 @@ __global__ void __launch_bounds__(kAThreads, 1)
             mbar_init(&sm.v_empty[i], 1);
         }
         sm.abort = 0;
+        // an earlier stage failed: every warp skips its role (one read, so the CTA agrees)
+        sm.skip = status_bad(P.status) ? 1 : 0;
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(&sm.tmem_base, 512);
@@ -326,213 +324,161 @@ __global__ void __launch_bounds__(kAThreads, 1)
     const Abort ab{&sm.abort};
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp < 4) {
+    if (sm.skip) {
+    } else if (warp < 4) {
         regs_dec<kRegsProducer>();
         if (warp == 0 || warp == 2) {
-            // ------------------------------------------------ K (warp 0) / V (warp 2) producer
+            // ------------------------------------------------ Q + K (warp 0) / V (warp 2) producer
             const bool is_k = warp == 0;
             if (lane == 0) {
+                if (is_k) tma_prefetch_desc(&tm_q);
                 tma_prefetch_desc(is_k ? &tm_k : &tm_v);
                 tma_prefetch_desc(is_k ? &tm_kb : &tm_vb);
             }
             const int ps_eff = min(P.page_size, 128);
-            const int npc = 128 / ps_eff;               // page chunks per 128-token block
+            const int npc = 128 / ps_eff;                   // page chunks per 128-token block
             const int oob_row = P.num_pages * P.page_size;  // first row past the pool: TMA fills zeros
             const int nst = is_k ? kKStages : kVStages;
             uint64_t *fullb = is_k ? sm.k_full : sm.v_full;
             uint64_t *emptyb = is_k ? sm.k_empty : sm.v_empty;
-            SlotWalk sw[2];
-            sw[0].start(P, 0);
-            sw[1].start(P, 1);
-            int turn = 0;
-            for (uint32_t i = 0;; ++i) {
-                // the tensor core consumes K (QK^T) and V (PV) tiles alternating between the slots
-                int x = turn;
-                if (!sw[x].live) x ^= 1;
-                if (!sw[x].live) break;
-                turn = x ^ 1;
-                SlotWalk &s = sw[x];
-                const ReqInfo r = P.req[s.sc.b];
-                const int J = s.take(P);
-                const int h = s.sc.h;
-                // lane l < kBoxes * npc (<= 32 as page_size >= 8) copies page chunk l % npc of d box l / npc;
-                // its page row is looked up before waiting for the slot
-                int row = oob_row;
-                if (J >= 0 && lane < C::kBoxes * npc) {
-                    const int tok = J * kBlock + (lane % npc) * ps_eff;
-                    if (tok < r.len) {
-                        const int page = P.pt[(int64_t)s.sc.b * P.pt_stride + tok / P.page_size];
-                        if (page >= 0 && page < P.num_pages)
-                            row = page * P.page_size + tok % P.page_size;
-                        else
-                            set_status(status, FP_ERR_DEVICE_PAGE, page);
-                    }
-                }
-                if (s.it == s.n) s.next_tile(P);
-                const int st = i % nst;
-                if (!mbar_wait(&emptyb[st], ((i / nst) & 1) ^ 1, ab)) break;
-                if (lane == 0) mbar_arrive_expect_tx(&fullb[st], C::kTile);
-                __syncwarp();
-                uint8_t *dst = is_k ? sm.k[st] : sm.v[st];
-                if (J >= 0) {
-                    if (lane < C::kBoxes * npc) {
-                        const int box = lane / npc, pc = lane % npc;
-                        tma_load_3d(dst + box * 16384 + pc * ps_eff * 128, is_k ? &tm_k : &tm_v, &fullb[st],
-                                    box * C::kBoxElems, h, row);
-                    }
-                } else if (lane < C::kBoxes) {
-                    tma_load_3d(dst + lane * 16384, is_k ? &tm_kb : &tm_vb, &fullb[st], lane * C::kBoxElems, h,
-                                r.blk_base + 128 * (-1 - J));
-                }
-            }
-        } else if (warp == 3) {
-            // ------------------------------------------------------ Q producer, one lane per slot
-            if (lane < 2) {
-                const int x = lane;
-                if (x == 0) tma_prefetch_desc(&tm_q);
-                SlotWalk s;
-                s.start(P, x);
-                for (uint32_t t = 0; s.live; ++t) {
-                    const ReqInfo r = P.req[s.sc.b];
-                    const int pos0 = r.q_start + (s.sc.t * kTileRows) / g;
-                    const int h = s.sc.h;
-                    if (!mbar_wait(&sm.q_empty[x], (t & 1) ^ 1, ab)) break;
-                    mbar_arrive_expect_tx(&sm.q_full[x], C::kTile);
-                    for (int i = 0; i < C::kBoxes; ++i)
-                        tma_load_4d(sm.q[x] + i * 16384, &tm_q, &sm.q_full[x], i * C::kBoxElems, 0, h, pos0);
-                    s.next_tile(P);
-                    if (s.live) {
-                        // warm L2 with the slot's next tile while this one runs
-                        const ReqInfo rn = P.req[s.sc.b];
-                        const int p1 = rn.q_start + (s.sc.t * kTileRows) / g;
-                        for (int i = 0; i < C::kBoxes; ++i) tma_prefetch_l2_4d(&tm_q, i * C::kBoxElems, 0, s.sc.h, p1);
-                    }
-                }
-            }
-        } else if (lane == 0) {
-            // ------------------------------------------------------------------ MMA issue
-            SlotWalk sw[2];
-            sw[0].start(P, 0);
-            sw[1].start(P, 1);
-            uint32_t ki = 0, vi = 0;
-            uint32_t qt[2] = {0, 0};    // tiles whose Q was consumed, per slot
-            uint32_t pt_[2] = {0, 0};   // PVs issued per slot
-            uint32_t ot[2] = {0, 0};    // tiles whose O was started, per slot
-            bool pv_pending[2] = {false, false}, pv_first[2] = {false, false}, pv_last[2] = {false, false};
+            TileWalk s;
+            s.start(P);
+            uint32_t gi = 0;
             bool ok = true;
-            // QK^T of slot x's next iteration into S_x
-            auto issue_qk = [&](int x) -> bool {
-                SlotWalk &s = sw[x];
-                const bool first = s.it == 0;
-                if (first && !mbar_wait(&sm.q_full[x], qt[x] & 1, ab)) return false;
-                s.take(P);
-                const bool last = s.it == s.n;
-                const int ks = ki % kKStages;
-                if (!mbar_wait(&sm.k_full[ks], (ki / kKStages) & 1, ab)) return false;
-                tc_fence_after();
-                const uint32_t qbase = smem_addr(sm.q[x]), kbase = smem_addr(sm.k[ks]);
-#pragma unroll
-                for (int k = 0; k < C::kNumK; ++k) {
-                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                    const uint64_t ad = sw128_desc(qbase + off, 16, 1024);
-                    const uint64_t bd = sw128_desc(kbase + off, 16, 1024);
-                    if (kDtype == FP_DTYPE_BF16)
-                        umma_f16_ss(tmem + kColS + x * 128, ad, bd, C::kIdescQK, k > 0);
-                    else
-                        umma_f8_ss(tmem + kColS + x * 128, ad, bd, C::kIdescQK, k > 0);
+            for (uint32_t ti = 0; s.live && ok; ++ti) {
+                const ReqInfo r = P.req[s.sc.b];
+                const int h = s.sc.h, b = s.sc.b;
+                if (is_k) {
+                    const int qb = ti & 1;
+                    if (!(ok = mbar_wait(&sm.q_empty[qb], ((ti >> 1) & 1) ^ 1, ab))) break;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&sm.q_full[qb], C::kTile);
+                        const int pos0 = r.q_start + (s.sc.t * kTileRows) / g;
+                        for (int i = 0; i < C::kBoxes; ++i)
+                            tma_load_4d(sm.q[qb] + i * 16384, &tm_q, &sm.q_full[qb], i * C::kBoxElems, 0, h, pos0);
+                    }
                 }
-                umma_commit(&sm.k_empty[ks]);
-                umma_commit(&sm.s_full[x]);
-                ++ki;
-                pv_pending[x] = true;
-                pv_first[x] = first;
-                pv_last[x] = last;
-                if (last) {
-                    umma_commit(&sm.q_empty[x]);
-                    ++qt[x];
-                    s.next_tile(P);
+                const int n = s.n;
+                for (int it = 0; it < n; ++it, ++gi) {
+                    const int J = s.take(P);
+                    // lane l < kBoxes * npc (<= 32 as page_size >= 8) copies page chunk l % npc of d box l / npc;
+                    // its page row is looked up before waiting for the slot
+                    int row = oob_row;
+                    if (J >= 0 && lane < C::kBoxes * npc) {
+                        const int tok = J * kBlock + (lane % npc) * ps_eff;
+                        if (tok < r.len) {
+                            const int page = P.pt[(int64_t)b * P.pt_stride + tok / P.page_size];
+                            if (page >= 0 && page < P.num_pages)
+                                row = page * P.page_size + tok % P.page_size;
+                            else
+                                set_status(status, FP_ERR_DEVICE_PAGE, page);
+                        }
+                    }
+                    const int st = gi % nst;
+                    if (!(ok = mbar_wait(&emptyb[st], ((gi / nst) & 1) ^ 1, ab))) break;
+                    if (lane == 0) mbar_arrive_expect_tx(&fullb[st], C::kTile);
+                    __syncwarp();
+                    uint8_t *dst = is_k ? sm.k[st] : sm.v[st];
+                    if (J >= 0) {
+                        if (lane < C::kBoxes * npc) {
+                            const int box = lane / npc, pc = lane % npc;
+                            tma_load_3d(dst + box * 16384 + pc * ps_eff * 128, is_k ? &tm_k : &tm_v, &fullb[st],
+                                        box * C::kBoxElems, h, row);
+                        }
+                    } else if (lane < C::kBoxes) {
+                        tma_load_3d(dst + lane * 16384, is_k ? &tm_kb : &tm_vb, &fullb[st], lane * C::kBoxElems, h,
+                                    r.blk_base + 128 * (-1 - J));
+                    }
                 }
-                return true;
-            };
-            // O_x (+)= P_x V of slot x's pending iteration
-            auto issue_pv = [&](int x) -> bool {
-                if (pv_first[x] && !mbar_wait(&sm.o_empty[x], (ot[x] & 1) ^ 1, ab)) return false;
-                const int vs = vi % kVStages;
-                if (!mbar_wait(&sm.v_full[vs], (vi / kVStages) & 1, ab)) return false;
-                if (!mbar_wait(&sm.p_full[x], pt_[x] & 1, ab)) return false;
+                s.next_tile(P);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------------------------ MMA issue
+            TileWalk s;
+            s.start(P);
+            uint32_t gi = 0;
+            bool ok = true;
+            // O_ob (+)= P(i) V(i); the first PV of a tile overwrites O_ob once its previous epilogue read it
+            auto issue_pv = [&](uint32_t i, bool first, int ob, uint32_t ti) -> bool {
+                const int vs = i % kVStages, pb = i & 1;
+                if (first && !mbar_wait(&sm.o_empty[ob], ((ti >> 1) & 1) ^ 1, ab)) return false;
+                if (!mbar_wait(&sm.v_full[vs], (i / kVStages) & 1, ab)) return false;
+                if (!mbar_wait(&sm.p_full[pb], (i >> 1) & 1, ab)) return false;
                 tc_fence_after();
                 const uint32_t vbase = smem_addr(sm.v[vs]);
 #pragma unroll
                 for (int k = 0; k < C::kNumK; ++k) {
                     // B = V, MN-major: 8-key row groups 1024 B apart, 64-element d atoms 16 KB apart
                     const uint64_t bd = sw128_desc(vbase + k * C::kKStep * 128, 16384, 1024);
-                    const uint32_t a = tmem + kColS + x * 128 + k * (C::kKStep * C::kEb / 4);
-                    const uint32_t acc = (!pv_first[x] || k > 0) ? 1u : 0u;
+                    const uint32_t a = tmem + kColS + pb * 128 + k * (C::kKStep * C::kEb / 4);
+                    const uint32_t acc = (!first || k > 0) ? 1u : 0u;
                     if (kDtype == FP_DTYPE_BF16)
-                        umma_f16_ts(tmem + kColO + x * 128, a, bd, C::kIdescPV, acc);
+                        umma_f16_ts(tmem + kColO + ob * 128, a, bd, C::kIdescPV, acc);
                     else
-                        umma_f8_ts(tmem + kColO + x * 128, a, bd, C::kIdescPV, acc);
+                        umma_f8_ts(tmem + kColO + ob * 128, a, bd, C::kIdescPV, acc);
                 }
                 umma_commit(&sm.v_empty[vs]);
-                ++vi;
-                ++pt_[x];
-                if (pv_first[x]) ++ot[x];
-                if (pv_last[x]) umma_commit(&sm.o_full[x]);
-                pv_pending[x] = false;
+                umma_commit(&sm.pv_done[pb]);
                 return true;
             };
-            for (int x = 0; x < 2 && ok; ++x)
-                if (sw[x].live) ok = issue_qk(x);
-            for (int x = 0; ok; x ^= 1) {
-                if (!pv_pending[0] && !pv_pending[1]) break;
-                if (pv_pending[x]) {
-                    if (!(ok = issue_pv(x))) break;
-                    if (sw[x].live && !(ok = issue_qk(x))) break;
+            for (uint32_t ti = 0; s.live && ok; ++ti) {
+                const int qb = ti & 1, ob = ti & 1;
+                const int n = s.n;
+                if (!(ok = mbar_wait(&sm.q_full[qb], (ti >> 1) & 1, ab))) break;
+                const uint32_t qbase = smem_addr(sm.q[qb]);
+                for (int it = 0; it < n; ++it, ++gi) {
+                    const int ks = gi % kKStages, sb = gi & 1;
+                    if (!(ok = mbar_wait(&sm.k_full[ks], (gi / kKStages) & 1, ab))) break;
+                    tc_fence_after();
+                    const uint32_t kbase = smem_addr(sm.k[ks]);
+#pragma unroll
+                    for (int k = 0; k < C::kNumK; ++k) {
+                        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                        const uint64_t ad = sw128_desc(qbase + off, 16, 1024);
+                        const uint64_t bd = sw128_desc(kbase + off, 16, 1024);
+                        if (kDtype == FP_DTYPE_BF16)
+                            umma_f16_ss(tmem + kColS + sb * 128, ad, bd, C::kIdescQK, k > 0);
+                        else
+                            umma_f8_ss(tmem + kColS + sb * 128, ad, bd, C::kIdescQK, k > 0);
+                    }
+                    umma_commit(&sm.k_empty[ks]);
+                    umma_commit(&sm.s_full[sb]);
+                    if (it == n - 1) umma_commit(&sm.q_empty[qb]);
+                    if (it >= 1 && !(ok = issue_pv(gi - 1, it == 1, ob, ti))) break;
                 }
+                if (!ok) break;
+                if (!(ok = issue_pv(gi - 1, n == 1, ob, ti))) break;
+                umma_commit(&sm.o_full[ob]);
+                s.next_tile(P);
             }
         }
-    } else {
+    } else if (warp < 8) {
         regs_inc<kRegsSoftmax>();
-        // ---------------------------------------------------- softmax / epilogue of one slot
-        const int x = (warp - 4) >> 2;          // slot
-        const int j = 32 * (warp & 3) + lane;   // TMEM lane = packed row of the tile
+        // -------------------------------------------------------------------------- softmax
+        const int j = 32 * (warp & 3) + lane;  // TMEM lane = packed row of the tile
         const uint32_t tlane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-        const uint32_t tS = tmem + tlane + kColS + x * 128, tO = tmem + tlane + kColO + x * 128;
         const float LOG2E = 1.4426950408889634f;
-        const float sl2 = (kDtype == FP_DTYPE_E4M3 ? P.c_q * P.c_k : 1.f) * LOG2E * rsqrtf((float)kHeadDim);
+        const float sl2 = P.c_q * P.c_k * LOG2E * rsqrtf((float)kHeadDim);
         // lazy rescale slack (log2 units): bf16 P may reach 2^8; FP8 P~ must stay within [0, 256]
         const float tau = kDtype == FP_DTYPE_E4M3 ? 0.f : 8.f;
         const float pshift = kDtype == FP_DTYPE_E4M3 ? 8.f : 0.f;  // FP8 probabilities in [0, 256] (Eq.15)
-        uint32_t si = 0, ti = 0;
+        TileWalk s;
+        s.start(P);
+        uint32_t gi = 0;
         bool ok = true;
-        SlotWalk s;
-        s.start(P, x);
-        // empty (but well-formed) segments of this slot get zero rows
-        for (int w = blockIdx.x + x * gridDim.x; w < P.nseg; w += 2 * gridDim.x) {
-            const int seg = P.work[w];
-            const SegMeta m = P.meta[seg];
-            if (m.n_exact != 0 || m.n_chunks != 0) continue;
-            const SegCoord sc = decode_seg(P.req, P.batch, g, seg);
-            const ReqInfo r = P.req[sc.b];
-            const int gr = sc.t * kTileRows + j;
-            if (j < sc.rows) {
-                const int64_t rowi = (int64_t)(r.q_start + gr / g) * P.hq + sc.h * g + gr % g;
-                for (int e = 0; e < kHeadDim; e += 8)
-                    *reinterpret_cast<uint4 *>(P.out + rowi * kHeadDim + e) = make_uint4(0, 0, 0, 0);
-                if (P.lse) P.lse[rowi] = -INFINITY;
-            }
-        }
-        while (s.live && ok) {
+        for (uint32_t ti = 0; s.live && ok; ++ti) {
+            const int ob = ti & 1;
             const SegCoord sc = s.sc;
             const ReqInfo r = P.req[sc.b];
-            const int gr = sc.t * kTileRows + j;
-            const int pos = gr / g, head = sc.h * g + gr % g;
-            const bool valid = j < sc.rows;
+            const int pos = (sc.t * kTileRows + j) / g;
             const uint32_t *tw = P.todo + (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
             const int nw = (sc.D + 31) / 32;
             const int n = s.n;
+            const uint32_t tO = tmem + tlane + kColO + ob * 128;
             float mx = -INFINITY, l = 0.f;
-            for (int it = 0; it < n; ++it, ++si) {
+            for (int it = 0; it < n; ++it, ++gi) {
+                const int sb = gi & 1;
+                const uint32_t tS = tmem + tlane + kColS + sb * 128;
                 const int J = s.take(P);
                 uint4 mv = make_uint4(0, 0, 0, 0);  // correction-chunk key mask
                 if (J < 0) {
@@ -542,7 +488,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
                     for (int q4 = 0; q4 < 4; ++q4) wv[q4] = (4 * c + q4 < nw) ? __ldg(tw + 4 * c + q4) : 0u;
                     mv = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
-                if (!(ok = mbar_wait(&sm.s_full[x], si & 1, ab))) break;
+                if (!(ok = mbar_wait(&sm.s_full[sb], (gi >> 1) & 1, ab))) break;
                 tc_fence_after();
                 uint32_t sv[4][32];
 #pragma unroll
@@ -559,7 +505,9 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 if (plain) {
                     // every key takes part (a block off the diagonal, or a chunk with no selected block)
 #pragma unroll
-                    for (int e = 0; e < 128; ++e) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(sv[e >> 5][e & 31]));
+                    for (int e = 0; e < 128; e += 2)
+                        pm[(e >> 1) & 7] = fmax3(pm[(e >> 1) & 7], __uint_as_float(sv[e >> 5][e & 31]),
+                                                 __uint_as_float(sv[e >> 5][(e & 31) + 1]));
                 } else if (J >= 0) {
                     const int lim = pos - J * kBlock;  // causal mask on the diagonal block
 #pragma unroll
@@ -577,16 +525,18 @@ __global__ void __launch_bounds__(kAThreads, 1)
                         pm[e & 7] = fmaxf(pm[e & 7], v);
                     }
                 }
-                const float rmax = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                         fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+                const float rmax = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
                 const float tmax = fmaf(rmax, sl2, shift);
-                // online softmax with lazy rescaling of O (PV of the previous iteration is complete:
-                // it was issued before this iteration's QK^T, whose completion s_full signalled)
+                // online softmax with lazy rescaling of O
                 const bool first = it == 0;
                 const bool grow = first || tmax > mx + tau;
                 const float m_new = grow ? fmaxf(mx, tmax) : mx;
                 const bool need_o = !first && grow;
                 if (__any_sync(0xffffffffu, need_o)) {
+                    // O holds the sum up to iteration it-1: wait for that PV, then rescale it in TMEM
+                    const uint32_t prev = gi - 1;
+                    if (!(ok = mbar_wait(&sm.pv_done[prev & 1], (prev >> 1) & 1, ab))) break;
+                    tc_fence_after();
                     const float f = need_o ? ex2(mx - m_new) : 1.f;
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
@@ -601,8 +551,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 }
                 if (!first) l *= ex2(mx - m_new);
                 mx = m_new;
-                // pass 2: p = 2^(x - m) (FP8: 2^(x - m + 8)), row sum, P written over S_x
-                // (packed in place over the consumed scores, 32 keys at a time)
+                // pass 2: p = 2^(x - m) (FP8: 2^(x - m + 8)), row sum, P packed in place and written over S
                 const float off = shift - mx + pshift;
                 float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -640,24 +589,48 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.p_full[x]);
+                if (lane == 0) mbar_arrive(&sm.p_full[sb]);
             }
             if (!ok) break;
+            // hand the row statistics to the epilogue (its previous use of this buffer must be done)
+            if (!(ok = mbar_wait(&sm.o_empty[ob], ((ti >> 1) & 1) ^ 1, ab))) break;
+            sm.stat_m[ob][j] = mx;
+            sm.stat_l[ob][j] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.st_full[ob]);
             s.next_tile(P);
-            // epilogue: wait for the tile's last PV, O / l to bf16, release O_x
-            if (!(ok = mbar_wait(&sm.o_full[x], ti & 1, ab))) break;
+        }
+    } else {
+        regs_dec<kRegsEpilogue>();
+        // ------------------------------------------------------------------------- epilogue
+        const int j = 32 * (warp & 3) + lane;
+        const uint32_t tlane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        const float pshift = kDtype == FP_DTYPE_E4M3 ? 8.f : 0.f;
+        TileWalk s;
+        s.start(P);
+        bool ok = true;
+        for (uint32_t ti = 0; s.live && ok; ++ti) {
+            const int ob = ti & 1;
+            const SegCoord sc = s.sc;
+            const ReqInfo r = P.req[sc.b];
+            const int gr = sc.t * kTileRows + j;
+            const int pos = gr / g, head = sc.h * g + gr % g;
+            const bool valid = j < sc.rows;
+            if (!(ok = mbar_wait(&sm.o_full[ob], (ti >> 1) & 1, ab))) break;
+            if (!(ok = mbar_wait(&sm.st_full[ob], (ti >> 1) & 1, ab))) break;
             tc_fence_after();
-            const float inv = l > 0.f ? (kDtype == FP_DTYPE_E4M3 ? P.c_v : 1.f) / l : 0.f;
+            const float mx = sm.stat_m[ob][j], l = sm.stat_l[ob][j];
             uint32_t ov[4][32];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tO + q4 * 32, ov[q4]);
+            for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tmem + tlane + kColO + ob * 128 + q4 * 32, ov[q4]);
             tmem_ld_wait();
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) reg_fence32(ov[q4]);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.o_empty[x]);
+            if (lane == 0) mbar_arrive(&sm.o_empty[ob]);
             if (valid) {
+                const float inv = l > 0.f ? P.c_v / l : 0.f;
                 __nv_bfloat16 *orow = P.out + ((int64_t)(r.q_start + pos) * P.hq + head) * kHeadDim;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
@@ -674,9 +647,25 @@ __global__ void __launch_bounds__(kAThreads, 1)
                         *reinterpret_cast<uint4 *>(orow + q4 * 32 + e) = pk;
                     }
                 }
-                if (P.lse) P.lse[(int64_t)(r.q_start + pos) * P.hq + head] = (mx + log2f(l) - pshift) * 0.6931471805599453f;
+                if (P.lse)
+                    P.lse[(int64_t)(r.q_start + pos) * P.hq + head] = (mx + log2f(l) - pshift) * 0.6931471805599453f;
             }
-            ++ti;
+            s.next_tile(P);
+        }
+        // empty (but well-formed) segments of this CTA get zero rows
+        for (int w = blockIdx.x; w < P.nseg; w += gridDim.x) {
+            const int seg = P.work[w];
+            const SegMeta m = P.meta[seg];
+            if (m.n_exact != 0 || m.n_chunks != 0) continue;
+            const SegCoord sc = decode_seg(P.req, P.batch, g, seg);
+            const ReqInfo r = P.req[sc.b];
+            const int gr = sc.t * kTileRows + j;
+            if (j < sc.rows) {
+                const int64_t rowi = (int64_t)(r.q_start + gr / g) * P.hq + sc.h * g + gr % g;
+                for (int e = 0; e < kHeadDim; e += 8)
+                    *reinterpret_cast<uint4 *>(P.out + rowi * kHeadDim + e) = make_uint4(0, 0, 0, 0);
+                if (P.lse) P.lse[rowi] = -INFINITY;
+            }
         }
     }
 
@@ -744,8 +733,7 @@ cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, c
         if (!make_tmap(&tm_kb, kb, fp8, 3, dims, strides, box)) return cudaErrorInvalidValue;
         if (!make_tmap(&tm_vb, vb, fp8, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    // two tile slots per CTA: enough CTAs to give every slot work, at most one per SM
-    const int grid = (nseg + 1) / 2 < num_sms() ? (nseg + 1) / 2 : num_sms();
+    const int grid = nseg < num_sms() ? nseg : num_sms();
     AttnParams prm;
     prm.pt = c.p.page_table;
     prm.pt_stride = c.p.page_table_stride;
