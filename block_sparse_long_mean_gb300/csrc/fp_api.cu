@@ -61,7 +61,7 @@ WsLayout layout(const fp_problem *p, const Sizes &s) {
     w.req = o; o = align256(o + (int64_t)sizeof(ReqInfo) * (p->batch + 1));
     w.seg_count = o; o = align256(o + 4 * (s.nseg + 1));
     w.mask = o; o = align256(o + 4 * (s.mask_words + 1));
-    w.work = o; o = align256(o + 4 * (s.nseg + 1));
+    w.work = o; o = align256(o + (int64_t)sizeof(TileTask) * (s.nseg + 1));
     w.hist = o; o = align256(o + 4 * (int64_t)(kCostBuckets + 2));
     w.counters = o; o = align256(o + 4 * 64);
     w.kstat = o; o = align256(o + 8 * (s.nblocks * p->num_kv_heads + 1));

@@ -28,6 +28,24 @@ struct SegMeta {
     uint32_t chunk_hi;    // same for c in [32, 64)
 };
 
+// One entry of the Stage 2 work list (heaviest first): everything the
+// attention kernel needs about a segment, in one 64-byte record.
+struct alignas(16) TileTask {
+    int32_t n_exact;    // selected blocks walked exactly, -1 if the CSR is malformed
+    int32_t n_chunks;   // correction chunks
+    uint32_t chunk_lo, chunk_hi;
+    int32_t csr_end;    // CSR offset one past the segment's last entry
+    int32_t b, h, t;    // request, KV head, tile
+    int32_t D;          // diagonal block of the tile
+    int32_t rows;       // valid packed rows (<= 128)
+    int32_t q_start;    // first token of the request
+    int32_t len;        // request length
+    int32_t blk_base;   // first pooled-mean row of the request
+    int32_t pad;
+    int64_t todo;       // first word of the segment's correction bitmap
+};
+static_assert(sizeof(TileTask) == 64, "TileTask is one 64-byte record");
+
 // Per-request table, built on the device from cu_seqlens at the start of each
 // call (the host mirrors it from host_cu_seqlens only to size buffers).
 struct ReqInfo {
@@ -65,7 +83,7 @@ struct Ctx {
     ReqInfo *req() const { return reinterpret_cast<ReqInfo *>(wsbase + ws.req); }
     int32_t *seg_count() const { return reinterpret_cast<int32_t *>(wsbase + ws.seg_count); }
     uint32_t *mask() const { return reinterpret_cast<uint32_t *>(wsbase + ws.mask); }
-    int32_t *work() const { return reinterpret_cast<int32_t *>(wsbase + ws.work); }
+    TileTask *tasks() const { return reinterpret_cast<TileTask *>(wsbase + ws.work); }
     int32_t *hist() const { return reinterpret_cast<int32_t *>(wsbase + ws.hist); }
     int32_t *counters() const { return reinterpret_cast<int32_t *>(wsbase + ws.counters); }
     // per (pooled block, KV head): {|kbar - operand-format kbar|_2, |kbar|_2}

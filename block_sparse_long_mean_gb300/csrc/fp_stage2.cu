@@ -137,36 +137,73 @@ __global__ void __launch_bounds__(1024) attn_bucket_kernel(int32_t *__restrict__
     }
 }
 
-__global__ void __launch_bounds__(256) attn_scatter_kernel(const SegMeta *__restrict__ meta, int32_t nseg,
-                                                           int32_t *__restrict__ hist, int32_t *__restrict__ work,
+// Places every segment in the work list (descending cost) as a TileTask.
+__global__ void __launch_bounds__(256) attn_scatter_kernel(const ReqInfo *__restrict__ req, int batch, int g,
+                                                           const SegMeta *__restrict__ meta, int32_t nseg,
+                                                           const int32_t *__restrict__ cu, int flags,
+                                                           int32_t *__restrict__ hist, TileTask *__restrict__ tasks,
                                                            int32_t *__restrict__ status) {
     if (status_bad(status)) return;
     const int64_t seg = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (seg >= nseg) return;
     const SegMeta m = meta[seg];
     const int cost = m.n_exact < 0 ? 0 : min(m.n_exact + m.n_chunks, kCostBuckets - 1);
-    work[atomicAdd(&hist[cost], 1)] = (int32_t)seg;
+    const SegCoord sc = decode_seg(req, batch, g, seg);
+    const ReqInfo r = req[sc.b];
+    TileTask t;
+    t.n_exact = m.n_exact;
+    t.n_chunks = m.n_chunks;
+    t.chunk_lo = m.chunk_lo;
+    t.chunk_hi = m.chunk_hi;
+    t.csr_end = (flags & FP_DENSE) ? 0 : cu[seg + 1];
+    t.b = sc.b;
+    t.h = sc.h;
+    t.t = sc.t;
+    t.D = sc.D;
+    t.rows = sc.rows;
+    t.q_start = r.q_start;
+    t.len = r.len;
+    t.blk_base = r.blk_base;
+    t.pad = 0;
+    t.todo = (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
+    tasks[atomicAdd(&hist[cost], 1)] = t;
 }
 
 // --------------------------------------------------------------- attention
 
-// Warp roles (three warpgroups; registers rebalanced with setmaxnreg):
-//   warp 0      Q and K producer (TMA)     warp 1   MMA issuer + TMEM owner
-//   warp 2      V producer (TMA)           warp 3   idle
-//   warps 4-7   softmax, one thread per packed row
-//   warps 8-11  epilogue: O / l to bf16, LSE
-// TMEM: two S buffers (P of an iteration is written over its S), two O buffers.
-// The MMA warp issues QK^T of iteration i+1 before PV of iteration i, so the
-// tensor core computes the next scores while the softmax works on these.
-// Every tcgen05.mma of the CTA comes from one thread and executes in issue
-// order, so QK^T(i+2) may be issued right after PV(i), which read P(i) from
-// the same columns. O is double-buffered so one tile's epilogue overlaps the
-// next tile's PVs.
-constexpr int kAWarps = 12;
+// Warp roles (four warpgroups; registers rebalanced with setmaxnreg):
+//   warp 0      walker: walks the CTA's tiles, looks up the CSR, the page table
+//               and the correction masks in batches, and publishes one record
+//               per iteration in a shared-memory ring, up to kRing ahead
+//   warp 1      MMA issue + TMEM owner
+//   warp 2      loader: Q, K and V tiles by TMA, as stages free up
+//   warp 3      idle
+//   warps 4-11  softmax: each row of the tile is shared by two threads, warp w
+//               (columns 0-63) and warp w + 4 (columns 64-127), which exchange
+//               their partial row maxima each iteration
+//   warps 12-15 epilogue: O / l to bf16, LSE
+// Exp2 is the softmax's bound (one per score); two warps per scheduler hide
+// its latency, so the softmax of an iteration takes less time than its two
+// MMAs.
+// TMEM: two S buffers (P of an iteration is written over its S), one O
+// buffer and two Q buffers. Each tile's Q is copied from shared memory into
+// TMEM once (tcgen05.cp), so both MMAs take A from TMEM and read only K or V
+// from shared memory: at 128x128x16 per instruction, an MMA reading both
+// operands from shared memory would take all of its bandwidth.
+// The iterations of all the CTA's tiles form one stream. MMA group g issues
+// PV(g - 2) then QK^T(g), so the tensor core computes the next scores while
+// the softmax works on these. Every tcgen05 operation of the CTA comes from
+// one thread and executes in issue order, so QK^T(g) may write the columns
+// PV(g - 2) reads P from. The epilogue drains O while the next tile's first
+// QK^T and softmax run.
+constexpr int kAWarps = 16;
 constexpr int kAThreads = 32 * kAWarps;
 constexpr int kKStages = 3, kVStages = 2;
-constexpr uint32_t kColS = 0, kColO = 256;  // S_b at 128 b, O_o at 256 + 128 o
-constexpr int kRegsProducer = 56, kRegsSoftmax = 232, kRegsEpilogue = 160;  // 128 x (56 + 232 + 160) <= 384 x 168
+constexpr int kRing = 8;                    // iteration records in flight
+constexpr int kRingUsers = 10;              // MMA warp, 8 softmax warps, loader
+constexpr int32_t kRecEnd = -0x7fffffff;    // record after the CTA's last iteration
+constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;  // S_b at 128 b, O at 256, Q_b at 384 + 64 b
+constexpr int kRegsProducer = 80, kRegsSoftmax = 152, kRegsEpilogue = 128;  // 128 x (80 + 2 x 152 + 128) = 64K
 
 template <int kDtype>
 struct ACfg {
@@ -181,17 +218,47 @@ struct ACfg {
     static constexpr uint32_t kIdescPV = instr_desc(kFmt, kFmt, false, true, 128, 128);
 };
 
+// One pipeline iteration as the walker publishes it.
+struct alignas(16) IterRec {
+    int32_t J;      // block id; -1 - c for correction chunk c; kRecEnd after the last iteration
+    int32_t tile;   // the CTA's tile counter (selects the Q buffers)
+    int32_t flags;  // bit 0: first iteration of its tile, bit 1: last
+    int32_t row0;   // first packed row of the tile (t * 128)
+    int32_t D;      // diagonal block of the tile
+    int32_t h;      // KV head
+    int32_t q_pos;  // first token of the tile's positions (Q rows, for its first iteration)
+    int32_t len;    // request length
+    union {
+        int32_t rows[16];  // block: pool row of each page chunk
+        struct {
+            int32_t mrow;      // chunk: first pooled-mean row
+            int32_t pad[3];
+            uint32_t mask[4];  // chunk: which of its 128 means are corrected
+        } c;
+    } u;
+};
+
+// MMA group g: PV(g - 2) (when g >= 2 and that iteration exists) followed by
+// QK^T(g) (when iteration g exists), closed by one commit to grp[g % 4]; its
+// completion means S(g) is ready, K stage g % 3 and V stage (g - 2) % 2 are
+// free and O holds PV(g - 2).
+
 template <int kDtype>
 struct AttnSmem {
-    alignas(1024) uint8_t q[2][ACfg<kDtype>::kTile];
+    alignas(1024) uint8_t q[ACfg<kDtype>::kTile];
     alignas(1024) uint8_t k[kKStages][ACfg<kDtype>::kTile];
     alignas(1024) uint8_t v[kVStages][ACfg<kDtype>::kTile];
-    float stat_m[2][128], stat_l[2][128];  // per O buffer: running max (log2) and denominator of each row
-    uint64_t q_full[2], q_empty[2], k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages],
-        s_full[2], p_full[2], pv_done[2], o_full[2], o_empty[2], st_full[2];
+    float xmax[2][2][128];             // [iteration parity][column half][row]: partial row maxima
+    float stat_m[128], stat_l[2][128];  // a finished tile's running max (log2) and half-row denominators
+    IterRec ring[kRing];
+    uint8_t chunk_list[kMaxChunks];  // walker scratch: a tile's correction chunks, descending
+    uint64_t q_full, q_empty, k_full[kKStages], v_full[kVStages], grp[4], p_full[2], qk_done[2], o_full, o_empty,
+        st_full, rec_full[kRing], rec_empty[kRing], xbar[4][2];
     uint32_t tmem_base;
     int abort, skip;
 };
+
+static_assert(sizeof(AttnSmem<FP_DTYPE_BF16>) <= 232448, "attention shared memory exceeds the 227 KB opt-in limit");
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -199,82 +266,38 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-template <uint32_t kRegs>
-__device__ __forceinline__ void regs_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
-}
-template <uint32_t kRegs>
-__device__ __forceinline__ void regs_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+// Registers per thread at launch: 64K over the CTA's threads, rounded down to a multiple of 8.
+constexpr int kRegsLaunch = (65536 / kAThreads) & ~7;
+static_assert(kRegsProducer + 2 * kRegsSoftmax + kRegsEpilogue <= 4 * kRegsLaunch, "register split exceeds the launch");
+
+// Sets this warpgroup's register count: setmaxnreg.inc to grow, .dec to shrink
+// (a .dec to a larger count is not allowed), chosen at compile time.
+template <int kRegs>
+__device__ __forceinline__ void regs_set() {
+    static_assert(kRegs % 8 == 0 && kRegs >= 24 && kRegs <= 256, "setmaxnreg range");
+    if constexpr (kRegs > kRegsLaunch)
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+    else if constexpr (kRegs < kRegsLaunch)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
 // Kernel arguments besides the tensor maps (read from the constant bank).
 struct AttnParams {
     const int32_t *pt;  // page table
     int pt_stride, num_pages, page_size;
-    const int32_t *csr_cu, *csr_idx;
-    const SegMeta *meta;
-    const uint32_t *todo;  // per-segment correction bitmaps
-    const int32_t *work;   // segments, heaviest first
+    const int32_t *csr_idx;
+    const uint32_t *todo;    // per-segment correction bitmaps
+    const TileTask *tasks;   // work list, heaviest first
     __nv_bfloat16 *out;
     float *lse;
-    const ReqInfo *req;
-    int batch, hq, g, flags;
+    int hq, g, flags;
     float c_q, c_k, c_v;
     int32_t nseg;
     uint32_t smem_bytes;
     int32_t *status;
 };
 
-// Walk over this CTA's tiles (work items blockIdx.x + k gridDim.x, skipping
-// empty or malformed segments) and each tile's iterations: the selected blocks
-// in descending order (Eq.17), then the correction chunks.
-struct TileWalk {
-    int w, seg, n, it, n_exact;
-    SegCoord sc;
-    int32_t end;
-    uint64_t chunks;
-    bool live;
-    __device__ __forceinline__ void start(const AttnParams &a) {
-        w = (int)blockIdx.x - (int)gridDim.x;
-        n = it = 0;
-        live = true;
-        next_tile(a);
-    }
-    // moves to the next tile holding at least one iteration; live = false when none is left
-    __device__ __forceinline__ void next_tile(const AttnParams &a) {
-        for (;;) {
-            w += gridDim.x;
-            if (w >= a.nseg) {
-                live = false;
-                return;
-            }
-            seg = a.work[w];
-            const SegMeta m = a.meta[seg];
-            if (m.n_exact < 0 || m.n_exact + m.n_chunks == 0) continue;
-            sc = decode_seg(a.req, a.batch, a.g, seg);
-            n_exact = m.n_exact;
-            n = m.n_exact + m.n_chunks;
-            it = 0;
-            end = (a.flags & FP_DENSE) ? 0 : (int32_t)a.csr_cu[seg + 1];
-            chunks = ((uint64_t)m.chunk_hi << 32) | m.chunk_lo;
-            return;
-        }
-    }
-    // block id (>= 0) or correction chunk (-1 - c) of iteration `it`, then advances
-    __device__ __forceinline__ int take(const AttnParams &a) {
-        int J;
-        if (it < n_exact) {
-            J = (a.flags & FP_DENSE) ? sc.D - it : a.csr_idx[end - 1 - it];
-        } else {
-            const int c = 63 - __clzll((long long)chunks);
-            chunks &= ~(1ull << c);
-            J = -1 - c;
-        }
-        ++it;
-        return J;
-    }
-};
+__device__ __forceinline__ bool task_live(const TileTask &t) { return t.n_exact >= 0 && t.n_exact + t.n_chunks > 0; }
 
 template <int kDtype>
 __global__ void __launch_bounds__(kAThreads, 1)
@@ -295,22 +318,24 @@ __global__ void __launch_bounds__(kAThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.q_full[i], 1);
-            mbar_init(&sm.q_empty[i], 1);
-            mbar_init(&sm.s_full[i], 1);
-            mbar_init(&sm.p_full[i], 4);
-            mbar_init(&sm.pv_done[i], 1);
-            mbar_init(&sm.o_full[i], 1);
-            mbar_init(&sm.o_empty[i], 4);
-            mbar_init(&sm.st_full[i], 4);
+            mbar_init(&sm.p_full[i], 8);
+            mbar_init(&sm.qk_done[i], 1);
         }
-        for (int i = 0; i < kKStages; ++i) {
-            mbar_init(&sm.k_full[i], 1);
-            mbar_init(&sm.k_empty[i], 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&sm.grp[i], 1);
+            mbar_init(&sm.xbar[i][0], 2);
+            mbar_init(&sm.xbar[i][1], 2);
         }
-        for (int i = 0; i < kVStages; ++i) {
-            mbar_init(&sm.v_full[i], 1);
-            mbar_init(&sm.v_empty[i], 1);
+        mbar_init(&sm.q_full, 1);
+        mbar_init(&sm.q_empty, 1);
+        mbar_init(&sm.o_full, 1);
+        mbar_init(&sm.o_empty, 4);
+        mbar_init(&sm.st_full, 8);
+        for (int i = 0; i < kKStages; ++i) mbar_init(&sm.k_full[i], 1);
+        for (int i = 0; i < kVStages; ++i) mbar_init(&sm.v_full[i], 1);
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(&sm.rec_full[i], 1);
+            mbar_init(&sm.rec_empty[i], kRingUsers);
         }
         sm.abort = 0;
         // an earlier stage failed: every warp skips its role (one read, so the CTA agrees)
@@ -323,88 +348,244 @@ __global__ void __launch_bounds__(kAThreads, 1)
     tc_fence_after();
     const Abort ab{&sm.abort};
     const uint32_t tmem = sm.tmem_base;
+    const int ps_eff = min(P.page_size, 128);
+    const int npc = 128 / ps_eff;  // page chunks per 128-token block (<= 16 as page_size >= 8)
+    const int oob_row = P.num_pages * P.page_size;  // first row past the pool: TMA fills zeros
+    const bool dense = P.flags & FP_DENSE;
 
     if (sm.skip) {
     } else if (warp < 4) {
-        regs_dec<kRegsProducer>();
-        if (warp == 0 || warp == 2) {
-            // ------------------------------------------------ Q + K (warp 0) / V (warp 2) producer
-            const bool is_k = warp == 0;
+        regs_set<kRegsProducer>();
+        if (warp == 0) {
+            // ------------------------------------------------------------------------ walker
+            uint32_t gi = 0;
+            bool ok = true;
+            // publishes iteration gi; `row` is this lane's page-chunk row (lane % npc) for a block
+            auto emit = [&](int J, int flags, int tile, const TileTask &tk, uint4 mk, int row) -> bool {
+                const int slot = gi % kRing;
+                if (!mbar_wait(&sm.rec_empty[slot], ((gi / kRing) & 1) ^ 1, ab)) return false;
+                IterRec &rc = sm.ring[slot];
+                if (J >= 0 && J != kRecEnd && lane < 16) rc.u.rows[lane] = row;
+                if (lane == 0) {
+                    rc.J = J;
+                    rc.tile = tile;
+                    rc.flags = flags;
+                    rc.row0 = tk.t * kTileRows;
+                    rc.D = tk.D;
+                    rc.h = tk.h;
+                    rc.q_pos = tk.q_start + (tk.t * kTileRows) / g;
+                    rc.len = tk.len;
+                    if (J < 0 && J != kRecEnd) {
+                        rc.u.c.mrow = tk.blk_base + 128 * (-1 - J);
+                        rc.u.c.mask[0] = mk.x;
+                        rc.u.c.mask[1] = mk.y;
+                        rc.u.c.mask[2] = mk.z;
+                        rc.u.c.mask[3] = mk.w;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.rec_full[slot]);
+                ++gi;
+                return true;
+            };
+            const int per = 32 / npc;  // block lookups per batch
+            uint32_t ti = 0;
+            int w = blockIdx.x;
+            TileTask cur;
+            if (w < P.nseg) cur = P.tasks[w];
+            while (w < P.nseg && ok) {
+                const int wn = w + gridDim.x;
+                TileTask nxt;
+                if (wn < P.nseg) nxt = P.tasks[wn];  // overlaps this tile
+                if (task_live(cur)) {
+                    const int n = cur.n_exact + cur.n_chunks;
+                    int it = 0;
+                    // selected blocks, descending (Eq.17): lane l looks up block base + l / npc, page chunk l % npc
+                    for (int bs = 0; bs < cur.n_exact && ok; bs += per) {
+                        const int my = bs + lane / npc, pc = lane % npc;
+                        int Jl = 0, rowl = oob_row;
+                        if (my < cur.n_exact) {
+                            Jl = dense ? cur.D - my : __ldg(P.csr_idx + cur.csr_end - 1 - my);
+                            const int tok = Jl * kBlock + pc * ps_eff;
+                            if (tok < cur.len) {
+                                const int page = __ldg(P.pt + (int64_t)cur.b * P.pt_stride + tok / P.page_size);
+                                if (page >= 0 && page < P.num_pages)
+                                    rowl = page * P.page_size + tok % P.page_size;
+                                else
+                                    set_status(status, FP_ERR_DEVICE_PAGE, page);
+                            }
+                        }
+                        const int cnt = min(per, cur.n_exact - bs);
+                        for (int i = 0; i < cnt; ++i, ++it) {
+                            const int J = __shfl_sync(0xffffffffu, Jl, i * npc);
+                            const int row = __shfl_sync(0xffffffffu, rowl, i * npc + pc);
+                            const int fl = (it == 0 ? 1 : 0) | (it == n - 1 ? 2 : 0);
+                            if (!(ok = emit(J, fl, (int)ti, cur, make_uint4(0, 0, 0, 0), row))) break;
+                        }
+                    }
+                    // correction chunks, descending: list them, then look up 32 masks at a time
+                    if (cur.n_chunks > 0 && ok) {
+                        const uint32_t hi = cur.chunk_hi, lo = cur.chunk_lo;
+                        const unsigned below = (1u << lane) - 1u;
+                        const bool in_hi = (hi >> (31 - lane)) & 1u, in_lo = (lo >> (31 - lane)) & 1u;
+                        const unsigned bhi = __ballot_sync(0xffffffffu, in_hi), blo = __ballot_sync(0xffffffffu, in_lo);
+                        // lane l stands for bits 31 - l: its rank counts the set bits above it
+                        if (in_hi) sm.chunk_list[__popc(bhi & below)] = (uint8_t)(63 - lane);
+                        if (in_lo) sm.chunk_list[__popc(hi) + __popc(blo & below)] = (uint8_t)(31 - lane);
+                        __syncwarp();
+                        const int nw = (cur.D + 31) / 32;
+                        for (int bs = 0; bs < cur.n_chunks && ok; bs += 32) {
+                            int cl = 0;
+                            uint4 ml = make_uint4(0, 0, 0, 0);
+                            if (bs + lane < cur.n_chunks) {
+                                cl = sm.chunk_list[bs + lane];
+                                const uint32_t *tw = P.todo + cur.todo + 4 * cl;
+                                ml.x = 4 * cl + 0 < nw ? __ldg(tw + 0) : 0u;
+                                ml.y = 4 * cl + 1 < nw ? __ldg(tw + 1) : 0u;
+                                ml.z = 4 * cl + 2 < nw ? __ldg(tw + 2) : 0u;
+                                ml.w = 4 * cl + 3 < nw ? __ldg(tw + 3) : 0u;
+                            }
+                            const int cnt = min(32, cur.n_chunks - bs);
+                            for (int i = 0; i < cnt; ++i, ++it) {
+                                const int c = __shfl_sync(0xffffffffu, cl, i);
+                                uint4 mk;
+                                mk.x = __shfl_sync(0xffffffffu, ml.x, i);
+                                mk.y = __shfl_sync(0xffffffffu, ml.y, i);
+                                mk.z = __shfl_sync(0xffffffffu, ml.z, i);
+                                mk.w = __shfl_sync(0xffffffffu, ml.w, i);
+                                const int fl = (it == 0 ? 1 : 0) | (it == n - 1 ? 2 : 0);
+                                if (!(ok = emit(-1 - c, fl, (int)ti, cur, mk, 0))) break;
+                            }
+                        }
+                        __syncwarp();
+                    }
+                    ++ti;
+                }
+                cur = nxt;
+                w = wn;
+            }
+            if (ok) emit(kRecEnd, 0, 0, cur, make_uint4(0, 0, 0, 0), 0);
+        } else if (warp == 2) {
+            // ------------------------------------------------------------------------ loader
             if (lane == 0) {
-                if (is_k) tma_prefetch_desc(&tm_q);
-                tma_prefetch_desc(is_k ? &tm_k : &tm_v);
-                tma_prefetch_desc(is_k ? &tm_kb : &tm_vb);
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
+                tma_prefetch_desc(&tm_kb);
+                tma_prefetch_desc(&tm_vb);
             }
-            const int ps_eff = min(P.page_size, 128);
-            const int npc = 128 / ps_eff;                   // page chunks per 128-token block
-            const int oob_row = P.num_pages * P.page_size;  // first row past the pool: TMA fills zeros
-            const int nst = is_k ? kKStages : kVStages;
-            uint64_t *fullb = is_k ? sm.k_full : sm.v_full;
-            uint64_t *emptyb = is_k ? sm.k_empty : sm.v_empty;
-            TileWalk s;
-            s.start(P);
-            uint32_t gi = 0;
-            bool ok = true;
-            for (uint32_t ti = 0; s.live && ok; ++ti) {
-                const ReqInfo r = P.req[s.sc.b];
-                const int h = s.sc.h, b = s.sc.b;
-                if (is_k) {
-                    const int qb = ti & 1;
-                    if (!(ok = mbar_wait(&sm.q_empty[qb], ((ti >> 1) & 1) ^ 1, ab))) break;
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(&sm.q_full[qb], C::kTile);
-                        const int pos0 = r.q_start + (s.sc.t * kTileRows) / g;
-                        for (int i = 0; i < C::kBoxes; ++i)
-                            tma_load_4d(sm.q[qb] + i * 16384, &tm_q, &sm.q_full[qb], i * C::kBoxElems, 0, h, pos0);
-                    }
+            // a block (J >= 0: lane L < kBoxes npc copies d box L / npc of page chunk L % npc) or 128 means
+            auto load = [&](const CUtensorMap *tm_pages, const CUtensorMap *tm_means, uint8_t *dst, uint64_t *bar,
+                            int J, int h, int row) {
+                if (lane == 0) mbar_arrive_expect_tx(bar, C::kTile);
+                __syncwarp();
+                if (J >= 0) {
+                    if (lane < C::kBoxes * npc)
+                        tma_load_3d(dst + (lane / npc) * 16384 + (lane % npc) * ps_eff * 128, tm_pages, bar,
+                                    (lane / npc) * C::kBoxElems, h, row);
+                } else if (lane < C::kBoxes) {
+                    tma_load_3d(dst + lane * 16384, tm_means, bar, lane * C::kBoxElems, h, row);
                 }
-                const int n = s.n;
-                for (int it = 0; it < n; ++it, ++gi) {
-                    const int J = s.take(P);
-                    // lane l < kBoxes * npc (<= 32 as page_size >= 8) copies page chunk l % npc of d box l / npc;
-                    // its page row is looked up before waiting for the slot
-                    int row = oob_row;
-                    if (J >= 0 && lane < C::kBoxes * npc) {
-                        const int tok = J * kBlock + (lane % npc) * ps_eff;
-                        if (tok < r.len) {
-                            const int page = P.pt[(int64_t)b * P.pt_stride + tok / P.page_size];
-                            if (page >= 0 && page < P.num_pages)
-                                row = page * P.page_size + tok % P.page_size;
-                            else
-                                set_status(status, FP_ERR_DEVICE_PAGE, page);
+            };
+            // V of the previous iteration, issued one step behind K (V is needed one MMA group later)
+            int pJ = kRecEnd, ph = 0, prow = 0;
+            for (uint32_t gi = 0;; ++gi) {
+                const int slot = gi % kRing;
+                if (!mbar_wait(&sm.rec_full[slot], (gi / kRing) & 1, ab)) break;
+                const IterRec &rc = sm.ring[slot];
+                const int J = rc.J, h = rc.h, fl = rc.flags, tile = rc.tile, q_pos = rc.q_pos;
+                const int row = J >= 0 ? rc.u.rows[lane % npc] : rc.u.c.mrow;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.rec_empty[slot]);
+                if (J != kRecEnd) {
+                    if (fl & 1) {
+                        // the shared Q buffer is free once the previous tile's Q was copied into TMEM
+                        if (!mbar_wait(&sm.q_empty, (tile & 1) ^ 1, ab)) break;
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(&sm.q_full, C::kTile);
+                            for (int i = 0; i < C::kBoxes; ++i)
+                                tma_load_4d(sm.q + i * 16384, &tm_q, &sm.q_full, i * C::kBoxElems, 0, h, q_pos);
                         }
                     }
-                    const int st = gi % nst;
-                    if (!(ok = mbar_wait(&emptyb[st], ((gi / nst) & 1) ^ 1, ab))) break;
-                    if (lane == 0) mbar_arrive_expect_tx(&fullb[st], C::kTile);
-                    __syncwarp();
-                    uint8_t *dst = is_k ? sm.k[st] : sm.v[st];
-                    if (J >= 0) {
-                        if (lane < C::kBoxes * npc) {
-                            const int box = lane / npc, pc = lane % npc;
-                            tma_load_3d(dst + box * 16384 + pc * ps_eff * 128, is_k ? &tm_k : &tm_v, &fullb[st],
-                                        box * C::kBoxElems, h, row);
-                        }
-                    } else if (lane < C::kBoxes) {
-                        tma_load_3d(dst + lane * 16384, is_k ? &tm_kb : &tm_vb, &fullb[st], lane * C::kBoxElems, h,
-                                    r.blk_base + 128 * (-1 - J));
-                    }
+                    // K stage gi % 3 was last read by QK^T(gi - 3), closed by group gi - 3
+                    if (gi >= kKStages && !mbar_wait(&sm.grp[(gi - 3) & 3], ((gi - 3) >> 2) & 1, ab)) break;
+                    load(&tm_k, &tm_kb, sm.k[gi % kKStages], &sm.k_full[gi % kKStages], J, h, row);
                 }
-                s.next_tile(P);
+                if (gi >= 1 && pJ != kRecEnd) {
+                    // V stage vi % kVStages was last read by PV(vi - kVStages), closed by group vi - kVStages + 2
+                    const uint32_t vi = gi - 1, gv = vi + 2 - kVStages;
+                    if (vi >= kVStages && !mbar_wait(&sm.grp[gv & 3], (gv >> 2) & 1, ab)) break;
+                    load(&tm_v, &tm_vb, sm.v[vi % kVStages], &sm.v_full[vi % kVStages], pJ, ph, prow);
+                }
+                if (J == kRecEnd) break;
+                pJ = J;
+                ph = h;
+                prow = row;
             }
-        } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------------------------ MMA issue
-            TileWalk s;
-            s.start(P);
-            uint32_t gi = 0;
-            bool ok = true;
-            // O_ob (+)= P(i) V(i); the first PV of a tile overwrites O_ob once its previous epilogue read it
-            auto issue_pv = [&](uint32_t i, bool first, int ob, uint32_t ti) -> bool {
+        } else if (warp == 1) {
+            // ------------------------------------------------------------------------- MMA
+            // Group g = PV(g - 2) then QK^T(g), one commit. Per iteration i the warp reads the record
+            // of iteration i + 2 and takes every wait of group i + 2 except the softmax's P(i) first
+            // (they are normally long satisfied), then waits for P(i) and issues the group at once.
+            // The tensor core holds about one queued MMA, so waits between groups leave it idle. The
+            // whole warp runs the loop (operands stay warp-uniform); one elected lane issues.
+            struct It {
+                int tile, fl;
+                bool valid;
+            };
+            // a wait whose outcome is the same in every lane (an abort seen by one lane ends them all),
+            // so the warp stays converged for elect.sync
+            auto wait_w = [&](uint64_t *bar, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait_spin(bar, parity, ab));
+            };
+            uint32_t nrec = 0;  // next record to read
+            auto fetch = [&](It &x) -> bool {
+                const int slot = nrec % kRing;
+                if (!wait_w(&sm.rec_full[slot], (nrec / kRing) & 1)) return false;
+                const int J = sm.ring[slot].J;
+                x.tile = sm.ring[slot].tile;
+                x.fl = sm.ring[slot].flags;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.rec_empty[slot]);
+                x.valid = J != kRecEnd;
+                if (x.valid) ++nrec;
+                return true;
+            };
+            // QK^T(gi) of x: its Q (a new tile), the QK^Ts of tile - 2 done with TMEM Q buffer, its K block
+            auto qk_ready = [&](uint32_t gi, const It &x) -> bool {
+                if (x.fl & 1) {
+                    if (!wait_w(&sm.q_full, x.tile & 1)) return false;
+                    if (!wait_w(&sm.qk_done[x.tile & 1], ((x.tile >> 1) & 1) ^ 1)) return false;
+                }
+                return wait_w(&sm.k_full[gi % kKStages], (gi / kKStages) & 1);
+            };
+            auto issue_qk = [&](uint32_t gi, const It &x) {
+                const int ks = gi % kKStages, sb = gi & 1, qb = x.tile & 1;
+                const uint32_t tq = tmem + kColQ + qb * 64;
+                if (x.fl & 1) {
+                    // a new tile: copy its Q into TMEM buffer qb (last read by the QK^Ts of tile - 2)
+                    const uint32_t qbase = smem_addr(sm.q);
+#pragma unroll
+                    for (int k = 0; k < C::kNumK; ++k)
+                        tmem_cp_128x256b(tq + k * 8, sw128_desc(qbase + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024));
+                    umma_commit(&sm.q_empty);
+                }
+                const uint32_t kbase = smem_addr(sm.k[ks]);
+#pragma unroll
+                for (int k = 0; k < C::kNumK; ++k) {
+                    // A = Q from TMEM (K step k: 32 bytes = 8 columns), B = K rows in shared memory
+                    const uint64_t bd = sw128_desc(kbase + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+                    if (kDtype == FP_DTYPE_BF16)
+                        umma_f16_ts(tmem + kColS + sb * 128, tq + k * 8, bd, C::kIdescQK, k > 0);
+                    else
+                        umma_f8_ts(tmem + kColS + sb * 128, tq + k * 8, bd, C::kIdescQK, k > 0);
+                }
+                if (x.fl & 2) umma_commit(&sm.qk_done[qb]);
+            };
+            // O (+)= P(i) V(i); a tile's first PV overwrites O
+            auto issue_pv = [&](uint32_t i, const It &x) {
                 const int vs = i % kVStages, pb = i & 1;
-                if (first && !mbar_wait(&sm.o_empty[ob], ((ti >> 1) & 1) ^ 1, ab)) return false;
-                if (!mbar_wait(&sm.v_full[vs], (i / kVStages) & 1, ab)) return false;
-                if (!mbar_wait(&sm.p_full[pb], (i >> 1) & 1, ab)) return false;
-                tc_fence_after();
+                const bool first = x.fl & 1;
                 const uint32_t vbase = smem_addr(sm.v[vs]);
 #pragma unroll
                 for (int k = 0; k < C::kNumK; ++k) {
@@ -413,259 +594,283 @@ __global__ void __launch_bounds__(kAThreads, 1)
                     const uint32_t a = tmem + kColS + pb * 128 + k * (C::kKStep * C::kEb / 4);
                     const uint32_t acc = (!first || k > 0) ? 1u : 0u;
                     if (kDtype == FP_DTYPE_BF16)
-                        umma_f16_ts(tmem + kColO + ob * 128, a, bd, C::kIdescPV, acc);
+                        umma_f16_ts(tmem + kColO, a, bd, C::kIdescPV, acc);
                     else
-                        umma_f8_ts(tmem + kColO + ob * 128, a, bd, C::kIdescPV, acc);
+                        umma_f8_ts(tmem + kColO, a, bd, C::kIdescPV, acc);
                 }
-                umma_commit(&sm.v_empty[vs]);
-                umma_commit(&sm.pv_done[pb]);
-                return true;
+                if (x.fl & 2) umma_commit(&sm.o_full);
             };
-            for (uint32_t ti = 0; s.live && ok; ++ti) {
-                const int qb = ti & 1, ob = ti & 1;
-                const int n = s.n;
-                if (!(ok = mbar_wait(&sm.q_full[qb], (ti >> 1) & 1, ab))) break;
-                const uint32_t qbase = smem_addr(sm.q[qb]);
-                for (int it = 0; it < n; ++it, ++gi) {
-                    const int ks = gi % kKStages, sb = gi & 1;
-                    if (!(ok = mbar_wait(&sm.k_full[ks], (gi / kKStages) & 1, ab))) break;
+            It a, b, c;
+            a.valid = b.valid = false;
+            bool ok = fetch(a);
+            if (ok && a.valid && (ok = qk_ready(0, a)) && elect_one()) {  // group 0
+                tc_fence_after();
+                issue_qk(0, a);
+                umma_commit(&sm.grp[0]);
+            }
+            __syncwarp();
+            if (ok && a.valid) ok = fetch(b);
+            if (ok && b.valid && (ok = qk_ready(1, b)) && elect_one()) {  // group 1
+                tc_fence_after();
+                issue_qk(1, b);
+                umma_commit(&sm.grp[1]);
+            }
+            __syncwarp();
+            for (uint32_t i = 0; ok && a.valid; ++i) {
+                // group i + 2: PV(i), then QK^T(i + 2) if that iteration exists
+                c.valid = false;
+                if (b.valid && !(ok = fetch(c))) break;
+                if (c.valid && !(ok = qk_ready(i + 2, c))) break;
+                if ((a.fl & 1) && !(ok = wait_w(&sm.o_empty, (a.tile & 1) ^ 1))) break;
+                if (!(ok = wait_w(&sm.v_full[i % kVStages], (i / kVStages) & 1))) break;
+                if (!(ok = wait_w(&sm.p_full[i & 1], (i >> 1) & 1))) break;
+                if (elect_one()) {
                     tc_fence_after();
-                    const uint32_t kbase = smem_addr(sm.k[ks]);
-#pragma unroll
-                    for (int k = 0; k < C::kNumK; ++k) {
-                        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                        const uint64_t ad = sw128_desc(qbase + off, 16, 1024);
-                        const uint64_t bd = sw128_desc(kbase + off, 16, 1024);
-                        if (kDtype == FP_DTYPE_BF16)
-                            umma_f16_ss(tmem + kColS + sb * 128, ad, bd, C::kIdescQK, k > 0);
-                        else
-                            umma_f8_ss(tmem + kColS + sb * 128, ad, bd, C::kIdescQK, k > 0);
-                    }
-                    umma_commit(&sm.k_empty[ks]);
-                    umma_commit(&sm.s_full[sb]);
-                    if (it == n - 1) umma_commit(&sm.q_empty[qb]);
-                    if (it >= 1 && !(ok = issue_pv(gi - 1, it == 1, ob, ti))) break;
+                    issue_pv(i, a);
+                    if (c.valid) issue_qk(i + 2, c);
+                    umma_commit(&sm.grp[(i + 2) & 3]);
                 }
-                if (!ok) break;
-                if (!(ok = issue_pv(gi - 1, n == 1, ob, ti))) break;
-                umma_commit(&sm.o_full[ob]);
-                s.next_tile(P);
+                __syncwarp();
+                a = b;
+                b = c;
             }
         }
-    } else if (warp < 8) {
-        regs_inc<kRegsSoftmax>();
+    } else if (warp < 12) {
+        regs_set<kRegsSoftmax>();
         // -------------------------------------------------------------------------- softmax
-        const int j = 32 * (warp & 3) + lane;  // TMEM lane = packed row of the tile
-        const uint32_t tlane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        const int quarter = warp & 3, half = (warp - 4) >> 2;
+        const int j = 32 * quarter + lane;  // TMEM lane = packed row of the tile
+        const int cb = 64 * half;           // this thread's 64 columns of S (keys) and of O (d)
+        const uint32_t tlane = static_cast<uint32_t>(32 * quarter) << 16;
         const float LOG2E = 1.4426950408889634f;
         const float sl2 = P.c_q * P.c_k * LOG2E * rsqrtf((float)kHeadDim);
         // lazy rescale slack (log2 units): bf16 P may reach 2^8; FP8 P~ must stay within [0, 256]
         const float tau = kDtype == FP_DTYPE_E4M3 ? 0.f : 8.f;
         const float pshift = kDtype == FP_DTYPE_E4M3 ? 8.f : 0.f;  // FP8 probabilities in [0, 256] (Eq.15)
-        TileWalk s;
-        s.start(P);
-        uint32_t gi = 0;
-        bool ok = true;
-        for (uint32_t ti = 0; s.live && ok; ++ti) {
-            const int ob = ti & 1;
-            const SegCoord sc = s.sc;
-            const ReqInfo r = P.req[sc.b];
-            const int pos = (sc.t * kTileRows + j) / g;
-            const uint32_t *tw = P.todo + (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
-            const int nw = (sc.D + 31) / 32;
-            const int n = s.n;
-            const uint32_t tO = tmem + tlane + kColO + ob * 128;
-            float mx = -INFINITY, l = 0.f;
-            for (int it = 0; it < n; ++it, ++gi) {
-                const int sb = gi & 1;
-                const uint32_t tS = tmem + tlane + kColS + sb * 128;
-                const int J = s.take(P);
-                uint4 mv = make_uint4(0, 0, 0, 0);  // correction-chunk key mask
-                if (J < 0) {
-                    const int c = -1 - J;
-                    uint32_t wv[4];
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) wv[q4] = (4 * c + q4 < nw) ? __ldg(tw + 4 * c + q4) : 0u;
-                    mv = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                }
-                if (!(ok = mbar_wait(&sm.s_full[sb], (gi >> 1) & 1, ab))) break;
-                tc_fence_after();
-                uint32_t sv[4][32];
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tS + q4 * 32, sv[q4]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) reg_fence32(sv[q4]);
-                // pass 1: mask and row maximum of the raw dot products
-                float pm[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-                const float shift = J < 0 ? 7.f : 0.f;  // log2 |B_J| of a full 128-token block for means
-                const bool plain = J >= 0 ? J != sc.D : (mv.x & mv.y & mv.z & mv.w) == 0xffffffffu;
-                if (plain) {
-                    // every key takes part (a block off the diagonal, or a chunk with no selected block)
-#pragma unroll
-                    for (int e = 0; e < 128; e += 2)
-                        pm[(e >> 1) & 7] = fmax3(pm[(e >> 1) & 7], __uint_as_float(sv[e >> 5][e & 31]),
-                                                 __uint_as_float(sv[e >> 5][(e & 31) + 1]));
-                } else if (J >= 0) {
-                    const int lim = pos - J * kBlock;  // causal mask on the diagonal block
-#pragma unroll
-                    for (int e = 0; e < 128; ++e) {
-                        const float v = e <= lim ? __uint_as_float(sv[e >> 5][e & 31]) : -INFINITY;
-                        sv[e >> 5][e & 31] = __float_as_uint(v);
-                        pm[e & 7] = fmaxf(pm[e & 7], v);
-                    }
-                } else {
-                    const uint32_t wv[4] = {mv.x, mv.y, mv.z, mv.w};
-#pragma unroll
-                    for (int e = 0; e < 128; ++e) {
-                        const float v = (wv[e >> 5] >> (e & 31)) & 1u ? __uint_as_float(sv[e >> 5][e & 31]) : -INFINITY;
-                        sv[e >> 5][e & 31] = __float_as_uint(v);
-                        pm[e & 7] = fmaxf(pm[e & 7], v);
-                    }
-                }
-                const float rmax = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
-                const float tmax = fmaf(rmax, sl2, shift);
-                // online softmax with lazy rescaling of O
-                const bool first = it == 0;
-                const bool grow = first || tmax > mx + tau;
-                const float m_new = grow ? fmaxf(mx, tmax) : mx;
-                const bool need_o = !first && grow;
-                if (__any_sync(0xffffffffu, need_o)) {
-                    // O holds the sum up to iteration it-1: wait for that PV, then rescale it in TMEM
-                    const uint32_t prev = gi - 1;
-                    if (!(ok = mbar_wait(&sm.pv_done[prev & 1], (prev >> 1) & 1, ab))) break;
-                    tc_fence_after();
-                    const float f = need_o ? ex2(mx - m_new) : 1.f;
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t ov[32];
-                        tmem_ld32(tO + q4 * 32, ov);
-                        tmem_ld_wait();
-                        reg_fence32(ov);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-                        tmem_st32(tO + q4 * 32, ov);
-                    }
-                }
-                if (!first) l *= ex2(mx - m_new);
-                mx = m_new;
-                // pass 2: p = 2^(x - m) (FP8: 2^(x - m + 8)), row sum, P packed in place and written over S
-                const float off = shift - mx + pshift;
-                float ps4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t *w32 = sv[q4];
-                    if (kDtype == FP_DTYPE_BF16) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float p0 = ex2(fmaf(__uint_as_float(w32[2 * e]), sl2, off));
-                            const float p1 = ex2(fmaf(__uint_as_float(w32[2 * e + 1]), sl2, off));
-                            ps4[e & 3] += p0 + p1;
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-                            w32[e] = *reinterpret_cast<const uint32_t *>(&b2);
-                        }
-                        tmem_st16(tS + q4 * 16, w32);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            uint32_t word = 0;
-#pragma unroll
-                            for (int b4 = 0; b4 < 4; b4 += 2) {
-                                const float p0 = ex2(fmaf(__uint_as_float(w32[4 * e + b4]), sl2, off));
-                                const float p1 = ex2(fmaf(__uint_as_float(w32[4 * e + b4 + 1]), sl2, off));
-                                const __nv_fp8x2_e4m3 q2(make_float2(p0, p1));
-                                const float2 back = float2(q2);  // Eq.15: the denominator sums the quantised values
-                                ps4[e & 3] += back.x + back.y;
-                                word |= (uint32_t)(*reinterpret_cast<const uint16_t *>(&q2)) << (8 * b4);
-                            }
-                            w32[e] = word;
-                        }
-                        tmem_st8(tS + q4 * 8, w32);
-                    }
-                }
-                l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.p_full[sb]);
-            }
-            if (!ok) break;
-            // hand the row statistics to the epilogue (its previous use of this buffer must be done)
-            if (!(ok = mbar_wait(&sm.o_empty[ob], ((ti >> 1) & 1) ^ 1, ab))) break;
-            sm.stat_m[ob][j] = mx;
-            sm.stat_l[ob][j] = l;
+        const int gshift = __ffs(g) - 1;                            // g is a power of two
+        float mx = -INFINITY, l = 0.f;
+        for (uint32_t gi = 0;; ++gi) {
+            const int slot = gi % kRing;
+            if (!mbar_wait(&sm.rec_full[slot], (gi / kRing) & 1, ab)) break;
+            const IterRec &rc = sm.ring[slot];
+            const int J = rc.J, fl = rc.flags, D = rc.D, tile = rc.tile;
+            const int pos = (rc.row0 + j) >> gshift;
+            const uint32_t mw0 = J < 0 ? rc.u.c.mask[2 * half] : 0u, mw1 = J < 0 ? rc.u.c.mask[2 * half + 1] : 0u;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.st_full[ob]);
-            s.next_tile(P);
+            if (lane == 0) mbar_arrive(&sm.rec_empty[slot]);
+            if (J == kRecEnd) break;
+            const int sb = gi & 1;
+            const uint32_t tS = tmem + tlane + kColS + sb * 128;
+            const uint32_t tO = tmem + tlane + kColO + cb;
+            const bool first = fl & 1;
+            if (first) {
+                mx = -INFINITY;
+                l = 0.f;
+            }
+            if (!mbar_wait(&sm.grp[gi & 3], (gi >> 2) & 1, ab)) break;  // group gi computed S(gi)
+            tc_fence_after();
+            uint32_t sv[2][32];
+            tmem_ld32(tS + cb, sv[0]);
+            tmem_ld32(tS + cb + 32, sv[1]);
+            tmem_ld_wait();
+            reg_fence32(sv[0]);
+            reg_fence32(sv[1]);
+            // pass 1: mask and partial row maximum of the raw dot products
+            float pm[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+            const float shift = J < 0 ? 7.f : 0.f;  // log2 |B_J| of a full 128-token block for means
+            const bool plain = J >= 0 ? J != D : (mw0 & mw1) == 0xffffffffu;
+            if (plain) {
+                // every key takes part (a block off the diagonal, or chunk means with no selected block)
+#pragma unroll
+                for (int e = 0; e < 64; e += 2)
+                    pm[(e >> 1) & 7] = fmax3(pm[(e >> 1) & 7], __uint_as_float(sv[e >> 5][e & 31]),
+                                             __uint_as_float(sv[e >> 5][(e & 31) + 1]));
+            } else if (J >= 0) {
+                const int lim = pos - J * kBlock - cb;  // causal mask on the diagonal block
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    const float v = e <= lim ? __uint_as_float(sv[e >> 5][e & 31]) : -INFINITY;
+                    sv[e >> 5][e & 31] = __float_as_uint(v);
+                    pm[e & 7] = fmaxf(pm[e & 7], v);
+                }
+            } else {
+                const uint32_t wv[2] = {mw0, mw1};
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    const float v = (wv[e >> 5] >> (e & 31)) & 1u ? __uint_as_float(sv[e >> 5][e & 31]) : -INFINITY;
+                    sv[e >> 5][e & 31] = __float_as_uint(v);
+                    pm[e & 7] = fmaxf(pm[e & 7], v);
+                }
+            }
+            float rmax = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+            // the other half-row's maximum: exchanged through shared memory, one mbarrier phase per
+            // iteration for each pair of warps
+            {
+                const int xp = gi & 1;
+                sm.xmax[xp][half][j] = rmax;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.xbar[quarter][xp]);
+                if (!mbar_wait(&sm.xbar[quarter][xp], (gi >> 1) & 1, ab)) break;
+                rmax = fmaxf(rmax, sm.xmax[xp][half ^ 1][j]);
+            }
+            const float tmax = fmaf(rmax, sl2, shift);
+            // online softmax with lazy rescaling of O
+            const bool grow = first || tmax > mx + tau;
+            const float m_new = grow ? fmaxf(mx, tmax) : mx;
+            const bool need_o = !first && grow;
+            if (__any_sync(0xffffffffu, need_o)) {
+                // O holds the sum up to iteration gi-1 of this tile: wait for that PV (in group gi + 1),
+                // then rescale this thread's half of it in TMEM
+                if (!mbar_wait(&sm.grp[(gi + 1) & 3], ((gi + 1) >> 2) & 1, ab)) break;
+                tc_fence_after();
+                const float f = need_o ? ex2(mx - m_new) : 1.f;
+                const uint64_t f2 = f2pack(f, f);
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + q2 * 32, ov);
+                    tmem_ld_wait();
+                    reg_fence32(ov);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float a, b2;
+                        f2unpack(fmul2(f2pack(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), f2), a, b2);
+                        ov[e] = __float_as_uint(a);
+                        ov[e + 1] = __float_as_uint(b2);
+                    }
+                    tmem_st32(tO + q2 * 32, ov);
+                }
+            }
+            if (!first) l *= ex2(mx - m_new);
+            mx = m_new;
+            // pass 2: p = 2^(x - m) (FP8: 2^(x - m + 8)), half-row sum, P packed in place and written over
+            // this half's part of S
+            const float off = shift - mx + pshift;
+            const uint64_t sl2x2 = f2pack(sl2, sl2), offx2 = f2pack(off, off);
+            uint64_t acc2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t *w32 = sv[q2];
+                if (kDtype == FP_DTYPE_BF16) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float y0, y1;
+                        f2unpack(ffma2(f2pack(__uint_as_float(w32[2 * e]), __uint_as_float(w32[2 * e + 1])), sl2x2,
+                                       offx2),
+                                 y0, y1);
+                        const float p0 = ex2(y0), p1 = ex2(y1);
+                        acc2[e & 1] = fadd2(acc2[e & 1], f2pack(p0, p1));
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+                        w32[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                    }
+                    // keys cb + 32 q2 .. : bf16 pairs in columns (cb + 32 q2) / 2 ..
+                    tmem_st16(tS + (cb >> 1) + q2 * 16, w32);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        uint32_t word = 0;
+#pragma unroll
+                        for (int b4 = 0; b4 < 4; b4 += 2) {
+                            const float p0 = ex2(fmaf(__uint_as_float(w32[4 * e + b4]), sl2, off));
+                            const float p1 = ex2(fmaf(__uint_as_float(w32[4 * e + b4 + 1]), sl2, off));
+                            const __nv_fp8x2_e4m3 q2v(make_float2(p0, p1));
+                            const float2 back = float2(q2v);  // Eq.15: the denominator sums the quantised values
+                            acc2[e & 1] = fadd2(acc2[e & 1], f2pack(back.x, back.y));
+                            word |= (uint32_t)(*reinterpret_cast<const uint16_t *>(&q2v)) << (8 * b4);
+                        }
+                        w32[e] = word;
+                    }
+                    // keys cb + 32 q2 .. : four e4m3 per column, from column (cb + 32 q2) / 4
+                    tmem_st8(tS + (cb >> 2) + q2 * 8, w32);
+                }
+            }
+            float s0, s1, s2, s3;
+            f2unpack(acc2[0], s0, s1);
+            f2unpack(acc2[1], s2, s3);
+            l += (s0 + s1) + (s2 + s3);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.p_full[sb]);
+            if (fl & 2) {
+                // hand the row statistics to the epilogue once it has finished the previous tile
+                if (!mbar_wait(&sm.o_empty, (tile & 1) ^ 1, ab)) break;
+                if (half == 0) sm.stat_m[j] = mx;
+                sm.stat_l[half][j] = l;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.st_full);
+            }
         }
     } else {
-        regs_dec<kRegsEpilogue>();
+        regs_set<kRegsEpilogue>();
         // ------------------------------------------------------------------------- epilogue
         const int j = 32 * (warp & 3) + lane;
         const uint32_t tlane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         const float pshift = kDtype == FP_DTYPE_E4M3 ? 8.f : 0.f;
-        TileWalk s;
-        s.start(P);
         bool ok = true;
-        for (uint32_t ti = 0; s.live && ok; ++ti) {
-            const int ob = ti & 1;
-            const SegCoord sc = s.sc;
-            const ReqInfo r = P.req[sc.b];
-            const int gr = sc.t * kTileRows + j;
-            const int pos = gr / g, head = sc.h * g + gr % g;
-            const bool valid = j < sc.rows;
-            if (!(ok = mbar_wait(&sm.o_full[ob], (ti >> 1) & 1, ab))) break;
-            if (!(ok = mbar_wait(&sm.st_full[ob], (ti >> 1) & 1, ab))) break;
-            tc_fence_after();
-            const float mx = sm.stat_m[ob][j], l = sm.stat_l[ob][j];
-            uint32_t ov[4][32];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tmem + tlane + kColO + ob * 128 + q4 * 32, ov[q4]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) reg_fence32(ov[q4]);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.o_empty[ob]);
-            if (valid) {
+        uint32_t ti = 0;
+        int w = blockIdx.x;
+        TileTask cur;
+        if (w < P.nseg) cur = P.tasks[w];
+        while (w < P.nseg && ok) {
+            const int wn = w + gridDim.x;
+            TileTask nxt;
+            if (wn < P.nseg) nxt = P.tasks[wn];
+            const int gr = cur.t * kTileRows + j;
+            const int64_t rowi = (int64_t)(cur.q_start + gr / g) * P.hq + cur.h * g + gr % g;
+            const bool valid = j < cur.rows;
+            if (task_live(cur)) {
+                if (!(ok = mbar_wait(&sm.o_full, ti & 1, ab))) break;
+                if (!(ok = mbar_wait(&sm.st_full, ti & 1, ab))) break;
+                tc_fence_after();
+                const float mx = sm.stat_m[j], l = sm.stat_l[0][j] + sm.stat_l[1][j];
                 const float inv = l > 0.f ? P.c_v / l : 0.f;
-                __nv_bfloat16 *orow = P.out + ((int64_t)(r.q_start + pos) * P.hq + head) * kHeadDim;
+                __nv_bfloat16 *orow = P.out + rowi * kHeadDim;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    uint32_t ov[2][32];
+                    tmem_ld32(tmem + tlane + kColO + q2 * 64, ov[0]);
+                    tmem_ld32(tmem + tlane + kColO + q2 * 64 + 32, ov[1]);
+                    tmem_ld_wait();
+                    reg_fence32(ov[0]);
+                    reg_fence32(ov[1]);
+                    if (q2 == 1) {
+                        // O is in registers: the next tile's PVs may overwrite it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sm.o_empty);
+                    }
+                    if (valid) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 pk;
-                        uint32_t *pw = reinterpret_cast<uint32_t *>(&pk);
+                        for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(
-                                __uint_as_float(ov[q4][e + 2 * u]) * inv, __uint_as_float(ov[q4][e + 2 * u + 1]) * inv);
-                            pw[u] = *reinterpret_cast<const uint32_t *>(&b2);
+                            for (int e = 0; e < 32; e += 8) {
+                                uint4 pk;
+                                uint32_t *pw = reinterpret_cast<uint32_t *>(&pk);
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const __nv_bfloat162 b2 =
+                                        __floats2bfloat162_rn(__uint_as_float(ov[hh][e + 2 * u]) * inv,
+                                                              __uint_as_float(ov[hh][e + 2 * u + 1]) * inv);
+                                    pw[u] = *reinterpret_cast<const uint32_t *>(&b2);
+                                }
+                                *reinterpret_cast<uint4 *>(orow + q2 * 64 + hh * 32 + e) = pk;
+                            }
                         }
-                        *reinterpret_cast<uint4 *>(orow + q4 * 32 + e) = pk;
                     }
                 }
-                if (P.lse)
-                    P.lse[(int64_t)(r.q_start + pos) * P.hq + head] = (mx + log2f(l) - pshift) * 0.6931471805599453f;
-            }
-            s.next_tile(P);
-        }
-        // empty (but well-formed) segments of this CTA get zero rows
-        for (int w = blockIdx.x; w < P.nseg; w += gridDim.x) {
-            const int seg = P.work[w];
-            const SegMeta m = P.meta[seg];
-            if (m.n_exact != 0 || m.n_chunks != 0) continue;
-            const SegCoord sc = decode_seg(P.req, P.batch, g, seg);
-            const ReqInfo r = P.req[sc.b];
-            const int gr = sc.t * kTileRows + j;
-            if (j < sc.rows) {
-                const int64_t rowi = (int64_t)(r.q_start + gr / g) * P.hq + sc.h * g + gr % g;
+                if (valid && P.lse) P.lse[rowi] = (mx + log2f(l) - pshift) * 0.6931471805599453f;
+                ++ti;
+            } else if (cur.n_exact == 0 && cur.n_chunks == 0 && valid) {
+                // a well-formed segment with nothing to attend: zero rows
                 for (int e = 0; e < kHeadDim; e += 8)
                     *reinterpret_cast<uint4 *>(P.out + rowi * kHeadDim + e) = make_uint4(0, 0, 0, 0);
                 if (P.lse) P.lse[rowi] = -INFINITY;
             }
+            cur = nxt;
+            w = wn;
         }
     }
 
@@ -701,7 +906,8 @@ cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, c
                                                             capacity, flags, c.meta(), c.mask(), c.hist(),
                                                             c.status());
     attn_bucket_kernel<<<1, 1024, 0, c.stream>>>(c.hist(), c.status());
-    attn_scatter_kernel<<<(nseg + 255) / 256, 256, 0, c.stream>>>(c.meta(), nseg, c.hist(), c.work(), c.status());
+    attn_scatter_kernel<<<(nseg + 255) / 256, 256, 0, c.stream>>>(c.req(), c.p.batch, c.s.g, c.meta(), nseg, csr_cu,
+                                                                   flags, c.hist(), c.tasks(), c.status());
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     const bool fp8 = c.p.dtype == FP_DTYPE_E4M3;
@@ -739,15 +945,11 @@ cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, c
     prm.pt_stride = c.p.page_table_stride;
     prm.num_pages = c.p.num_pages;
     prm.page_size = c.p.page_size;
-    prm.csr_cu = csr_cu;
     prm.csr_idx = csr_idx;
-    prm.meta = c.meta();
     prm.todo = c.mask();
-    prm.work = c.work();
+    prm.tasks = c.tasks();
     prm.out = (__nv_bfloat16 *)out;
     prm.lse = lse;
-    prm.req = c.req();
-    prm.batch = c.p.batch;
     prm.hq = hq;
     prm.g = g;
     prm.flags = flags;

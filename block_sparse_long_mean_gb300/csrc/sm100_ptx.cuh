@@ -23,6 +23,31 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return r;
 }
 
+// Packed fp32 pairs (one 64-bit register pair, two lanes of work per instruction).
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -50,6 +75,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Non-blocking probe: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -70,14 +107,94 @@ struct Abort {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 
+// One lane of a fully active warp (the same one each time: the lowest). Issuing
+// tcgen05 instructions from a whole warp under elect.sync, rather than from a
+// lane branched off on its own, keeps their operands in warp-uniform registers;
+// from a lone lane the issue of each MMA costs tens of cycles more.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t p;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(p));
+    return p != 0;
+}
+
+// Shared-memory counter handoff between two threads of the CTA.
+__device__ __forceinline__ void st_release_shared(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_shared(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
 // Waits for the phase with the given parity to complete. Returns false (and
 // sets the CTA's abort flag) if the limit expires or another role aborted.
+// A non-blocking probe comes first: mbarrier.try_wait costs tens of cycles
+// even on a completed phase, and in the thread that issues tcgen05.mma that
+// time leaves the tensor core idle.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Abort ab) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 0) {
+            if (*ab.flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *ab.flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Same, polling with the non-blocking probe only: for the MMA-issuing thread,
+// which must notice a completed phase as early as possible.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, Abort ab) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test(bar, parity)) return true;
+        if ((it & 255) == 0) {
+            if (*ab.flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *ab.flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Spins until *p > n (bounded like the mbarrier waits).
+__device__ __forceinline__ bool spin_above(const uint32_t *p, uint32_t n, Abort ab) {
+    if (ld_acquire_shared(p) > n) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ld_acquire_shared(p) > n) return true;
+        if ((it & 255) == 0) {
+            if (*ab.flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *ab.flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Spins until the group word at p carries sequence number g + 1 (bits 11-30,
+// mod 2^20); returns it in w. Bounded like the mbarrier waits.
+__device__ __forceinline__ bool spin_group(const uint32_t *p, uint32_t g, uint32_t &w, Abort ab) {
+    const uint32_t want = (g + 1) & 0xfffffu;
+    w = ld_acquire_shared(p);
+    if ((w >> 11) == want) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        w = ld_acquire_shared(p);
+        if ((w >> 11) == want) return true;
+        if ((it & 255) == 0) {
             if (*ab.flag) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 *ab.flag = 1;
@@ -184,6 +301,12 @@ __device__ __forceinline__ void umma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uin
 }
 
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far has completed.
+// Copies a 128-row x 32-byte slice of a shared-memory matrix (described like an
+// MMA operand) into TMEM: row r to lane r, 8 consecutive 32-bit columns.
+// Asynchronous, in issue order with the thread's tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_addr(bar))
