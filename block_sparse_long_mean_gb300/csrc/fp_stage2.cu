@@ -601,7 +601,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 if (x.fl & 2) umma_commit(&sm.o_full);
             };
             It a, b, c;
-            a.valid = b.valid = false;
+            a.valid = b.valid = c.valid = false;
             bool ok = fetch(a);
             if (ok && a.valid && (ok = qk_ready(0, a)) && elect_one()) {  // group 0
                 tc_fence_after();
@@ -616,23 +616,38 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 umma_commit(&sm.grp[1]);
             }
             __syncwarp();
+            if (ok && b.valid) ok = fetch(c);
             for (uint32_t i = 0; ok && a.valid; ++i) {
-                // group i + 2: PV(i), then QK^T(i + 2) if that iteration exists
-                c.valid = false;
-                if (b.valid && !(ok = fetch(c))) break;
-                if (c.valid && !(ok = qk_ready(i + 2, c))) break;
-                if ((a.fl & 1) && !(ok = wait_w(&sm.o_empty, (a.tile & 1) ^ 1))) break;
-                if (!(ok = wait_w(&sm.v_full[i % kVStages], (i / kVStages) & 1))) break;
+                // group i + 2: PV(i), then QK^T(i + 2) if that iteration exists. Its inputs other than
+                // P(i) are probed together (the probes' latencies overlap); only a missing one is waited for.
+                const uint32_t i2 = i + 2;
+                bool ready = mbar_test(&sm.v_full[i % kVStages], (i / kVStages) & 1);
+                if (a.fl & 1) ready &= mbar_test(&sm.o_empty, (a.tile & 1) ^ 1);
+                if (c.valid) {
+                    ready &= mbar_test(&sm.k_full[i2 % kKStages], (i2 / kKStages) & 1);
+                    if (c.fl & 1)
+                        ready &= mbar_test(&sm.q_full, c.tile & 1) &
+                                 mbar_test(&sm.qk_done[c.tile & 1], ((c.tile >> 1) & 1) ^ 1);
+                }
+                if (!__all_sync(0xffffffffu, ready)) {
+                    if (c.valid && !(ok = qk_ready(i2, c))) break;
+                    if ((a.fl & 1) && !(ok = wait_w(&sm.o_empty, (a.tile & 1) ^ 1))) break;
+                    if (!(ok = wait_w(&sm.v_full[i % kVStages], (i / kVStages) & 1))) break;
+                }
                 if (!(ok = wait_w(&sm.p_full[i & 1], (i >> 1) & 1))) break;
                 if (elect_one()) {
                     tc_fence_after();
                     issue_pv(i, a);
-                    if (c.valid) issue_qk(i + 2, c);
-                    umma_commit(&sm.grp[(i + 2) & 3]);
+                    if (c.valid) issue_qk(i2, c);
+                    umma_commit(&sm.grp[i2 & 3]);
                 }
                 __syncwarp();
+                // the record of iteration i + 3, read while the group's last MMAs run
+                const bool more = c.valid;
                 a = b;
                 b = c;
+                c.valid = false;
+                if (more && !(ok = fetch(c))) break;
             }
         }
     } else if (warp < 12) {
