@@ -178,9 +178,8 @@ __global__ void __launch_bounds__(256) attn_scatter_kernel(const ReqInfo *__rest
 //   warp 1      MMA issue + TMEM owner
 //   warp 2      loader: Q, K and V tiles by TMA, as stages free up
 //   warp 3      idle
-//   warps 4-11  softmax: each row of the tile is shared by two threads, warp w
-//               (columns 0-63) and warp w + 4 (columns 64-127), which exchange
-//               their partial row maxima each iteration
+//   warps 4-11  softmax: each warp owns 16 rows of the tile, each row spread
+//               over the 4 threads of a quad (two rows per thread)
 //   warps 12-15 epilogue: O / l to bf16, LSE
 // Exp2 is the softmax's bound (one per score); two warps per scheduler hide
 // its latency, so the softmax of an iteration takes less time than its two
@@ -198,12 +197,12 @@ __global__ void __launch_bounds__(256) attn_scatter_kernel(const ReqInfo *__rest
 // QK^T and softmax run.
 constexpr int kAWarps = 16;
 constexpr int kAThreads = 32 * kAWarps;
-constexpr int kKStages = 3, kVStages = 2;
+constexpr int kKStages = 3, kVStages = 3;
 constexpr int kRing = 8;                    // iteration records in flight
 constexpr int kRingUsers = 10;              // MMA warp, 8 softmax warps, loader
 constexpr int32_t kRecEnd = -0x7fffffff;    // record after the CTA's last iteration
 constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;  // S_b at 128 b, O at 256, Q_b at 384 + 64 b
-constexpr int kRegsProducer = 80, kRegsSoftmax = 152, kRegsEpilogue = 128;  // 128 x (80 + 2 x 152 + 128) = 64K
+constexpr int kRegsProducer = 80, kRegsSoftmax = 160, kRegsEpilogue = 112;  // 128 x (80 + 2 x 160 + 112) = 64K
 
 template <int kDtype>
 struct ACfg {
@@ -240,7 +239,7 @@ struct alignas(16) IterRec {
 
 // MMA group g: PV(g - 2) (when g >= 2 and that iteration exists) followed by
 // QK^T(g) (when iteration g exists), closed by one commit to grp[g % 4]; its
-// completion means S(g) is ready, K stage g % 3 and V stage (g - 2) % 2 are
+// completion means S(g) is ready, K stage g % 3 and V stage (g - 2) % 3 are
 // free and O holds PV(g - 2).
 
 template <int kDtype>
@@ -248,12 +247,11 @@ struct AttnSmem {
     alignas(1024) uint8_t q[ACfg<kDtype>::kTile];
     alignas(1024) uint8_t k[kKStages][ACfg<kDtype>::kTile];
     alignas(1024) uint8_t v[kVStages][ACfg<kDtype>::kTile];
-    float xmax[2][2][128];             // [iteration parity][column half][row]: partial row maxima
-    float stat_m[128], stat_l[2][128];  // a finished tile's running max (log2) and half-row denominators
+    float stat_m[128], stat_l[128];    // a finished tile's running max (log2) and denominator per row
     IterRec ring[kRing];
     uint8_t chunk_list[kMaxChunks];  // walker scratch: a tile's correction chunks, descending
     uint64_t q_full, q_empty, k_full[kKStages], v_full[kVStages], grp[4], p_full[2], qk_done[2], o_full, o_empty,
-        st_full, rec_full[kRing], rec_empty[kRing], xbar[4][2];
+        st_full, rec_full[kRing], rec_empty[kRing];
     uint32_t tmem_base;
     int abort, skip;
 };
@@ -321,11 +319,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
             mbar_init(&sm.p_full[i], 8);
             mbar_init(&sm.qk_done[i], 1);
         }
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(&sm.grp[i], 1);
-            mbar_init(&sm.xbar[i][0], 2);
-            mbar_init(&sm.xbar[i][1], 2);
-        }
+        for (int i = 0; i < 4; ++i) mbar_init(&sm.grp[i], 1);
         mbar_init(&sm.q_full, 1);
         mbar_init(&sm.q_empty, 1);
         mbar_init(&sm.o_full, 1);
@@ -653,167 +647,215 @@ __global__ void __launch_bounds__(kAThreads, 1)
     } else if (warp < 12) {
         regs_set<kRegsSoftmax>();
         // -------------------------------------------------------------------------- softmax
-        const int quarter = warp & 3, half = (warp - 4) >> 2;
-        const int j = 32 * quarter + lane;  // TMEM lane = packed row of the tile
-        const int cb = 64 * half;           // this thread's 64 columns of S (keys) and of O (d)
-        const uint32_t tlane = static_cast<uint32_t>(32 * quarter) << 16;
+        // Warp w owns 16 rows of the tile, lanes 32 (w % 4) + 16 sub .. + 15 (TMEM lane = packed row).
+        // Thread t holds rows ra = t/4 and rb = t/4 + 8 of them and, of every 8 keys, the two at
+        // 2 (t % 4): a row's 128 scores are spread over the 4 threads of a quad, whose row maxima
+        // and sums combine with two shuffles.
+        const int quarter = warp & 3, sub = (warp - 4) >> 2;
+        const int c4 = lane & 3;
+        const int ra = 32 * quarter + 16 * sub + (lane >> 2), rb = ra + 8;  // rows of the tile
+        const uint32_t tlane = static_cast<uint32_t>(32 * quarter + 16 * sub) << 16;
         const float LOG2E = 1.4426950408889634f;
         const float sl2 = P.c_q * P.c_k * LOG2E * rsqrtf((float)kHeadDim);
         // lazy rescale slack (log2 units): bf16 P may reach 2^8; FP8 P~ must stay within [0, 256]
         const float tau = kDtype == FP_DTYPE_E4M3 ? 0.f : 8.f;
         const float pshift = kDtype == FP_DTYPE_E4M3 ? 8.f : 0.f;  // FP8 probabilities in [0, 256] (Eq.15)
         const int gshift = __ffs(g) - 1;                            // g is a power of two
-        float mx = -INFINITY, l = 0.f;
+        float mxa = -INFINITY, mxb = -INFINITY, la = 0.f, lb = 0.f;  // per row; l partial over this thread's keys
         for (uint32_t gi = 0;; ++gi) {
             const int slot = gi % kRing;
             if (!mbar_wait(&sm.rec_full[slot], (gi / kRing) & 1, ab)) break;
             const IterRec &rc = sm.ring[slot];
-            const int J = rc.J, fl = rc.flags, D = rc.D, tile = rc.tile;
-            const int pos = (rc.row0 + j) >> gshift;
-            const uint32_t mw0 = J < 0 ? rc.u.c.mask[2 * half] : 0u, mw1 = J < 0 ? rc.u.c.mask[2 * half + 1] : 0u;
+            const int J = rc.J, fl = rc.flags, D = rc.D, tile = rc.tile, row0 = rc.row0;
+            uint4 mw = make_uint4(0, 0, 0, 0);
+            if (J < 0) mw = make_uint4(rc.u.c.mask[0], rc.u.c.mask[1], rc.u.c.mask[2], rc.u.c.mask[3]);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.rec_empty[slot]);
             if (J == kRecEnd) break;
             const int sb = gi & 1;
             const uint32_t tS = tmem + tlane + kColS + sb * 128;
-            const uint32_t tO = tmem + tlane + kColO + cb;
+            const uint32_t tO = tmem + tlane + kColO;
             const bool first = fl & 1;
             if (first) {
-                mx = -INFINITY;
-                l = 0.f;
+                mxa = mxb = -INFINITY;
+                la = lb = 0.f;
             }
             if (!mbar_wait(&sm.grp[gi & 3], (gi >> 2) & 1, ab)) break;  // group gi computed S(gi)
             tc_fence_after();
+            // sv[h][4k + e] (k < 8): key 64 h + 8k + 2 c4 + (e & 1), row ra (e < 2) or rb (e >= 2)
             uint32_t sv[2][32];
-            tmem_ld32(tS + cb, sv[0]);
-            tmem_ld32(tS + cb + 32, sv[1]);
+            tmem_ld_16x256b_x8(tS, sv[0]);
+            tmem_ld_16x256b_x8(tS + 64, sv[1]);
             tmem_ld_wait();
             reg_fence32(sv[0]);
             reg_fence32(sv[1]);
-            // pass 1: mask and partial row maximum of the raw dot products
-            float pm[8];
+            // pass 1: mask and row maxima of the raw dot products
+            float pa[4], pb[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+            for (int u = 0; u < 4; ++u) pa[u] = pb[u] = -INFINITY;
             const float shift = J < 0 ? 7.f : 0.f;  // log2 |B_J| of a full 128-token block for means
-            const bool plain = J >= 0 ? J != D : (mw0 & mw1) == 0xffffffffu;
+            const bool plain = J >= 0 ? J != D : (mw.x & mw.y & mw.z & mw.w) == 0xffffffffu;
             if (plain) {
                 // every key takes part (a block off the diagonal, or chunk means with no selected block)
 #pragma unroll
-                for (int e = 0; e < 64; e += 2)
-                    pm[(e >> 1) & 7] = fmax3(pm[(e >> 1) & 7], __uint_as_float(sv[e >> 5][e & 31]),
-                                             __uint_as_float(sv[e >> 5][(e & 31) + 1]));
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        pa[k & 3] = fmax3(pa[k & 3], __uint_as_float(sv[h][4 * k]), __uint_as_float(sv[h][4 * k + 1]));
+                        pb[k & 3] = fmax3(pb[k & 3], __uint_as_float(sv[h][4 * k + 2]), __uint_as_float(sv[h][4 * k + 3]));
+                    }
             } else if (J >= 0) {
-                const int lim = pos - J * kBlock - cb;  // causal mask on the diagonal block
+                // causal mask on the diagonal block: key <= position - 128 J
+                const int lima = ((row0 + ra) >> gshift) - J * kBlock - 2 * c4;
+                const int limb = ((row0 + rb) >> gshift) - J * kBlock - 2 * c4;
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    const float v = e <= lim ? __uint_as_float(sv[e >> 5][e & 31]) : -INFINITY;
-                    sv[e >> 5][e & 31] = __float_as_uint(v);
-                    pm[e & 7] = fmaxf(pm[e & 7], v);
-                }
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int kk = 64 * h + 8 * k + (e & 1);  // key - 2 c4
+                            const bool keep = kk <= ((e < 2) ? lima : limb);
+                            const float v = keep ? __uint_as_float(sv[h][4 * k + e]) : -INFINITY;
+                            sv[h][4 * k + e] = __float_as_uint(v);
+                            if (e < 2) pa[k & 3] = fmaxf(pa[k & 3], v);
+                            else pb[k & 3] = fmaxf(pb[k & 3], v);
+                        }
             } else {
-                const uint32_t wv[2] = {mw0, mw1};
+                // correction chunk: keep the means of pruned blocks only
+                const uint32_t wv[4] = {mw.x >> (2 * c4), mw.y >> (2 * c4), mw.z >> (2 * c4), mw.w >> (2 * c4)};
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                    const float v = (wv[e >> 5] >> (e & 31)) & 1u ? __uint_as_float(sv[e >> 5][e & 31]) : -INFINITY;
-                    sv[e >> 5][e & 31] = __float_as_uint(v);
-                    pm[e & 7] = fmaxf(pm[e & 7], v);
-                }
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            // key 64 h + 8 k + 2 c4 + (e & 1): word 2 h + k / 4, bit 8 (k % 4) + 2 c4 + (e & 1)
+                            const bool keep = (wv[2 * h + (k >> 2)] >> (8 * (k & 3) + (e & 1))) & 1u;
+                            const float v = keep ? __uint_as_float(sv[h][4 * k + e]) : -INFINITY;
+                            sv[h][4 * k + e] = __float_as_uint(v);
+                            if (e < 2) pa[k & 3] = fmaxf(pa[k & 3], v);
+                            else pb[k & 3] = fmaxf(pb[k & 3], v);
+                        }
             }
-            float rmax = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
-            // the other half-row's maximum: exchanged through shared memory, one mbarrier phase per
-            // iteration for each pair of warps
-            {
-                const int xp = gi & 1;
-                sm.xmax[xp][half][j] = rmax;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.xbar[quarter][xp]);
-                if (!mbar_wait(&sm.xbar[quarter][xp], (gi >> 1) & 1, ab)) break;
-                rmax = fmaxf(rmax, sm.xmax[xp][half ^ 1][j]);
-            }
-            const float tmax = fmaf(rmax, sl2, shift);
+            float rma = fmaxf(fmaxf(pa[0], pa[1]), fmaxf(pa[2], pa[3]));
+            float rmb = fmaxf(fmaxf(pb[0], pb[1]), fmaxf(pb[2], pb[3]));
+            rma = fmaxf(rma, __shfl_xor_sync(0xffffffffu, rma, 1));
+            rmb = fmaxf(rmb, __shfl_xor_sync(0xffffffffu, rmb, 1));
+            rma = fmaxf(rma, __shfl_xor_sync(0xffffffffu, rma, 2));
+            rmb = fmaxf(rmb, __shfl_xor_sync(0xffffffffu, rmb, 2));
+            const float tma = fmaf(rma, sl2, shift), tmb = fmaf(rmb, sl2, shift);
             // online softmax with lazy rescaling of O
-            const bool grow = first || tmax > mx + tau;
-            const float m_new = grow ? fmaxf(mx, tmax) : mx;
-            const bool need_o = !first && grow;
+            const bool growa = first || tma > mxa + tau, growb = first || tmb > mxb + tau;
+            const float mna = growa ? fmaxf(mxa, tma) : mxa, mnb = growb ? fmaxf(mxb, tmb) : mxb;
+            const bool need_o = !first && (growa || growb);
             if (__any_sync(0xffffffffu, need_o)) {
                 // O holds the sum up to iteration gi-1 of this tile: wait for that PV (in group gi + 1),
-                // then rescale this thread's half of it in TMEM
+                // then rescale this thread's part of its two rows in TMEM
                 if (!mbar_wait(&sm.grp[(gi + 1) & 3], ((gi + 1) >> 2) & 1, ab)) break;
                 tc_fence_after();
-                const float f = need_o ? ex2(mx - m_new) : 1.f;
-                const uint64_t f2 = f2pack(f, f);
+                const float fa = (!first && growa) ? ex2(mxa - mna) : 1.f;
+                const float fb = (!first && growb) ? ex2(mxb - mnb) : 1.f;
+                const uint64_t f2a = f2pack(fa, fa), f2b = f2pack(fb, fb);
 #pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
+                for (int h = 0; h < 2; ++h) {
                     uint32_t ov[32];
-                    tmem_ld32(tO + q2 * 32, ov);
+                    tmem_ld_16x256b_x8(tO + 64 * h, ov);
                     tmem_ld_wait();
                     reg_fence32(ov);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float a, b2;
-                        f2unpack(fmul2(f2pack(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])), f2), a, b2);
-                        ov[e] = __float_as_uint(a);
-                        ov[e + 1] = __float_as_uint(b2);
+                    for (int k = 0; k < 8; ++k) {
+                        float x0, x1;
+                        f2unpack(fmul2(f2pack(__uint_as_float(ov[4 * k]), __uint_as_float(ov[4 * k + 1])), f2a), x0, x1);
+                        ov[4 * k] = __float_as_uint(x0);
+                        ov[4 * k + 1] = __float_as_uint(x1);
+                        f2unpack(fmul2(f2pack(__uint_as_float(ov[4 * k + 2]), __uint_as_float(ov[4 * k + 3])), f2b), x0, x1);
+                        ov[4 * k + 2] = __float_as_uint(x0);
+                        ov[4 * k + 3] = __float_as_uint(x1);
                     }
-                    tmem_st32(tO + q2 * 32, ov);
+                    tmem_st_16x256b_x8(tO + 64 * h, ov);
                 }
             }
-            if (!first) l *= ex2(mx - m_new);
-            mx = m_new;
-            // pass 2: p = 2^(x - m) (FP8: 2^(x - m + 8)), half-row sum, P packed in place and written over
-            // this half's part of S
-            const float off = shift - mx + pshift;
-            const uint64_t sl2x2 = f2pack(sl2, sl2), offx2 = f2pack(off, off);
-            uint64_t acc2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+            if (!first) {
+                la *= ex2(mxa - mna);
+                lb *= ex2(mxb - mnb);
+            }
+            mxa = mna;
+            mxb = mnb;
+            // pass 2: p = 2^(x - m) (FP8: 2^(x - m + 8)), partial row sums, P packed and written over S
+            const float offa = shift - mxa + pshift, offb = shift - mxb + pshift;
+            const uint64_t sl2x2 = f2pack(sl2, sl2), offa2 = f2pack(offa, offa), offb2 = f2pack(offb, offb);
+            uint64_t acca = f2pack(0.f, 0.f), accb = f2pack(0.f, 0.f);
+            if (kDtype == FP_DTYPE_BF16) {
+                // P word 2k (k < 16) = keys 8k + 2 c4, +1 of row ra, word 2k + 1 the same of row rb:
+                // exactly the .16x128b layout of P columns 4k + c4
+                uint32_t pw[32];
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t *w32 = sv[q2];
-                if (kDtype == FP_DTYPE_BF16) {
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        float y0, y1;
-                        f2unpack(ffma2(f2pack(__uint_as_float(w32[2 * e]), __uint_as_float(w32[2 * e + 1])), sl2x2,
-                                       offx2),
+                    for (int k = 0; k < 8; ++k) {
+                        float y0, y1, y2, y3;
+                        f2unpack(ffma2(f2pack(__uint_as_float(sv[h][4 * k]), __uint_as_float(sv[h][4 * k + 1])), sl2x2, offa2),
                                  y0, y1);
-                        const float p0 = ex2(y0), p1 = ex2(y1);
-                        acc2[e & 1] = fadd2(acc2[e & 1], f2pack(p0, p1));
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-                        w32[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                        f2unpack(ffma2(f2pack(__uint_as_float(sv[h][4 * k + 2]), __uint_as_float(sv[h][4 * k + 3])), sl2x2,
+                                       offb2),
+                                 y2, y3);
+                        const float p0 = ex2(y0), p1 = ex2(y1), p2 = ex2(y2), p3 = ex2(y3);
+                        acca = fadd2(acca, f2pack(p0, p1));
+                        accb = fadd2(accb, f2pack(p2, p3));
+                        const __nv_bfloat162 ba = __floats2bfloat162_rn(p0, p1), bb = __floats2bfloat162_rn(p2, p3);
+                        pw[2 * (8 * h + k)] = *reinterpret_cast<const uint32_t *>(&ba);
+                        pw[2 * (8 * h + k) + 1] = *reinterpret_cast<const uint32_t *>(&bb);
                     }
-                    // keys cb + 32 q2 .. : bf16 pairs in columns (cb + 32 q2) / 2 ..
-                    tmem_st16(tS + (cb >> 1) + q2 * 16, w32);
-                } else {
+                tmem_st_16x128b_x16(tS, pw);
+            } else {
+                // four e4m3 per column: column 2k + c4 / 2 holds keys 8k + 4 (c4 / 2) .. + 3, of row ra for an
+                // even c4 (own pair + the odd neighbour's) and of row rb for an odd c4 (.16x64b layout)
+                uint32_t pw[16];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        uint32_t word = 0;
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                        for (int b4 = 0; b4 < 4; b4 += 2) {
-                            const float p0 = ex2(fmaf(__uint_as_float(w32[4 * e + b4]), sl2, off));
-                            const float p1 = ex2(fmaf(__uint_as_float(w32[4 * e + b4 + 1]), sl2, off));
-                            const __nv_fp8x2_e4m3 q2v(make_float2(p0, p1));
-                            const float2 back = float2(q2v);  // Eq.15: the denominator sums the quantised values
-                            acc2[e & 1] = fadd2(acc2[e & 1], f2pack(back.x, back.y));
-                            word |= (uint32_t)(*reinterpret_cast<const uint16_t *>(&q2v)) << (8 * b4);
-                        }
-                        w32[e] = word;
+                    for (int k = 0; k < 8; ++k) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sv[h][4 * k]), sl2, offa));
+                        const float p1 = ex2(fmaf(__uint_as_float(sv[h][4 * k + 1]), sl2, offa));
+                        const float p2 = ex2(fmaf(__uint_as_float(sv[h][4 * k + 2]), sl2, offb));
+                        const float p3 = ex2(fmaf(__uint_as_float(sv[h][4 * k + 3]), sl2, offb));
+                        const __nv_fp8x2_e4m3 qa(make_float2(p0, p1)), qb(make_float2(p2, p3));
+                        const float2 fa2 = float2(qa), fb2 = float2(qb);  // Eq.15: the sum uses the quantised values
+                        acca = fadd2(acca, f2pack(fa2.x, fa2.y));
+                        accb = fadd2(accb, f2pack(fb2.x, fb2.y));
+                        const uint32_t ua = *reinterpret_cast<const uint16_t *>(&qa);
+                        const uint32_t ub = *reinterpret_cast<const uint16_t *>(&qb);
+                        const uint32_t give = (c4 & 1) ? ua : ub;
+                        const uint32_t got = __shfl_xor_sync(0xffffffffu, give, 1);
+                        pw[8 * h + k] = (c4 & 1) ? (got | (ub << 16)) : (ua | (got << 16));
                     }
-                    // keys cb + 32 q2 .. : four e4m3 per column, from column (cb + 32 q2) / 4
-                    tmem_st8(tS + (cb >> 2) + q2 * 8, w32);
-                }
+                tmem_st_16x64b_x16(tS, pw);
             }
-            float s0, s1, s2, s3;
-            f2unpack(acc2[0], s0, s1);
-            f2unpack(acc2[1], s2, s3);
-            l += (s0 + s1) + (s2 + s3);
+            {
+                float s0, s1;
+                f2unpack(acca, s0, s1);
+                la += s0 + s1;
+                f2unpack(accb, s0, s1);
+                lb += s0 + s1;
+            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.p_full[sb]);
             if (fl & 2) {
                 // hand the row statistics to the epilogue once it has finished the previous tile
+                float ta = la + __shfl_xor_sync(0xffffffffu, la, 1);
+                float tb = lb + __shfl_xor_sync(0xffffffffu, lb, 1);
+                ta += __shfl_xor_sync(0xffffffffu, ta, 2);
+                tb += __shfl_xor_sync(0xffffffffu, tb, 2);
                 if (!mbar_wait(&sm.o_empty, (tile & 1) ^ 1, ab)) break;
-                if (half == 0) sm.stat_m[j] = mx;
-                sm.stat_l[half][j] = l;
+                if (c4 == 0) {
+                    sm.stat_m[ra] = mxa;
+                    sm.stat_l[ra] = ta;
+                    sm.stat_m[rb] = mxb;
+                    sm.stat_l[rb] = tb;
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.st_full);
             }
@@ -840,7 +882,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 if (!(ok = mbar_wait(&sm.o_full, ti & 1, ab))) break;
                 if (!(ok = mbar_wait(&sm.st_full, ti & 1, ab))) break;
                 tc_fence_after();
-                const float mx = sm.stat_m[j], l = sm.stat_l[0][j] + sm.stat_l[1][j];
+                const float mx = sm.stat_m[j], l = sm.stat_l[j];
                 const float inv = l > 0.f ? P.c_v / l : 0.f;
                 __nv_bfloat16 *orow = P.out + rowi * kHeadDim;
 #pragma unroll
