@@ -200,36 +200,44 @@ __global__ void __launch_bounds__(kSThreads, 1)
         }
     } else if (warp == 1) {
         // --------------------------------------------------------------- MMA issue
-        if (lane == 0 && scoring) {
+        // The whole warp runs the loop (descriptors stay warp-uniform) and one elected lane issues:
+        // issued from a lone lane, every MMA costs tens of cycles more. Waits end alike in all lanes.
+        if (scoring) {
+            auto wait_w = [&](uint64_t *bar, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab));
+            };
             uint32_t tile_it = 0, chunk_it = 0;
             for (int w = blockIdx.x; w < nseg; w += gridDim.x, ++tile_it) {
                 const SegCoord sc = decode_seg(req, batch, g, nseg - 1 - w);
                 const int qb = tile_it & 1;
-                if (!mbar_wait(&sm.q_full[qb], (tile_it >> 1) & 1, ab)) break;
+                if (!wait_w(&sm.q_full[qb], (tile_it >> 1) & 1)) break;
                 const int nch = sc.D / 128 + 1;
                 bool ok = true;
                 for (int cc = 0; cc < nch; ++cc, ++chunk_it) {
                     const int st = chunk_it % kSStages;
                     const int sb = chunk_it & 1;
-                    if (!(ok = mbar_wait(&sm.k_full[st], (chunk_it / kSStages) & 1, ab))) break;
-                    if (!(ok = mbar_wait(&sm.s_empty[sb], ((chunk_it >> 1) & 1) ^ 1, ab))) break;
-                    tc_fence_after();
-                    const uint32_t abase = smem_addr(sm.k[st]), bbase = smem_addr(sm.q[qb]);
+                    if (!(ok = wait_w(&sm.k_full[st], (chunk_it / kSStages) & 1))) break;
+                    if (!(ok = wait_w(&sm.s_empty[sb], ((chunk_it >> 1) & 1) ^ 1))) break;
+                    if (elect_one()) {
+                        tc_fence_after();
+                        const uint32_t abase = smem_addr(sm.k[st]), bbase = smem_addr(sm.q[qb]);
 #pragma unroll
-                    for (int k = 0; k < C::kNumK; ++k) {
-                        const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                        const uint64_t ad = sw128_desc(abase + off, 16, 1024);
-                        const uint64_t bd = sw128_desc(bbase + off, 16, 1024);
-                        if (kDtype == FP_DTYPE_BF16)
-                            umma_f16_ss(tmem + sb * 128, ad, bd, C::kIdesc, k > 0);
-                        else
-                            umma_f8_ss(tmem + sb * 128, ad, bd, C::kIdesc, k > 0);
+                        for (int k = 0; k < C::kNumK; ++k) {
+                            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                            const uint64_t ad = sw128_desc(abase + off, 16, 1024);
+                            const uint64_t bd = sw128_desc(bbase + off, 16, 1024);
+                            if (kDtype == FP_DTYPE_BF16)
+                                umma_f16_ss(tmem + sb * 128, ad, bd, C::kIdesc, k > 0);
+                            else
+                                umma_f8_ss(tmem + sb * 128, ad, bd, C::kIdesc, k > 0);
+                        }
+                        umma_commit(&sm.k_empty[st]);
+                        umma_commit(&sm.s_full[sb]);
+                        if (cc == nch - 1) umma_commit(&sm.q_empty[qb]);
                     }
-                    umma_commit(&sm.k_empty[st]);
-                    umma_commit(&sm.s_full[sb]);
+                    __syncwarp();
                 }
                 if (!ok) break;
-                umma_commit(&sm.q_empty[qb]);
             }
         }
     } else {
