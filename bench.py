@@ -34,7 +34,23 @@ METRIC = "sparse prefill-attn ms/layer & dense-equiv TFLOP/s at 128K; tensor-pip
 UNIT = "ms/layer"
 DEFAULT_WORKLOAD = "qwen30b_128k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS_PER_STEP = 7   # fp_select: prep, pool, score, csr scan, csr expand; fp_attention: prep, attention
+KERNELS_PER_STEP = 10  # fp_select: prep, pool, score, csr scan, csr expand; fp_attention: prep, meta, bucket, scatter, attention
+
+# DRAM bytes (read + write) of one attention-kernel launch on this workload, from one ncu capture
+# (profiles/attn_tc_qwen30b_128k.md), valid while the kernel's sources are those the capture ran.
+ATTN_TRAFFIC = {"workload": "qwen30b_128k", "bytes": 1.365476e9 + 1.032635e9,
+                "sources_sha256": "4dd33fe1fe18a898be7e0804ccfde6a803d874d21a614a2d05a1cd847a1c0649"}
+
+
+def attn_traffic(workload: str):
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("fp_stage2.cu", "fp_internal.cuh", "sm100_ptx.cuh"):
+        with open(os.path.join(ROOT, "block_sparse_long_mean_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if workload == ATTN_TRAFFIC["workload"] and h.hexdigest() == ATTN_TRAFFIC["sources_sha256"]:
+        return ATTN_TRAFFIC["bytes"]
+    return None
 
 
 def peaks():
@@ -305,10 +321,11 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
                executed_tflops=achieved_tflops,
                dense_equiv_tflops=acc["dense_equiv_flop"] / (ms_step * 1e-3) / 1e12,
                stage1_gbs=stage1_gbs, density=acc["density"], correction_chunks=acc["corr_chunks"],
-               roofline=dict(bound="tensor", kernel="fp_attention (Stage 2)", achieved=achieved_tflops,
+               roofline=dict(bound="tensor", kernel="fp_attention (Stage 2: meta, bucket, scatter, attention kernels)",
+                             achieved=achieved_tflops,
                              peak=peak_t, unit="TFLOP/s", frac=achieved_tflops / peak_t,
                              peak_source=f"{pk_src} bf16 burst" + (" x2 for e4m3" if w.dtype == "e4m3" else ""),
-                             traffic=None),
+                             traffic=attn_traffic(args.workload), traffic_unit="bytes per launch"),
                stage1_roofline=dict(bound="hbm", achieved=stage1_gbs, peak=float(pk.get("hbm_gbs", 6800.0)),
                                     unit="GB/s", frac=stage1_gbs / float(pk.get("hbm_gbs", 6800.0))),
                e2e=dict(value=e2e_ms, unit=UNIT, h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h)),
