@@ -38,9 +38,15 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kSWarps = 6;  // warp 0: TMA, warp 1: MMA + TMEM, warps 2-5: reduction / selection
+// warp 0: TMA, warp 1: MMA + TMEM, warps 2-3 idle; warps 4-7 and 8-11: two reduction / selection sets
+// that take alternate tiles, so one tile's selection overlaps the next tile's scores
+constexpr int kSWarps = 12;
 constexpr int kSThreads = 32 * kSWarps;
-constexpr int kSStages = 3;  // pooled-key chunk stages
+constexpr int kSStages = 2;  // pooled-key chunk stages
+// registers per thread: 64K over the CTA at launch, then 48 for the TMA/MMA warpgroup and 224 for each set
+constexpr int kSRegsLaunch = (65536 / kSThreads) & ~7;
+constexpr int kSRegsProducer = 48, kSRegsReduce = 224;
+static_assert(kSRegsProducer + 2 * kSRegsReduce <= 3 * kSRegsLaunch, "register split exceeds the launch");
 constexpr int kRedThreads = 128;
 constexpr int kRefineList = 256;
 constexpr int kCand = 128;  // candidates per tile settled without the exact path
@@ -59,23 +65,27 @@ struct SCfg {
         instr_desc(kDtype == FP_DTYPE_BF16 ? 1u : 0u, kDtype == FP_DTYPE_BF16 ? 1u : 0u, false, false, 128, 128);
 };
 
-template <int kDtype>
-struct ScoreSmem {
-    alignas(1024) uint8_t q[2][SCfg<kDtype>::kTile];
-    alignas(1024) uint8_t k[kSStages][SCfg<kDtype>::kTile];
+// Scratch of one reduction set.
+struct RedScratch {
     float lE[kMaxBlocks];       // screened log-energy, upper bound, or refined value
     uint8_t state[kMaxBlocks];  // see kSt* below
     int32_t list[kRefineList];
     uint32_t words[kMaxBlocks / 32];  // selection mask of the current tile
     int32_t cand[kCand];              // blocks with a screened log-energy
-    uint64_t q_full[2], q_empty[2], k_full[kSStages], k_empty[kSStages], s_full[2], s_empty[2];
-    uint32_t tmem_base;
-    int abort;
     float red[2][4];
     float red3[3][4];
     int nlist, ncand, nsel;
-    int any;
-    int any2[2];  // per tile parity: some candidate was left open (read after the tile's last barrier)
+    int any2[2];  // per tile of the set, alternately: some candidate was left open (read after the tile's last barrier)
+};
+
+template <int kDtype>
+struct ScoreSmem {
+    alignas(1024) uint8_t q[2][SCfg<kDtype>::kTile];  // Q buffer s belongs to set s
+    alignas(1024) uint8_t k[kSStages][SCfg<kDtype>::kTile];
+    RedScratch rs[2];
+    uint64_t q_full[2], q_empty[2], k_full[kSStages], k_empty[kSStages], s_full[2][2], s_empty[2][2];
+    uint32_t tmem_base;
+    int abort;
 };
 
 // state bits
@@ -85,7 +95,17 @@ constexpr uint8_t kStMaxCand = 4;    // may hold the maximum
 constexpr uint8_t kStRefined = 8;    // lE is the fp32 recomputation
 constexpr uint8_t kStSelected = 0x80;
 
-__device__ __forceinline__ void red_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier of one reduction set (ids 1 and 2; 128 threads each).
+__device__ __forceinline__ void red_bar(int set) { asm volatile("bar.sync %0, 128;" ::"r"(1 + set) : "memory"); }
+
+template <int kRegs>
+__device__ __forceinline__ void sregs_set() {
+    static_assert(kRegs % 8 == 0 && kRegs >= 24 && kRegs <= 256, "setmaxnreg range");
+    if constexpr (kRegs > kSRegsLaunch)
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+    else if constexpr (kRegs < kSRegsLaunch)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -102,23 +122,21 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Max over the 128 reduction threads (warps 2-5); slot selects the smem buffer.
-template <typename S>
-__device__ __forceinline__ float red_max(S &sm, float v, int slot) {
+// Max over the 128 threads of reduction set `set`; slot selects the smem buffer.
+__device__ __forceinline__ float red_max(RedScratch &rs, int set, float v, int slot) {
     v = warp_max(v);
-    const int w = (threadIdx.x >> 5) - 2;
-    if ((threadIdx.x & 31) == 0) sm.red[slot][w] = v;
-    red_bar();
-    const float r = fmaxf(fmaxf(sm.red[slot][0], sm.red[slot][1]), fmaxf(sm.red[slot][2], sm.red[slot][3]));
+    const int w = (threadIdx.x >> 5) & 3;
+    if ((threadIdx.x & 31) == 0) rs.red[slot][w] = v;
+    red_bar(set);
+    const float r = fmaxf(fmaxf(rs.red[slot][0], rs.red[slot][1]), fmaxf(rs.red[slot][2], rs.red[slot][3]));
     return r;
 }
-template <typename S>
-__device__ __forceinline__ float red_sum(S &sm, float v, int slot) {
+__device__ __forceinline__ float red_sum(RedScratch &rs, int set, float v, int slot) {
     v = warp_sum(v);
-    const int w = (threadIdx.x >> 5) - 2;
-    if ((threadIdx.x & 31) == 0) sm.red[slot][w] = v;
-    red_bar();
-    return (sm.red[slot][0] + sm.red[slot][1]) + (sm.red[slot][2] + sm.red[slot][3]);
+    const int w = (threadIdx.x >> 5) & 3;
+    if ((threadIdx.x & 31) == 0) rs.red[slot][w] = v;
+    red_bar(set);
+    return (rs.red[slot][0] + rs.red[slot][1]) + (rs.red[slot][2] + rs.red[slot][3]);
 }
 
 // Element (row r, column c) of a 128x128 tile stored by TMA with 128-byte swizzling.
@@ -150,9 +168,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.q_full[i], 1);
-            mbar_init(&sm.q_empty[i], 2);  // MMA commit + reduction warps done with Q
-            mbar_init(&sm.s_full[i], 1);
-            mbar_init(&sm.s_empty[i], 4);  // one arrival per reduction warp
+            mbar_init(&sm.q_empty[i], 2);  // MMA commit + reduction set done with Q
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&sm.s_full[i][b], 1);
+                mbar_init(&sm.s_empty[i][b], 4);  // one arrival per warp of the set
+            }
         }
         for (int i = 0; i < kSStages; ++i) {
             mbar_init(&sm.k_full[i], 1);
@@ -161,7 +181,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         sm.abort = 0;
         fence_barrier_init();
     }
-    if (warp == 1) tmem_alloc(&sm.tmem_base, 256);
+    if (warp == 1) tmem_alloc(&sm.tmem_base, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -170,6 +190,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const bool scoring = mode == kModeScore;
 
     if (warp == 0) {
+        sregs_set<kSRegsProducer>();
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && scoring) {
             tma_prefetch_desc(&tm_q);
@@ -199,6 +220,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
             }
         }
     } else if (warp == 1) {
+        sregs_set<kSRegsProducer>();
         // --------------------------------------------------------------- MMA issue
         // The whole warp runs the loop (descriptors stay warp-uniform) and one elected lane issues:
         // issued from a lone lane, every MMA costs tens of cycles more. Waits end alike in all lanes.
@@ -207,17 +229,19 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab));
             };
             uint32_t tile_it = 0, chunk_it = 0;
+            uint32_t set_chunk[2] = {0, 0};  // chunks issued into each set's S buffers
             for (int w = blockIdx.x; w < nseg; w += gridDim.x, ++tile_it) {
                 const SegCoord sc = decode_seg(req, batch, g, nseg - 1 - w);
-                const int qb = tile_it & 1;
+                const int qb = tile_it & 1;  // = the set that reduces this tile
                 if (!wait_w(&sm.q_full[qb], (tile_it >> 1) & 1)) break;
                 const int nch = sc.D / 128 + 1;
                 bool ok = true;
                 for (int cc = 0; cc < nch; ++cc, ++chunk_it) {
                     const int st = chunk_it % kSStages;
-                    const int sb = chunk_it & 1;
+                    const uint32_t sc_it = set_chunk[qb]++;
+                    const int sb = sc_it & 1;
                     if (!(ok = wait_w(&sm.k_full[st], (chunk_it / kSStages) & 1))) break;
-                    if (!(ok = wait_w(&sm.s_empty[sb], ((chunk_it >> 1) & 1) ^ 1))) break;
+                    if (!(ok = wait_w(&sm.s_empty[qb][sb], ((sc_it >> 1) & 1) ^ 1))) break;
                     if (elect_one()) {
                         tc_fence_after();
                         const uint32_t abase = smem_addr(sm.k[st]), bbase = smem_addr(sm.q[qb]);
@@ -227,12 +251,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
                             const uint64_t ad = sw128_desc(abase + off, 16, 1024);
                             const uint64_t bd = sw128_desc(bbase + off, 16, 1024);
                             if (kDtype == FP_DTYPE_BF16)
-                                umma_f16_ss(tmem + sb * 128, ad, bd, C::kIdesc, k > 0);
+                                umma_f16_ss(tmem + qb * 256 + sb * 128, ad, bd, C::kIdesc, k > 0);
                             else
-                                umma_f8_ss(tmem + sb * 128, ad, bd, C::kIdesc, k > 0);
+                                umma_f8_ss(tmem + qb * 256 + sb * 128, ad, bd, C::kIdesc, k > 0);
                         }
                         umma_commit(&sm.k_empty[st]);
-                        umma_commit(&sm.s_full[sb]);
+                        umma_commit(&sm.s_full[qb][sb]);
                         if (cc == nch - 1) umma_commit(&sm.q_empty[qb]);
                     }
                     __syncwarp();
@@ -240,7 +264,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 if (!ok) break;
             }
         }
+    } else if (warp < 4) {
+        sregs_set<kSRegsProducer>();  // idle
     } else {
+        sregs_set<kSRegsReduce>();
         // --------------------------------------------------- reduction / selection
         // Thread j owns block J = 128 c + j of each chunk c. Its screened maximum logit ms_J bounds the
         // block's log-energy, ms_J - eps_J <= lE_J <= ms_J + ln(rows) + eps_J. Blocks whose upper bound
@@ -248,9 +275,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
         // others ("candidates") get a screened log-energy and are settled at the end of the tile against
         // the threshold interval, and any candidate the interval cannot settle sends the tile through the
         // exact fp32 path. Mask words start from the forced blocks (sink, window, diagonal).
-        const int rt = threadIdx.x - 64;              // 0..127 across warps 2-5
+        const int set = (warp - 4) >> 2;               // this set takes the CTA's tiles k with k % 2 == set
+        RedScratch &rs = sm.rs[set];
+        const int rt = (threadIdx.x - 128) & 127;     // 0..127 within the set
         const int j = 32 * (warp & 3) + lane;         // TMEM lane = block in chunk = tile row
-        const uint32_t tlane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        const uint32_t tlane = (static_cast<uint32_t>(32 * (warp & 3)) << 16) + set * 256;
         const float inv_sqrt_d = rsqrtf((float)kHeadDim);
         const float scale = qscale * kscale * inv_sqrt_d;  // raw MMA dot -> logit
         const float LOG2E = 1.4426950408889634f, LN2 = 0.6931471805599453f;
@@ -262,32 +291,35 @@ __global__ void __launch_bounds__(kSThreads, 1)
             const uint32_t up = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
             return up & ~((1u << lo) - 1u);
         };
-        uint32_t tile_it = 0, chunk_it = 0;
+        uint32_t tile_it = set, chunk_it = 0;  // tile_it: the CTA's tile counter; chunk_it: this set's chunks
         bool ok = true;
+        const int wstep = 2 * (int)gridDim.x;
         // the next tile's coordinates and request record are fetched a tile ahead
-        SegCoord sc_next = decode_seg(req, batch, g, nseg - 1 - (int)blockIdx.x);
+        const int w0 = (int)blockIdx.x + set * (int)gridDim.x;
+        SegCoord sc_next = decode_seg(req, batch, g, nseg - 1 - min(w0, nseg - 1));
         ReqInfo r_next = req[sc_next.b];
-        for (int w = blockIdx.x; w < nseg && ok; w += gridDim.x, ++tile_it) {
+        for (int w = w0; w < nseg && ok; w += wstep, tile_it += 2) {
             const int seg = nseg - 1 - w;
             const SegCoord sc = sc_next;
             const ReqInfo r = r_next;
-            if (w + (int)gridDim.x < nseg) {
-                sc_next = decode_seg(req, batch, g, nseg - 1 - (w + (int)gridDim.x));
+            if (w + wstep < nseg) {
+                sc_next = decode_seg(req, batch, g, nseg - 1 - (w + wstep));
                 r_next = req[sc_next.b];
             }
+            const int ap = (tile_it >> 1) & 1;  // alternates between this set's consecutive tiles
             const int D = sc.D, rows = sc.rows;
-            const int qb = tile_it & 1;
+            const int qb = set;
             const int nch = D / 128 + 1;
             const float2 *ks_base = kstat + (int64_t)r.blk_base * hkv + sc.h;
             const float lnrows = logf((float)rows);
             const int s_end = min(sink, D + 1), w_lo = max(D - window, 0);
             // mask words of this tile start as the forced set; thread k owns word k
             for (int k = rt; k < r.words; k += kRedThreads)
-                sm.words[k] = range_bits(k, 0, s_end) | range_bits(k, w_lo, D) | range_bits(k, D, D + 1);
+                rs.words[k] = range_bits(k, 0, s_end) | range_bits(k, w_lo, D) | range_bits(k, D, D + 1);
             if (rt == 0) {
-                sm.ncand = 0;
-                sm.nsel = 0;
-                sm.any2[tile_it & 1] = 0;
+                rs.ncand = 0;
+                rs.nsel = 0;
+                rs.any2[ap] = 0;
             }
             float eps_tile = 0.f;                    // largest per-block logit error bound of the tile
             float mlo = -INFINITY, mhi = -INFINITY;  // this thread's bounds of max_J lE_J
@@ -319,7 +351,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     const uint32_t b = max(max(mx & 0xffu, (mx >> 8) & 0xffu), max((mx >> 16) & 0xffu, mx >> 24));
                     amax = float(*reinterpret_cast<const __nv_fp8_e4m3 *>(&b));
                 }
-                const float qmax = red_max(sm, amax, 0) * qscale * sqrtf((float)kHeadDim);
+                const float qmax = red_max(rs, set, amax, 0) * qscale * sqrtf((float)kHeadDim);
                 // rounding statistics of this thread's block, loaded one chunk ahead
                 float2 ks_next = (128 * (nch - 1) + j <= D) ? __ldg(ks_base + (int64_t)(128 * (nch - 1) + j) * hkv)
                                                             : make_float2(0.f, 0.f);
@@ -330,7 +362,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     const bool valid = J <= D;
                     const float2 ks = ks_next;
                     if (c > 0) ks_next = __ldg(ks_base + (int64_t)(J - 128) * hkv);
-                    if (!(ok = mbar_wait(&sm.s_full[sb], (chunk_it >> 1) & 1, ab))) break;
+                    if (!(ok = mbar_wait(&sm.s_full[set][sb], (chunk_it >> 1) & 1, ab))) break;
                     tc_fence_after();
                     uint32_t v[4][32];
 #pragma unroll
@@ -340,7 +372,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     for (int q4 = 0; q4 < 4; ++q4) reg_fence32(v[q4]);
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&sm.s_empty[sb]);
+                    if (lane == 0) mbar_arrive(&sm.s_empty[set][sb]);
                     float pm[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
@@ -360,7 +392,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     const float ms = m * scale;
                     // the first chunk holds the diagonal block (usually the maximum): one block-wide max of the
                     // lower bounds there gives m_run, a proven lower bound of max_J lE_J for the whole tile
-                    if (cc == 0) m_run = red_max(sm, valid ? ms - eps : -INFINITY, 1);
+                    if (cc == 0) m_run = red_max(rs, set, valid ? ms - eps : -INFINITY, 1);
                     if (valid) {
                         eps_tile = fmaxf(eps_tile, eps);
                         const float hi = ms + lnrows + eps;
@@ -378,16 +410,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
                                     if (x < rows) ps[x & 3] += ex2((__uint_as_float(v[x >> 5][x & 31]) - m) * k2);
                             }
                             const float lE = ms + log2f((ps[0] + ps[1]) + (ps[2] + ps[3])) * LN2;
-                            sm.lE[J] = lE;
-                            sm.state[J] = 0;
+                            rs.lE[J] = lE;
+                            rs.state[J] = 0;
                             mlo = fmaxf(mlo, lE - eps);
                             mhi = fmaxf(mhi, lE + eps);
-                            const int slot = atomicAdd(&sm.ncand, 1);
-                            if (slot < kCand) sm.cand[slot] = J;
+                            const int slot = atomicAdd(&rs.ncand, 1);
+                            if (slot < kCand) rs.cand[slot] = J;
                         } else {
                             // certainly pruned and certainly not the maximum: hi < ln(alpha) + m_run
-                            sm.lE[J] = hi;
-                            sm.state[J] = kStBound;
+                            rs.lE[J] = hi;
+                            rs.state[J] = kStBound;
                             mhi = fmaxf(mhi, hi);
                         }
                     }
@@ -405,75 +437,75 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 3; ++q) e3[q] = fmaxf(e3[q], __shfl_xor_sync(0xffffffffu, e3[q], o));
                 if (lane == 0)
-                    for (int q = 0; q < 3; ++q) sm.red3[q][warp - 2] = e3[q];
-                red_bar();
+                    for (int q = 0; q < 3; ++q) rs.red3[q][warp & 3] = e3[q];
+                red_bar(set);
 #pragma unroll
                 for (int q = 0; q < 3; ++q)
-                    e3[q] = fmaxf(fmaxf(sm.red3[q][0], sm.red3[q][1]), fmaxf(sm.red3[q][2], sm.red3[q][3]));
+                    e3[q] = fmaxf(fmaxf(rs.red3[q][0], rs.red3[q][1]), fmaxf(rs.red3[q][2], rs.red3[q][3]));
                 eps_tile = e3[0];
                 mlo = e3[1];
                 mhi = e3[2];
                 thr_lo = log_alpha + mlo;
                 thr_hi = log_alpha + mhi;
                 // settle the candidates against the threshold interval
-                const int nc = sm.ncand;
+                const int nc = rs.ncand;
                 if (nc > kCand) {
-                    if (rt == 0) sm.any2[tile_it & 1] = 1;
+                    if (rt == 0) rs.any2[ap] = 1;
                 } else {
                     for (int i = rt; i < nc; i += kRedThreads) {
-                        const int J = sm.cand[i];
+                        const int J = rs.cand[i];
                         const bool forced = J < sink || (J >= D - window && J < D) || J == D;
                         if (forced) continue;
-                        const float lE = sm.lE[J];
+                        const float lE = rs.lE[J];
                         if (lE - eps_tile >= thr_hi) {
-                            atomicOr(&sm.words[J >> 5], 1u << (J & 31));
-                            atomicAdd(&sm.nsel, 1);
+                            atomicOr(&rs.words[J >> 5], 1u << (J & 31));
+                            atomicAdd(&rs.nsel, 1);
                         } else if (lE + eps_tile >= thr_lo) {
-                            sm.any2[tile_it & 1] = 1;
+                            rs.any2[ap] = 1;
                         }
                     }
                 }
-                red_bar();
+                red_bar(set);
             }
-            if (scoring && sm.any2[tile_it & 1]) {
+            if (scoring && rs.any2[ap]) {
                 // fp32 recomputation of every unsettled block and every candidate for the maximum
                 for (int J = rt; J <= D; J += kRedThreads) {
                     const bool forced = J < sink || (J >= D - window && J < D) || J == D;
-                    const bool bound = sm.state[J] & kStBound;
-                    const float lo = bound ? -INFINITY : sm.lE[J] - eps_tile;
-                    const float hi = bound ? sm.lE[J] : sm.lE[J] + eps_tile;
+                    const bool bound = rs.state[J] & kStBound;
+                    const float lo = bound ? -INFINITY : rs.lE[J] - eps_tile;
+                    const float hi = bound ? rs.lE[J] : rs.lE[J] + eps_tile;
                     uint8_t st = 0;
                     if (forced || lo >= thr_hi) st |= kStSelected;
                     else if (!(hi < thr_lo)) st |= kStUncertain;
                     if (hi >= mlo) st |= kStMaxCand;
-                    sm.state[J] = st;
+                    rs.state[J] = st;
                 }
                 float qr[kHeadDim];
 #pragma unroll
                 for (int c = 0; c < kHeadDim; ++c) qr[c] = j < rows ? q_elem<kDtype>(sm.q[qb], j, c) * qscale : 0.f;
                 for (;;) {
-                    if (rt == 0) sm.nlist = 0;
-                    red_bar();
+                    if (rt == 0) rs.nlist = 0;
+                    red_bar(set);
                     // collect up to kRefineList pending candidates, in order
                     for (int J0 = 0; J0 <= D; J0 += kRedThreads) {
                         const int J = J0 + rt;
-                        const bool need = J <= D && (sm.state[J] & (kStUncertain | kStMaxCand)) &&
-                                          !(sm.state[J] & kStRefined);
+                        const bool need = J <= D && (rs.state[J] & (kStUncertain | kStMaxCand)) &&
+                                          !(rs.state[J] & kStRefined);
                         const unsigned bal = __ballot_sync(0xffffffffu, need);
                         int base = 0;
-                        if (lane == 0 && bal) base = atomicAdd(&sm.nlist, __popc(bal));
+                        if (lane == 0 && bal) base = atomicAdd(&rs.nlist, __popc(bal));
                         base = __shfl_sync(0xffffffffu, base, 0);
                         if (need) {
                             const int slot = base + __popc(bal & ((1u << lane) - 1u));
-                            if (slot < kRefineList) sm.list[slot] = J;
+                            if (slot < kRefineList) rs.list[slot] = J;
                         }
-                        red_bar();
-                        if (sm.nlist >= kRefineList) break;
+                        red_bar(set);
+                        if (rs.nlist >= kRefineList) break;
                     }
-                    const int n = min(sm.nlist, kRefineList);
+                    const int n = min(rs.nlist, kRefineList);
                     if (n == 0) break;
                     for (int i = 0; i < n; ++i) {
-                        const int J = sm.list[i];
+                        const int J = rs.list[i];
                         const float *kb = kbar + ((int64_t)(r.blk_base + J) * hkv + sc.h) * kHeadDim;
                         float dot = 0.f;
 #pragma unroll
@@ -485,51 +517,51 @@ __global__ void __launch_bounds__(kSThreads, 1)
                             dot = fmaf(qr[c + 3], k4.w, dot);
                         }
                         const float s = j < rows ? dot * inv_sqrt_d : -INFINITY;
-                        const float mxs = red_max(sm, s, 0);
+                        const float mxs = red_max(rs, set, s, 0);
                         const float e = j < rows ? expf(s - mxs) : 0.f;
-                        const float sum = red_sum(sm, e, 1);
+                        const float sum = red_sum(rs, set, e, 1);
                         if (rt == 0) {
-                            sm.lE[J] = mxs + logf(sum);
-                            sm.state[J] |= kStRefined;
+                            rs.lE[J] = mxs + logf(sum);
+                            rs.state[J] |= kStRefined;
                         }
-                        red_bar();
+                        red_bar(set);
                     }
-                    red_bar();
+                    red_bar(set);
                 }
                 // every candidate for the maximum is now exact
                 float mex = -INFINITY;
                 for (int J = rt; J <= D; J += kRedThreads)
-                    if (sm.state[J] & kStMaxCand) mex = fmaxf(mex, sm.lE[J]);
-                mex = red_max(sm, mex, 0);
+                    if (rs.state[J] & kStMaxCand) mex = fmaxf(mex, rs.lE[J]);
+                mex = red_max(rs, set, mex, 0);
                 const float thr = log_alpha + mex;
                 for (int J = rt; J <= D; J += kRedThreads) {
-                    const uint8_t st = sm.state[J];
-                    if ((st & kStUncertain) && sm.lE[J] >= thr) sm.state[J] = st | kStSelected;
+                    const uint8_t st = rs.state[J];
+                    if ((st & kStUncertain) && rs.lE[J] >= thr) rs.state[J] = st | kStSelected;
                 }
-                red_bar();
+                red_bar(set);
                 // rebuild the mask words from the final states
                 int cnt = 0;
                 for (int J0 = 32 * (warp & 3); J0 < 32 * r.words; J0 += kRedThreads) {
                     const int J = J0 + lane;
-                    const bool sel = J <= D && (sm.state[J] & kStSelected);
+                    const bool sel = J <= D && (rs.state[J] & kStSelected);
                     const unsigned bits = __ballot_sync(0xffffffffu, sel);
                     if (lane == 0) mask[wbase + (J0 >> 5)] = bits;
                     cnt += __popc(bits);
                 }
-                cnt = (int)red_sum(sm, lane == 0 ? (float)cnt : 0.f, 0);
+                cnt = (int)red_sum(rs, set, lane == 0 ? (float)cnt : 0.f, 0);
                 if (rt == 0) seg_count[seg] = cnt;
-                red_bar();
+                red_bar(set);
             } else {
                 // settled by bounds: forced blocks plus the selected candidates
-                if (!scoring) red_bar();  // the forced words are complete
+                if (!scoring) red_bar(set);  // the forced words are complete
                 for (int k = rt; k < r.words; k += kRedThreads) {
-                    uint32_t wv = sm.words[k];
+                    uint32_t wv = rs.words[k];
                     if (mode == kModeAll) wv = range_bits(k, 0, D + 1);
                     mask[wbase + k] = wv;
                 }
                 if (rt == 0) {
                     const int forced_cnt = s_end + max(0, D - max(w_lo, s_end)) + (D >= sink ? 1 : 0);
-                    seg_count[seg] = mode == kModeAll ? D + 1 : forced_cnt + (scoring ? sm.nsel : 0);
+                    seg_count[seg] = mode == kModeAll ? D + 1 : forced_cnt + (scoring ? rs.nsel : 0);
                 }
             }
             if (scoring && rt == 0) mbar_arrive(&sm.q_empty[qb]);
@@ -541,7 +573,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     if (sm.abort && threadIdx.x == 0) set_status(status, FP_ERR_DEVICE_TIMEOUT, blockIdx.x);
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
