@@ -129,6 +129,20 @@ struct SegCoord {
     int b, h, t, D, rows;  // rows: valid packed rows of the tile (<= 128)
 };
 
+// Coordinates of segment `seg` of request b, whose record is r.
+__device__ __forceinline__ SegCoord coord_in_req(const ReqInfo &r, int b, int g, int64_t seg) {
+    SegCoord c;
+    c.b = b;
+    int rem = (int)(seg - r.seg_base);
+    c.h = rem / r.ntiles;
+    c.t = rem - c.h * r.ntiles;
+    int r0 = c.t * kTileRows;
+    int total_rows = g * r.len;
+    c.rows = min(kTileRows, total_rows - r0);
+    c.D = (r0 / g) / kBlock;
+    return c;
+}
+
 __device__ __forceinline__ SegCoord decode_seg(const ReqInfo *req, int batch, int g, int64_t seg) {
     SegCoord c;
     c.b = find_req_by_seg(req, batch, seg);

@@ -296,15 +296,17 @@ __global__ void __launch_bounds__(kSThreads, 1)
         const int wstep = 2 * (int)gridDim.x;
         // the next tile's coordinates and request record are fetched a tile ahead
         const int w0 = (int)blockIdx.x + set * (int)gridDim.x;
-        SegCoord sc_next = decode_seg(req, batch, g, nseg - 1 - min(w0, nseg - 1));
-        ReqInfo r_next = req[sc_next.b];
+        int b_next = find_req_by_seg(req, batch, nseg - 1 - min(w0, nseg - 1));
+        ReqInfo r_next = req[b_next];
         for (int w = w0; w < nseg && ok; w += wstep, tile_it += 2) {
             const int seg = nseg - 1 - w;
-            const SegCoord sc = sc_next;
+            // this tile's coordinates from the request record loaded a tile ago (no load to wait for here);
+            // the next tile's record is loaded now and used a tile later
             const ReqInfo r = r_next;
+            const SegCoord sc = coord_in_req(r, b_next, g, seg);
             if (w + wstep < nseg) {
-                sc_next = decode_seg(req, batch, g, nseg - 1 - (w + wstep));
-                r_next = req[sc_next.b];
+                b_next = find_req_by_seg(req, batch, nseg - 1 - (w + wstep));
+                r_next = req[b_next];
             }
             const int ap = (tile_it >> 1) & 1;  // alternates between this set's consecutive tiles
             const int D = sc.D, rows = sc.rows;
