@@ -29,7 +29,7 @@ STATUS = {
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTS = ["fp_workspace_bytes", "fp_num_segments", "fp_num_blocks", "fp_csr_capacity", "fp_select",
-           "fp_attention", "fp_device_status", "fp_status_string", "fp_select_noalloc"]
+           "fp_attention", "fp_device_status", "fp_status_string", "fp_select_noalloc", "fp_csr_expand64"]
 
 
 class FpError(RuntimeError):
@@ -63,6 +63,8 @@ def _load():
     L.fp_select_noalloc.argtypes = [P, vp, vp, vp, f32, i32, i32, vp, vp, i64, vp, vp, vp, vp, vp, vp]
     L.fp_attention.restype = ctypes.c_int
     L.fp_attention.argtypes = [P, vp, vp, vp, vp, vp, i64, vp, vp, i32, vp, vp, vp, sz, vp]
+    L.fp_csr_expand64.restype = ctypes.c_int
+    L.fp_csr_expand64.argtypes = [P, vp, vp, vp, vp, i64, vp, sz, vp]
     L.fp_device_status.restype = ctypes.c_int
     L.fp_device_status.argtypes = [vp, vp]
     L.fp_status_string.restype = ctypes.c_char_p
@@ -177,6 +179,17 @@ def fp_select_noalloc(p: Problem, q, k_pages, v_pages, alpha: float, sink_blocks
                                  _p(kbar_op), _p(vbar_op), _p(device_status), _stream(stream))
     if check:
         _check(code, "fp_select_noalloc")
+    return code
+
+
+def fp_csr_expand64(p: Problem, csr_cu, csr_idx, tile_cu, tile_idx, workspace, stream=None,
+                    check: bool = True) -> int:
+    """fp_select's CSR over 128-token blocks -> the same CSR over 64-token KV tiles."""
+    code = lib.fp_csr_expand64(p.ref, _p(csr_cu), _p(csr_idx), _p(tile_cu), _p(tile_idx),
+                               int(tile_idx.numel()) if tile_idx is not None else 0, _p(workspace),
+                               int(workspace.numel() * workspace.element_size()), _stream(stream))
+    if check:
+        _check(code, "fp_csr_expand64")
     return code
 
 

@@ -200,6 +200,20 @@ fp_status fp_select(const fp_problem *p, const void *q, const void *k_pages, con
     return launched(e);
 }
 
+fp_status fp_csr_expand64(const fp_problem *p, const int32_t *csr_cu, const int32_t *csr_idx, int32_t *tile_cu,
+                          int32_t *tile_idx, int64_t tile_idx_capacity, void *workspace, size_t workspace_bytes,
+                          fp_stream_t stream) {
+    Ctx c;
+    fp_status st = make_ctx(p, workspace, workspace_bytes, stream, &c);
+    if (st != FP_OK) return st;
+    if (tile_idx_capacity < 0 || !tile_cu) return FP_ERR_INVALID_ARG;
+    if (c.s.nseg > 0 && (!csr_cu || !csr_idx || (tile_idx_capacity > 0 && !tile_idx))) return FP_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(c.status(), 0, 64 * 4, c.stream);
+    if (e == cudaSuccess) e = launch_prep(c);
+    if (e == cudaSuccess) e = launch_expand64(c, csr_cu, csr_idx, tile_cu, tile_idx, tile_idx_capacity);
+    return launched(e);
+}
+
 fp_status fp_attention(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages,
                        const int32_t *csr_cu, const int32_t *csr_idx, int64_t csr_idx_capacity,
                        const void *kbar_op, const void *vbar_op, int32_t flags, void *out, float *lse,

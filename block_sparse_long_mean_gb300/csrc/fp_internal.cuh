@@ -190,6 +190,8 @@ cudaError_t launch_pool(const Ctx &c, const void *k_pages, const void *v_pages, 
 cudaError_t launch_score(const Ctx &c, const void *q, const float *kbar, const void *kbar_op, float alpha, int sink,
                          int window);
 cudaError_t launch_csr(const Ctx &c, int32_t *csr_cu, int32_t *csr_idx, int64_t capacity);
+cudaError_t launch_expand64(const Ctx &c, const int32_t *csr_cu, const int32_t *csr_idx, int32_t *tile_cu,
+                            int32_t *tile_idx, int64_t capacity);
 cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, const void *v_pages,
                              const int32_t *csr_cu, const int32_t *csr_idx, int64_t capacity, const void *kbar_op,
                              const void *vbar_op, int flags, void *out, float *lse);

@@ -298,6 +298,81 @@ cudaError_t launch_pool(const Ctx &c, const void *k_pages, const void *v_pages, 
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------- 64-token tile expansion
+
+// Tiles block J of a request of length len covers: 2J, and 2J + 1 when (2J + 1) * 64 < len.
+__device__ __forceinline__ int tiles_of_block(int J, int len) { return 1 + ((2 * J + 1) * 64 < len ? 1 : 0); }
+
+// One warp per segment: the number of 64-token tiles its selected blocks cover.
+__global__ void __launch_bounds__(256) tile_count_kernel(const ReqInfo *__restrict__ req, int batch, int g,
+                                                         int32_t nseg, const int32_t *__restrict__ cu,
+                                                         const int32_t *__restrict__ idx, int32_t *__restrict__ count,
+                                                         int32_t *__restrict__ status) {
+    if (status_bad(status)) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t seg = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (seg >= nseg) return;
+    const int b = find_req_by_seg(req, batch, seg);
+    const ReqInfo r = req[b];
+    int n = 0;
+    for (int64_t i = cu[seg] + lane; i < cu[seg + 1]; i += 32) {
+        const int J = idx[i];
+        if (J < 0 || J >= r.nblocks) set_status(status, FP_ERR_DEVICE_CSR, (int32_t)seg);
+        else n += tiles_of_block(J, r.len);
+    }
+    for (int o = 16; o; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+    if (lane == 0) count[seg] = n;
+}
+
+// One warp per segment: writes the tiles in order (a warp-wide exclusive scan of the per-entry counts).
+__global__ void __launch_bounds__(256) tile_expand_kernel(const ReqInfo *__restrict__ req, int batch, int32_t nseg,
+                                                          const int32_t *__restrict__ cu,
+                                                          const int32_t *__restrict__ idx,
+                                                          const int32_t *__restrict__ tile_cu, int64_t capacity,
+                                                          int32_t *__restrict__ tile_idx, int32_t *__restrict__ status) {
+    if (status_bad(status)) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t seg = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (seg >= nseg) return;
+    const ReqInfo r = req[find_req_by_seg(req, batch, seg)];
+    int64_t out = tile_cu[seg];
+    for (int64_t i0 = cu[seg]; i0 < cu[seg + 1]; i0 += 32) {
+        const int64_t i = i0 + lane;
+        int J = -1, n = 0;
+        if (i < cu[seg + 1]) {
+            J = idx[i];
+            if (J >= 0 && J < r.nblocks) n = tiles_of_block(J, r.len);
+        }
+        int incl = n;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const int64_t at = out + incl - n;
+        for (int k = 0; k < n; ++k)
+            if (at + k < capacity) tile_idx[at + k] = 2 * J + k;
+        out += __shfl_sync(0xffffffffu, incl, 31);
+    }
+}
+
+cudaError_t launch_expand64(const Ctx &c, const int32_t *csr_cu, const int32_t *csr_idx, int32_t *tile_cu,
+                            int32_t *tile_idx, int64_t capacity) {
+    const int64_t nseg = c.s.nseg;
+    const unsigned blocks = (unsigned)((nseg + 7) / 8);
+    if (nseg > 0) {
+        tile_count_kernel<<<blocks, 256, 0, c.stream>>>(c.req(), c.p.batch, c.s.g, (int32_t)nseg, csr_cu, csr_idx,
+                                                        c.seg_count(), c.status());
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    csr_scan_kernel<<<1, 1024, 0, c.stream>>>(c.seg_count(), (int32_t)nseg, capacity, tile_cu, c.status());
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || nseg == 0) return e;
+    tile_expand_kernel<<<blocks, 256, 0, c.stream>>>(c.req(), c.p.batch, (int32_t)nseg, csr_cu, csr_idx, tile_cu,
+                                                     capacity, tile_idx, c.status());
+    return cudaGetLastError();
+}
+
 cudaError_t launch_csr(const Ctx &c, int32_t *csr_cu, int32_t *csr_idx, int64_t capacity) {
     csr_scan_kernel<<<1, 1024, 0, c.stream>>>(c.seg_count(), (int32_t)c.s.nseg, capacity, csr_cu, c.status());
     cudaError_t e = cudaGetLastError();

@@ -185,6 +185,22 @@ fp_status fp_select_noalloc(const fp_problem *p, const void *q, const void *k_pa
                             int32_t *csr_idx, int64_t csr_idx_capacity, float *kbar, float *vbar, void *kbar_op,
                             void *vbar_op, int32_t *device_status, fp_stream_t stream);
 
+/* Expands a CSR of 128-token blocks (fp_select's format) into the same CSR over
+ * 64-token physical KV tiles, the unit the serving integration's page table
+ * and attention backend index (Sec.3.4 "Serving Integration", Alg.1 step 5):
+ * block J of a request becomes tiles 2J and 2J + 1, the second only when the
+ * request holds a token at position (2J + 1) * 64, i.e. when
+ * (2J + 1) * 64 < L_b. Segments keep their order and each stays ascending.
+ *   csr_cu, csr_idx    a CSR from fp_select (block ids must lie in [0, ceil(L_b / 128));
+ *                      an id outside is skipped and reported as FP_ERR_DEVICE_CSR)
+ *   tile_cu            out [num_segments + 1]
+ *   tile_idx           out [tile_idx_capacity]; 2 * csr_cu[num_segments] always suffices;
+ *                      a larger result is cut off and reported as FP_ERR_DEVICE_OVERFLOW
+ *   workspace          as for fp_select (its status word and request table are used) */
+fp_status fp_csr_expand64(const fp_problem *p, const int32_t *csr_cu, const int32_t *csr_idx, int32_t *tile_cu,
+                          int32_t *tile_idx, int64_t tile_idx_capacity, void *workspace, size_t workspace_bytes,
+                          fp_stream_t stream);
+
 /* Waits for `stream`, then returns the device-detected error recorded in
  * `workspace` by the most recent fp_select or fp_attention on it (each call
  * clears the status word when it starts), FP_OK if none, or FP_ERR_CUDA if

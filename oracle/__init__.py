@@ -270,6 +270,27 @@ def selection_from_csr(seg: Segments, cu: np.ndarray, idx: np.ndarray) -> np.nda
     return full
 
 
+def tiles64_from_csr(p: Problem, seg: Segments, cu: np.ndarray, idx: np.ndarray):
+    """The CSR over 64-token physical KV tiles that covers the same tokens as a block CSR (FlashPrefill V2
+    Sec.3.4 "Serving Integration", Alg.1 step 5): per segment, the ascending ids u of the 64-token tiles
+    [64u, 64u + 64) that hold a token of a selected block J, i.e. of [128J, min(128J + 128, L_b))."""
+    L = p.lengths()
+    counts = np.zeros(len(seg), dtype=np.int64)
+    parts = []
+    for s in range(len(seg)):
+        Lb = int(L[seg.b[s]])
+        tiles = []
+        for J in idx[cu[s]:cu[s + 1]]:
+            lo, hi = p.block * int(J), min(p.block * (int(J) + 1), Lb)
+            tiles.extend(range(lo // 64, (hi - 1) // 64 + 1))
+        t = np.array(sorted(set(tiles)), dtype=np.int32)
+        counts[s] = len(t)
+        parts.append(t)
+    tcu = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    tidx = np.concatenate(parts).astype(np.int32) if parts else np.zeros(0, np.int32)
+    return tcu, tidx
+
+
 def attend(p: Problem, sel_full: np.ndarray, correction: bool = True, dense: bool = False,
            seg: Optional[Segments] = None, pooled: Optional[Pooled] = None, seg_ids: Optional[Sequence[int]] = None,
            nthreads: Optional[int] = None):

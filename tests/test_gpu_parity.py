@@ -171,3 +171,58 @@ def test_varlen16_sampled_parity(name):
     w = synth.make_workload(name, device="cuda")
     rep = compare(run_gpu(w), n_random=32)
     (check_fp8 if w.dtype == "e4m3" else check_bf16)(rep)
+
+
+# ------------------------------------------------- serving formats and the paper's forced set
+
+@pytest.mark.parametrize("page", [64, 16])
+def test_tiles64_expansion_matches_oracle(page):
+    import oracle
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[1000, 333, 0, 2112, 129, 64], hq=8, hkv=2,
+                            mu_scale=0.5, alpha=0.05, paging="random", page_size=page)
+    r = run_gpu(w)
+    nseg = B.fp_num_segments(r.p)
+    nnz = int(r.bufs.csr_cu[-1])
+    tile_cu = torch.empty(nseg + 1, dtype=torch.int32, device="cuda")
+    tile_idx = torch.full((2 * nnz + 16,), -7, dtype=torch.int32, device="cuda")
+    B.fp_csr_expand64(r.p, r.bufs.csr_cu, r.bufs.csr_idx, tile_cu, tile_idx, r.bufs.workspace)
+    assert B.fp_device_status(r.bufs.workspace) == B.FP_OK
+    op = oracle.Problem.from_workload(w)
+    seg = oracle.segments(op)
+    cu = r.bufs.csr_cu.cpu().numpy()
+    want_cu, want_idx = oracle.tiles64_from_csr(op, seg, cu, r.bufs.csr_idx[:nnz].cpu().numpy())
+    got_cu = tile_cu.cpu().numpy()
+    assert np.array_equal(got_cu, want_cu)
+    assert np.array_equal(tile_idx[:got_cu[-1]].cpu().numpy(), want_idx)
+    assert bool((tile_idx[got_cu[-1]:] == -7).all())   # nothing written past the result
+
+
+def test_tiles64_expansion_reports_bad_ids_and_overflow():
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[1024, 300], hq=4, hkv=1)
+    r = run_gpu(w)
+    nseg = B.fp_num_segments(r.p)
+    nnz = int(r.bufs.csr_cu[-1])
+    tile_cu = torch.empty(nseg + 1, dtype=torch.int32, device="cuda")
+    full = torch.empty(2 * nnz, dtype=torch.int32, device="cuda")
+    B.fp_csr_expand64(r.p, r.bufs.csr_cu, r.bufs.csr_idx, tile_cu, full, r.bufs.workspace)
+    assert B.fp_device_status(r.bufs.workspace) == B.FP_OK
+    # too small a capacity: reported, and the result is cut off at the capacity
+    small = torch.full((3,), -7, dtype=torch.int32, device="cuda")
+    B.fp_csr_expand64(r.p, r.bufs.csr_cu, r.bufs.csr_idx, tile_cu, small, r.bufs.workspace)
+    assert B.fp_device_status(r.bufs.workspace) == B.STATUS_CODE["FP_ERR_DEVICE_OVERFLOW"]
+    assert torch.equal(small, full[:3])
+    # a block id past the request: reported and skipped
+    bad = r.bufs.csr_idx.clone()
+    bad[nnz - 1] = 10 ** 6
+    B.fp_csr_expand64(r.p, r.bufs.csr_cu, bad, tile_cu, full, r.bufs.workspace)
+    assert B.fp_device_status(r.bufs.workspace) == B.STATUS_CODE["FP_ERR_DEVICE_CSR"]
+
+
+@pytest.mark.parametrize("name", ["tiny_2k", "llama8b_32k"])
+def test_paper_default_forced_set_parity(name):
+    # 256 sink tokens and a 512-token local window = 2 sink blocks and 4 window blocks of 128 tokens
+    kw = dict(lengths=[2048, 900], hq=8, hkv=2, mu_scale=0.6) if name == "tiny_2k" else {}
+    w = synth.make_workload(name, device="cuda", **kw)
+    w.sink_blocks, w.window_blocks = 2, 4
+    rep = compare(run_gpu(w), n_random=32)
+    check_bf16(rep)

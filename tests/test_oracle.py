@@ -442,3 +442,35 @@ def test_correction_reduces_error_on_the_generator():
     corr = oracle.run(p, alpha=0.1, sink=1, window=1, correction=True)["O"]
     nocorr = oracle.run(p, alpha=0.1, sink=1, window=1, correction=False)["O"]
     assert np.linalg.norm(corr - dense) < np.linalg.norm(nocorr - dense)
+
+
+# ------------------------------------------- 64-token tile CSR (serving format)
+
+def test_tiles64_hand_example_and_token_enumeration():
+    """Block J of a request covers the 64-token tiles holding any of its tokens (Sec.3.4, Alg.1 step 5)."""
+    w = small_workload(lengths=(300, 64, 129), hq=4, hkv=1)
+    op = oracle.Problem.from_workload(w)
+    seg = oracle.segments(op)
+    # request 0: L = 300 -> blocks 0..2 cover tiles {0, 1}, {2, 3}, {4} (tokens 256..299 lie in tile 4 only)
+    s0 = int(np.nonzero(seg.b == 0)[0][-1])   # the last tile of request 0 reaches block 2
+    assert seg.D[s0] == 2
+    cu = np.zeros(len(seg) + 1, np.int32)
+    parts = []
+    rng = np.random.default_rng(7)
+    for s in range(len(seg)):
+        ids = np.array([0, 1, 2], np.int32) if s == s0 else np.sort(
+            rng.choice(seg.D[s] + 1, size=rng.integers(1, seg.D[s] + 2), replace=False)).astype(np.int32)
+        parts.append(ids)
+        cu[s + 1] = cu[s] + len(ids)
+    idx = np.concatenate(parts)
+    tcu, tidx = oracle.tiles64_from_csr(op, seg, cu, idx)
+    assert list(tidx[tcu[s0]:tcu[s0 + 1]]) == [0, 1, 2, 3, 4]
+    L = op.lengths()
+    for s in range(len(seg)):
+        # explicit token enumeration: every token of every selected block, mapped to its tile
+        toks = np.concatenate([np.arange(128 * J, min(128 * J + 128, L[seg.b[s]])) for J in idx[cu[s]:cu[s + 1]]])
+        want = np.unique(toks // 64)
+        assert np.array_equal(tidx[tcu[s]:tcu[s + 1]], want), s
+        # closed form of the count: two tiles per block, one for a block with at most 64 tokens
+        n = sum(2 if 128 * J + 64 < L[seg.b[s]] else 1 for J in idx[cu[s]:cu[s + 1]])
+        assert tcu[s + 1] - tcu[s] == n
