@@ -20,6 +20,11 @@ The pool holds sum_b ceil(L_b / 64) pages plus 5% unused pages, randomly
 permuted (or the identity for a contiguous layout) and dealt to the requests
 in order; unused slots hold small finite filler values.
 
+Chunked prefill after a cached prefix: with kv_lengths[b] = L_b^kv > L_b^q the
+generator draws the whole sequence of L_b^kv positions, puts all L_b^kv keys and
+values in the paged pool and keeps the queries of the last L_b^q positions (the
+new chunk), so a chunked run sees exactly the tensors of the unchunked one.
+
 FP8 workloads quantise the bf16 tensors to OCP E4M3 with per-tensor scales
 c = absmax / 448 (the scales are part of the input, as in the paper's FP8
 execution, Sec.3.3 Eq.15).
@@ -68,7 +73,7 @@ class Workload:
     v_pages: torch.Tensor      # [num_pages, 64, hkv, d]
     page_table: torch.Tensor   # [batch, max_pages] int32, -1 past a request's pages
     cu_seqlens: torch.Tensor   # [batch+1] int32 (same device as q)
-    lengths: List[int]
+    lengths: List[int]         # new-token (query) lengths L_b^q
     hq: int
     hkv: int
     dtype: str                 # "bf16" or "e4m3"
@@ -78,10 +83,16 @@ class Workload:
     alpha: float
     sink_blocks: int
     window_blocks: int
+    kv_lengths: Optional[List[int]] = None    # L_b^kv (cached prefix + new tokens); None: = lengths
+    seqlens_kv: Optional[torch.Tensor] = None  # [batch] int32 copy of kv_lengths on q's device
 
     @property
     def batch(self) -> int:
         return len(self.lengths)
+
+    @property
+    def host_seqlens_kv(self) -> Optional[np.ndarray]:
+        return None if self.kv_lengths is None else np.asarray(self.kv_lengths, dtype=np.int32)
 
     @property
     def num_pages(self) -> int:
@@ -148,10 +159,13 @@ def make_workload(name: str, device="cpu", seed: int = BASE_SEED, lengths: Optio
                   hq: Optional[int] = None, hkv: Optional[int] = None, dtype: Optional[str] = None,
                   paging: Optional[str] = None, stripes: Optional[bool] = None, mu_scale: float = 1.0,
                   alpha: Optional[float] = None, sink_blocks: int = 1, window_blocks: int = 1,
-                  extra_page_frac: float = 0.05, page_size: int = PAGE) -> Workload:
+                  extra_page_frac: float = 0.05, page_size: int = PAGE,
+                  kv_lengths: Optional[List[int]] = None) -> Workload:
     """Builds a named workload; keyword arguments override its shape (for small test cases).
 
-    mu_scale < 1 gives the "stress" variant with much denser block selection.
+    mu_scale < 1 gives the "stress" variant with much denser block selection. kv_lengths (>= lengths,
+    element-wise) makes each request the last lengths[b] tokens of a kv_lengths[b]-token sequence whose
+    earlier tokens are a cached prefix.
     """
     spec = dict(WORKLOADS[name])
     cfg_id = WORKLOAD_INDEX[name]
@@ -160,6 +174,11 @@ def make_workload(name: str, device="cpu", seed: int = BASE_SEED, lengths: Optio
         if lengths == "loguniform16":
             lengths = loguniform_lengths(16, 4096, 131072, _mix(seed, cfg_id, 999))
     lengths = [int(x) for x in lengths]
+    if kv_lengths is not None:
+        kv_lengths = [int(x) for x in kv_lengths]
+        if len(kv_lengths) != len(lengths) or any(kv < L for kv, L in zip(kv_lengths, lengths)):
+            raise ValueError("kv_lengths must give one length >= the query length per request")
+    kvl = kv_lengths if kv_lengths is not None else lengths
     hq = hq or spec["hq"]
     hkv = hkv or spec["hkv"]
     dtype = dtype or spec["dtype"]
@@ -174,7 +193,7 @@ def make_workload(name: str, device="cpu", seed: int = BASE_SEED, lengths: Optio
 
     # page table: pages dealt to requests in order from a (permuted) pool
     PAGE = page_size
-    pages_per = [(L + PAGE - 1) // PAGE for L in lengths]
+    pages_per = [(L + PAGE - 1) // PAGE for L in kvl]
     used = sum(pages_per)
     num_pages = max(1, used + int(math.ceil(extra_page_frac * used)))
     pgen = torch.Generator(device="cpu")
@@ -197,17 +216,17 @@ def make_workload(name: str, device="cpu", seed: int = BASE_SEED, lengths: Optio
     q = torch.empty(T, hq, d, device=device, dtype=torch.float32)
     pt_dev = pt.to(device)
     start = 0
-    for b, L in enumerate(lengths):
-        if L:
-            j = torch.arange(L, device=device)
+    for b, (L, Lkv) in enumerate(zip(lengths, kvl)):
+        if Lkv:
+            j = torch.arange(Lkv, device=device)
             slot = pt_dev[b, j // PAGE].long() * PAGE + (j % PAGE)
         for h in range(hkv):
             gen = torch.Generator(device=device)
             gen.manual_seed(_mix(seed, cfg_id, b, h))
-            if L == 0:
+            if Lkv == 0:
                 continue
-            qh, kh, vh = _gen_head(L, g, d, gen, device, mu_scale, stripes)
-            q[start:start + L, h * g:(h + 1) * g] = qh
+            qh, kh, vh = _gen_head(Lkv, g, d, gen, device, mu_scale, stripes)
+            q[start:start + L, h * g:(h + 1) * g] = qh[Lkv - L:]
             kpool[slot, h] = kh
             vpool[slot, h] = vh
         start += L
@@ -219,12 +238,15 @@ def make_workload(name: str, device="cpu", seed: int = BASE_SEED, lengths: Optio
     if dtype == "e4m3":
         def absmax(x):
             return float(x.float().abs().max()) if x.numel() else 1.0
-        # scales from the real tokens only (filler slots are far smaller)
+        # scales from the real tokens only (filler slots are far smaller); with a cached prefix the query
+        # scale covers the new tokens only
         c_q = max(absmax(qb), 1e-12) / 448.0
         c_k = max(absmax(kb), 1e-12) / 448.0
         c_v = max(absmax(vb), 1e-12) / 448.0
         qb, kb, vb = _e4m3(qb, c_q), _e4m3(kb, c_k), _e4m3(vb, c_v)
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32), device=device)
+    skv = None if kv_lengths is None else torch.tensor(np.asarray(kv_lengths, dtype=np.int32), device=device)
     return Workload(name=name, q=qb.contiguous(), k_pages=kb.contiguous(), v_pages=vb.contiguous(),
                     page_table=pt_dev.contiguous(), cu_seqlens=cu, lengths=lengths, hq=hq, hkv=hkv, dtype=dtype,
-                    c_q=c_q, c_k=c_k, c_v=c_v, alpha=alpha, sink_blocks=sink_blocks, window_blocks=window_blocks)
+                    c_q=c_q, c_k=c_k, c_v=c_v, alpha=alpha, sink_blocks=sink_blocks, window_blocks=window_blocks,
+                    kv_lengths=kv_lengths, seqlens_kv=skv)

@@ -34,6 +34,7 @@ class _Problem(ctypes.Structure):
         ("cu_seqlens", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
         ("pt_stride", ctypes.c_int32), ("num_pages", ctypes.c_int32),
         ("q", ctypes.c_void_p), ("k_pages", ctypes.c_void_p), ("v_pages", ctypes.c_void_p),
+        ("seqlens_kv", ctypes.c_void_p),
     ]
 
 
@@ -43,8 +44,7 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            _build_lib()
+        _build_lib()  # compiles only when the library is missing or older than its source
         L = ctypes.CDLL(LIB_PATH)
         P = ctypes.POINTER(_Problem)
         vp = ctypes.c_void_p
@@ -99,13 +99,16 @@ class Problem:
     c_v: float = 1.0
     block: int = 128
     tile_rows: int = 128
+    seqlens_kv: Optional[np.ndarray] = None  # [batch] L_b^kv >= L_b^q (cached prefix + new tokens); None: = L_b^q
 
     @classmethod
     def from_workload(cls, w, tile_rows: int = 128) -> "Problem":
+        kv = getattr(w, "host_seqlens_kv", None)
         return cls(q=_raw(w.q), k_pages=_raw(w.k_pages), v_pages=_raw(w.v_pages),
                    cu_seqlens=np.asarray(w.host_cu_seqlens, dtype=np.int32),
                    page_table=np.ascontiguousarray(w.page_table.to("cpu").numpy().astype(np.int32)),
-                   hq=w.hq, hkv=w.hkv, dtype=w.dtype, c_q=w.c_q, c_k=w.c_k, c_v=w.c_v, tile_rows=tile_rows)
+                   hq=w.hq, hkv=w.hkv, dtype=w.dtype, c_q=w.c_q, c_k=w.c_k, c_v=w.c_v, tile_rows=tile_rows,
+                   seqlens_kv=None if kv is None else np.asarray(kv, dtype=np.int32))
 
     def __post_init__(self):
         self.q = np.ascontiguousarray(self.q)
@@ -115,6 +118,8 @@ class Problem:
         self.page_table = np.ascontiguousarray(self.page_table, dtype=np.int32)
         if self.page_table.ndim == 1:
             self.page_table = self.page_table[None, :]
+        if self.seqlens_kv is not None:
+            self.seqlens_kv = np.ascontiguousarray(self.seqlens_kv, dtype=np.int32)
 
     @property
     def d(self) -> int:
@@ -133,7 +138,16 @@ class Problem:
         return self.hq // self.hkv
 
     def lengths(self):
+        """New-token (query) lengths L_b^q."""
         return np.diff(self.cu_seqlens).astype(np.int64)
+
+    def kv_lengths(self):
+        """KV lengths L_b^kv (cached prefix plus the new tokens)."""
+        return self.lengths() if self.seqlens_kv is None else self.seqlens_kv.astype(np.int64)
+
+    def q_shifts(self):
+        """Absolute position of each request's first new token, L_b^kv - L_b^q."""
+        return self.kv_lengths() - self.lengths()
 
     def c_struct(self) -> _Problem:
         s = _Problem()
@@ -148,15 +162,18 @@ class Problem:
         s.q = self.q.ctypes.data
         s.k_pages = self.k_pages.ctypes.data
         s.v_pages = self.v_pages.ctypes.data
+        s.seqlens_kv = None if self.seqlens_kv is None else self.seqlens_kv.ctypes.data
         return s
 
 
 @dataclasses.dataclass
 class Segments:
-    """Segment enumeration in (request, KV head, tile) order."""
+    """Segment enumeration in (request, KV head, tile) order; t is the tile's index within its request,
+    T its index on the grid of absolute packed rows (T = t unless the request has a cached prefix)."""
     b: np.ndarray
     h: np.ndarray
     t: np.ndarray
+    T: np.ndarray
     D: np.ndarray            # diagonal block of each tile
     full_off: np.ndarray     # offset of each segment's D+1 per-block entries
     full_total: int
@@ -167,23 +184,31 @@ class Segments:
         return len(self.b)
 
 
+def first_tiles(p: Problem) -> np.ndarray:
+    """Absolute tile of each request's first tile: packed rows are numbered by absolute position
+    (r = g pos + head mod g) and tiled from r = 0, and the new queries start at row g (L^kv - L^q)."""
+    return (p.g * p.q_shifts()) // p.tile_rows
+
+
 def segments(p: Problem) -> Segments:
-    L = p.lengths()
-    nb = (L + p.block - 1) // p.block
-    ntiles = (p.g * L + p.tile_rows - 1) // p.tile_rows
-    bs, hs, ts = [], [], []
+    Lq, Lkv = p.lengths(), p.kv_lengths()
+    nb = (Lkv + p.block - 1) // p.block
+    T0 = first_tiles(p)
+    ntiles = np.where(Lq > 0, (p.g * Lkv + p.tile_rows - 1) // p.tile_rows - T0, 0)
+    bs, hs, ts, Ts = [], [], [], []
     for b in range(p.batch):
         for h in range(p.hkv):
             bs.append(np.full(ntiles[b], b))
             hs.append(np.full(ntiles[b], h))
             ts.append(np.arange(ntiles[b]))
+            Ts.append(T0[b] + np.arange(ntiles[b]))
     cat = lambda xs: np.concatenate(xs).astype(np.int32) if xs else np.zeros(0, np.int32)
-    b, h, t = cat(bs), cat(hs), cat(ts)
-    D = ((t.astype(np.int64) * p.tile_rows) // p.g) // p.block
+    b, h, t, T = cat(bs), cat(hs), cat(ts), cat(Ts)
+    D = ((T.astype(np.int64) * p.tile_rows) // p.g) // p.block
     full_off = np.concatenate([[0], np.cumsum(D + 1)]).astype(np.int64)
     blk_base = np.concatenate([[0], np.cumsum(nb)]).astype(np.int64)
-    return Segments(b=b, h=h, t=t, D=D.astype(np.int64), full_off=full_off[:-1].copy(), full_total=int(full_off[-1]),
-                    blk_base=blk_base[:-1].copy(), total_blocks=int(blk_base[-1]))
+    return Segments(b=b, h=h, t=t, T=T, D=D.astype(np.int64), full_off=full_off[:-1].copy(),
+                    full_total=int(full_off[-1]), blk_base=blk_base[:-1].copy(), total_blocks=int(blk_base[-1]))
 
 
 @dataclasses.dataclass
@@ -273,8 +298,8 @@ def selection_from_csr(seg: Segments, cu: np.ndarray, idx: np.ndarray) -> np.nda
 def tiles64_from_csr(p: Problem, seg: Segments, cu: np.ndarray, idx: np.ndarray):
     """The CSR over 64-token physical KV tiles that covers the same tokens as a block CSR (FlashPrefill V2
     Sec.3.4 "Serving Integration", Alg.1 step 5): per segment, the ascending ids u of the 64-token tiles
-    [64u, 64u + 64) that hold a token of a selected block J, i.e. of [128J, min(128J + 128, L_b))."""
-    L = p.lengths()
+    [64u, 64u + 64) that hold a token of a selected block J, i.e. of [128J, min(128J + 128, L_b^kv))."""
+    L = p.kv_lengths()
     counts = np.zeros(len(seg), dtype=np.int64)
     parts = []
     for s in range(len(seg)):
@@ -320,16 +345,17 @@ def tile_rows_to_tokens(p: Problem, seg: Segments, seg_ids: Sequence[int], O_til
     T = int(p.cu_seqlens[-1])
     O = np.full((T, p.hq, p.d), np.nan)
     lse = np.full((T, p.hq), np.nan)
-    L = p.lengths()
+    Lkv, shift = p.kv_lengths(), p.q_shifts()
     for i, s in enumerate(seg_ids):
-        b, h, t = int(seg.b[s]), int(seg.h[s]), int(seg.t[s])
-        r0 = t * p.tile_rows
-        r1 = min(r0 + p.tile_rows, p.g * int(L[b]))
+        b, h = int(seg.b[s]), int(seg.h[s])
+        base = int(seg.T[s]) * p.tile_rows          # absolute packed row of tile row 0
+        r0 = max(base, p.g * int(shift[b]))
+        r1 = min(base + p.tile_rows, p.g * int(Lkv[b]))
         r = np.arange(r0, r1)
-        pos = p.cu_seqlens[b] + r // p.g
+        tok = p.cu_seqlens[b] + r // p.g - int(shift[b])
         head = h * p.g + r % p.g
-        O[pos, head] = O_tiles[i, :r1 - r0]
-        lse[pos, head] = lse_tiles[i, :r1 - r0]
+        O[tok, head] = O_tiles[i, r0 - base:r1 - base]
+        lse[tok, head] = lse_tiles[i, r0 - base:r1 - base]
     return O, lse
 
 

@@ -27,7 +27,11 @@
  *     diagonal block D, and D itself ([V2] Eq.20);
  *   - corrected blocks are C = {J < D} \ S, the causal blocks fully visible to
  *     the whole tile that were not selected ([V2] Sec.3.2 "Implementation");
- *   - the logit shift of a corrected block is the natural log ln|B_J|.
+ *   - the logit shift of a corrected block is the natural log ln|B_J|;
+ *   - with a cached prefix (L^kv > L^q, [V2] Sec.3.4), the new queries are the
+ *     last L^q positions, pooling and selection cover all L^kv keys, and tiles
+ *     sit on the grid of absolute packed rows (a chunk whose first row is off
+ *     that grid starts with a partial tile), so no tile straddles two blocks.
  *
  * Element formats: bf16 (bit pattern, exactly widened), and OCP FP8 E4M3
  * ("fn": no infinities, S.1111.111 is NaN, max 448) multiplied by its
@@ -54,6 +58,7 @@ typedef struct {
     int32_t num_pages;
     const void *q;                  /* [T, hq, d] elements */
     const void *k_pages, *v_pages;  /* [num_pages, page_size, hkv, d] elements */
+    const int32_t *seqlens_kv;      /* [batch] KV lengths L_b^kv >= L_b^q, or NULL for L_b^kv = L_b^q */
 } orc_problem;
 
 /* ------------------------------------------------------------------ decode */
@@ -85,18 +90,43 @@ static double elem(const orc_problem *p, const void *base, size_t i, double scal
 
 /* --------------------------------------------------------------- geometry */
 
-static int req_len(const orc_problem *p, int b) { return p->cu_seqlens[b + 1] - p->cu_seqlens[b]; }
+/* Request b brings L^q new query tokens against L^kv cached keys/values, the
+ * new tokens last ([V2] Sec.3.4 and Alg.1 inputs: lengths (L_b^q, L_b^kv)):
+ * query i sits at absolute position L^kv - L^q + i, and attends causally to
+ * the keys at positions 0 .. L^kv - L^q + i. L^kv = L^q is a plain prefill;
+ * L^kv > L^q is a chunk of a chunked prefill after a cached prefix. */
+static int q_len(const orc_problem *p, int b) { return p->cu_seqlens[b + 1] - p->cu_seqlens[b]; }
+static int kv_len(const orc_problem *p, int b) { return p->seqlens_kv ? p->seqlens_kv[b] : q_len(p, b); }
+static int q_shift(const orc_problem *p, int b) { return kv_len(p, b) - q_len(p, b); }
 static int group(const orc_problem *p) { return p->hq / p->hkv; }
-int orc_req_blocks(const orc_problem *p, int b) { return (req_len(p, b) + p->block - 1) / p->block; }
+int orc_req_blocks(const orc_problem *p, int b) { return (kv_len(p, b) + p->block - 1) / p->block; }
+
+/* Packed rows ([V2] Eq.12-13) are numbered by absolute position,
+ * r = g pos + (head mod g), and tiled 128 at a time from r = 0, so every tile
+ * lies inside one block. The tiles of request b under one KV head are those
+ * holding one of its query rows r in [g (L^kv - L^q), g L^kv); local tile t is
+ * absolute tile first_tile + t. Without a prefix this is the usual tiling from
+ * the request's first row. */
+static long first_tile(const orc_problem *p, int b) { return (long)group(p) * q_shift(p, b) / p->tile_rows; }
 int orc_req_tiles(const orc_problem *p, int b) {
-    long rows = (long)group(p) * req_len(p, b);
-    return (int)((rows + p->tile_rows - 1) / p->tile_rows);
+    if (q_len(p, b) <= 0) return 0;
+    long end = ((long)group(p) * kv_len(p, b) + p->tile_rows - 1) / p->tile_rows;
+    return (int)(end - first_tile(p, b));
 }
 
-/* Diagonal block of packed tile t: the block holding the tile's first
- * position, pos(r) = floor(r / g) ([V2] Eq.13). */
-int orc_tile_diag(const orc_problem *p, int t) {
-    long first_row = (long)t * p->tile_rows;
+/* Absolute packed rows [*r0, *r1) of local tile t of request b that are query rows. */
+static void tile_rows(const orc_problem *p, int b, int t, long *r0, long *r1) {
+    long g = group(p), lo = (first_tile(p, b) + t) * p->tile_rows, hi = lo + p->tile_rows;
+    if (lo < g * q_shift(p, b)) lo = g * q_shift(p, b);
+    if (hi > g * kv_len(p, b)) hi = g * kv_len(p, b);
+    *r0 = lo;
+    *r1 = hi;
+}
+
+/* Diagonal block of local tile t of request b: the block holding the tile's
+ * positions, pos(r) = floor(r / g) ([V2] Eq.13). */
+int orc_tile_diag(const orc_problem *p, int b, int t) {
+    long first_row = (first_tile(p, b) + t) * p->tile_rows;
     return (int)((first_row / group(p)) / p->block);
 }
 
@@ -109,13 +139,14 @@ static size_t kv_offset(const orc_problem *p, int b, int j, int h) {
     return (slot * p->hkv + h) * p->d;
 }
 
-/* Element offset of packed row r of request b under KV head h:
- * pos(r) = floor(r/g), head(r) = h*g + (r mod g) ([V2] Eq.12-13). */
+/* Element offset of absolute packed row r of request b under KV head h:
+ * pos(r) = floor(r/g), head(r) = h*g + (r mod g) ([V2] Eq.12-13); the query of
+ * position pos is token cu_seqlens[b] + pos - (L^kv - L^q) of q. */
 static size_t q_offset(const orc_problem *p, int b, long r, int h) {
     int g = group(p);
     long pos = r / g;
     int head = h * g + (int)(r % g);
-    return ((size_t)(p->cu_seqlens[b] + pos) * p->hq + head) * p->d;
+    return ((size_t)(p->cu_seqlens[b] + pos - q_shift(p, b)) * p->hq + head) * p->d;
 }
 
 /* Checks the description and every page id a request can touch. */
@@ -126,8 +157,8 @@ int orc_validate(const orc_problem *p) {
     if (p->tile_rows % group(p)) return ORC_EINVAL;
     if (p->block % (p->tile_rows / group(p))) return ORC_EINVAL;
     for (int b = 0; b < p->batch; ++b) {
-        int L = req_len(p, b);
-        if (L < 0) return ORC_EINVAL;
+        int L = kv_len(p, b);
+        if (q_len(p, b) < 0 || L < q_len(p, b)) return ORC_EINVAL;
         int npg = (L + p->page_size - 1) / p->page_size;
         if (npg > p->pt_stride) return ORC_EINVAL;
         for (int i = 0; i < npg; ++i) {
@@ -140,12 +171,12 @@ int orc_validate(const orc_problem *p) {
 
 /* ---------------------------------------------------------------- pooling */
 
-/* Block means of one (request, KV head) ([V2] Sec.3.2 Eq.5):
+/* Block means of one (request, KV head) over all L^kv keys ([V2] Sec.3.2 Eq.5):
  *   kbar_J = (1/|B_J|) sum_{i in B_J} k_i,  vbar_J = (1/|B_J|) sum_{i in B_J} v_i,
- * with |B_J| = min(B, L - J*B) for the ragged last block. FP8 inputs are
+ * with |B_J| = min(B, L^kv - J*B) for the ragged last block. FP8 inputs are
  * descaled before pooling ([V2] Alg.1 step 2). Outputs are [nb, d] and [nb]. */
 int orc_pool(const orc_problem *p, int b, int h, double *kbar, double *vbar, int32_t *cnt) {
-    int L = req_len(p, b), B = p->block, d = p->d, nb = orc_req_blocks(p, b);
+    int L = kv_len(p, b), B = p->block, d = p->d, nb = orc_req_blocks(p, b);
     for (int J = 0; J < nb; ++J) {
         int n = L - J * B < B ? L - J * B : B;
         double *kb = kbar + (size_t)J * d, *vb = vbar + (size_t)J * d;
@@ -177,11 +208,10 @@ int orc_pool(const orc_problem *p, int b, int h, double *kbar, double *vbar, int
  * E must hold D+1 entries. Returns D (the diagonal block) or a negative code. */
 int orc_energies(const orc_problem *p, const double *kbar, long kstride, int b, int h, int t, double *E,
                  double *M_out) {
-    int g = group(p), d = p->d;
-    long rows_total = (long)g * req_len(p, b);
-    long r0 = (long)t * p->tile_rows, r1 = r0 + p->tile_rows;
-    if (r1 > rows_total) r1 = rows_total;
-    int D = orc_tile_diag(p, t);
+    int d = p->d;
+    long r0, r1;
+    tile_rows(p, b, t, &r0, &r1);
+    int D = orc_tile_diag(p, b, t);
     long nr = r1 - r0;
     double *s = (double *)malloc(sizeof(double) * (size_t)nr * (size_t)(D + 1));
     double *q = (double *)malloc(sizeof(double) * (size_t)d);
@@ -250,14 +280,15 @@ int orc_select(const double *E, int D, double alpha, int sink, int window, uint8
  *   exact terms       (q.k_j/sqrt(d), v_j)               j in B_J, J in S, j <= pos
  *   correction terms  (q.kbar_J/sqrt(d) + ln|B_J|, vbar_J) J in C = {J < D} \ S
  *   O = sum e^{s-m} v / sum e^{s-m},  LSE = m + ln sum e^{s-m},  m = max s.
- * O is [tile_rows, d] and lse is [tile_rows]; rows past the request stay 0. */
+ * O is [tile_rows, d] and lse is [tile_rows], row i holding absolute packed
+ * row 128 (first tile + t) + i; rows that are not query rows stay 0. */
 int orc_attend_tile(const orc_problem *p, const double *kbar, const double *vbar, long kstride, const int32_t *cnt,
                     int b, int h, int t, const uint8_t *sel, int flags, double *O, double *lse) {
-    int g = group(p), d = p->d, B = p->block, L = req_len(p, b);
-    long rows_total = (long)g * L;
-    long r0 = (long)t * p->tile_rows, r1 = r0 + p->tile_rows;
-    if (r1 > rows_total) r1 = rows_total;
-    int D = orc_tile_diag(p, t);
+    int g = group(p), d = p->d, B = p->block, L = kv_len(p, b);
+    long r0, r1;
+    tile_rows(p, b, t, &r0, &r1);
+    long row_base = (first_tile(p, b) + t) * p->tile_rows; /* absolute row of the tile's row 0 */
+    int D = orc_tile_diag(p, b, t);
     int nb = orc_req_blocks(p, b);
     size_t maxterms = (size_t)(D + 1) * B + (size_t)nb;
     double *s = (double *)malloc(sizeof(double) * maxterms);
@@ -300,7 +331,7 @@ int orc_attend_tile(const orc_problem *p, const double *kbar, const double *vbar
         for (size_t i = 0; i < n; ++i)
             if (s[i] > m) m = s[i];
         double den = 0.0;
-        double *o = O + (size_t)(r - r0) * d;
+        double *o = O + (size_t)(r - row_base) * d;
         for (size_t i = 0; i < n; ++i) {
             double w = exp(s[i] - m);
             den += w;
@@ -313,7 +344,7 @@ int orc_attend_tile(const orc_problem *p, const double *kbar, const double *vbar
             }
         }
         for (int c = 0; c < d; ++c) o[c] /= den;
-        lse[r - r0] = m + log(den);
+        lse[r - row_base] = m + log(den);
     }
     free(s);
     free(who);
@@ -360,7 +391,7 @@ static void *orc_worker(void *arg) {
         if (i >= job->nseg) break;
         int64_t sg = job->seg_ids[i];
         int b = job->seg_b[sg], h = job->seg_h[sg], t = job->seg_t[sg];
-        int D = orc_tile_diag(p, t);
+        int D = orc_tile_diag(p, b, t);
         size_t d = (size_t)p->d;
         /* pooled rows of this (b, h): row J lives at (blk_base[b] + J) * hkv + h */
         long kstride = (long)p->hkv * p->d;

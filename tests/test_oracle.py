@@ -56,8 +56,8 @@ def dequant(p: oracle.Problem, raw, scale):
 
 
 def gathered(p: oracle.Problem, b: int):
-    """Contiguous fp64 K, V [L, hkv, d] of request b, gathered by plain indexing."""
-    L = int(p.cu_seqlens[b + 1] - p.cu_seqlens[b])
+    """Contiguous fp64 K, V [L^kv, hkv, d] of request b, gathered by plain indexing."""
+    L = int(p.kv_lengths()[b])
     j = np.arange(L)
     pages = p.page_table[b, j // p.page_size]
     K = dequant(p, p.k_pages[pages, j % p.page_size], p.c_k)
@@ -66,7 +66,8 @@ def gathered(p: oracle.Problem, b: int):
 
 
 def torch_dense_causal(p: oracle.Problem):
-    """Textbook causal softmax attention, per request and query head, via torch."""
+    """Textbook causal softmax attention, per request and query head, via torch; the L^q queries are the
+    last positions of the L^kv keys (bottom-right aligned causal mask)."""
     Q = dequant(p, p.q, p.c_q)
     out = torch.zeros_like(Q)
     for b in range(p.batch):
@@ -74,10 +75,11 @@ def torch_dense_causal(p: oracle.Problem):
         if e == s:
             continue
         K, V = gathered(p, b)
+        Lkv = K.shape[0]
         for hh in range(p.hq):
             kv = hh // p.g
             logits = Q[s:e, hh] @ K[:, kv].T / math.sqrt(D)
-            mask = torch.ones(e - s, e - s, dtype=torch.bool).tril()
+            mask = torch.ones(e - s, Lkv, dtype=torch.bool).tril(diagonal=Lkv - (e - s))
             logits = logits.masked_fill(~mask, float("-inf"))
             out[s:e, hh] = torch.softmax(logits, dim=-1) @ V[:, kv]
     return out.numpy()
@@ -89,9 +91,10 @@ def rel_err(a, b):
 
 
 def small_workload(lengths=(300, 200), hq=8, hkv=2, mu_scale=0.5, seed=1, paging="random", dtype="bf16",
-                   stripes=False):
+                   stripes=False, kv_lengths=None):
     return synth.make_workload("tiny_2k", lengths=list(lengths), hq=hq, hkv=hkv, mu_scale=mu_scale, seed=seed,
-                               paging=paging, dtype=dtype, stripes=stripes)
+                               paging=paging, dtype=dtype, stripes=stripes,
+                               kv_lengths=None if kv_lengths is None else list(kv_lengths))
 
 
 # ------------------------------------------------------ element decoding
@@ -293,27 +296,34 @@ def test_two_block_closed_form():
 def brute_force(p: oracle.Problem, alpha, sink, window, correction=True):
     """Materialises the whole [rows x blocks] pooled-logit matrix per (request, KV head) and
     selects with the per-(tile, block) maxima m_IJ, M_I and the normalised Score of Eq.1-2 (eps = 0);
-    attention enumerates each row's token set explicitly."""
+    attention enumerates each row's token set explicitly. Query rows are keyed by absolute position
+    (the new tokens are the last L^q of L^kv) and grouped into tiles by the absolute packed row
+    g pos + head mod g; the result is keyed by (request, KV head, absolute tile)."""
     Q = dequant(p, p.q, p.c_q)
     out = np.zeros(Q.shape)
     sels = {}
+    Lq_all, Lkv_all = p.lengths(), p.kv_lengths()
     for b in range(p.batch):
-        s0, L = int(p.cu_seqlens[b]), int(p.cu_seqlens[b + 1] - p.cu_seqlens[b])
-        if L == 0:
+        s0, Lq, L = int(p.cu_seqlens[b]), int(Lq_all[b]), int(Lkv_all[b])
+        if Lq == 0:
             continue
+        shift = L - Lq
         K, V = gathered(p, b)
         nb = (L + 127) // 128
         cnt = torch.tensor([min(128, L - 128 * J) for J in range(nb)], dtype=torch.float64)
         kbar = torch.stack([K[128 * J:128 * J + int(cnt[J])].mean(0) for J in range(nb)])   # [nb, hkv, d]
         vbar = torch.stack([V[128 * J:128 * J + int(cnt[J])].mean(0) for J in range(nb)])
         for h in range(p.hkv):
-            rows = torch.arange(p.g * L)
-            pos, head = rows // p.g, h * p.g + rows % p.g
-            Qp = Q[s0 + pos, head]                                   # packed Q' rows [gL, d]
-            logits = Qp @ kbar[:, h].T / math.sqrt(D)                # [gL, nb]
-            for t in range((p.g * L + 127) // 128):
-                r = slice(128 * t, min(128 * t + 128, p.g * L))
-                Dg = int(pos[128 * t]) // 128
+            pos = torch.arange(shift, L).repeat_interleave(p.g)       # absolute position of each query row
+            head = h * p.g + torch.arange(p.g).repeat(Lq)
+            tok = s0 + pos - shift                                    # row of q holding that query
+            Qp = Q[tok, head]                                         # packed Q' rows [g L^q, d]
+            logits = Qp @ kbar[:, h].T / math.sqrt(D)                 # [g L^q, nb]
+            tile = (p.g * pos + head % p.g) // 128
+            for T in torch.unique(tile).tolist():
+                r = torch.nonzero(tile == T).flatten()
+                Dg = int(pos[r[0]]) // 128
+                assert int(pos[r[-1]]) // 128 == Dg
                 lg = logits[r, :Dg + 1]
                 m_IJ = lg.max(0).values
                 S_IJ = torch.exp(lg - m_IJ).sum(0)
@@ -324,21 +334,21 @@ def brute_force(p: oracle.Problem, alpha, sink, window, correction=True):
                 J = torch.arange(Dg + 1)
                 forced = (J < sink) | ((J >= Dg - window) & (J < Dg)) | (J == Dg)
                 sel = (score >= thresh) | forced
-                sels[(b, h, t)] = sel.numpy()
-                for rr in range(r.start, r.stop):
-                    ps, hh = int(pos[rr]), int(head[rr])
+                sels[(b, h, T)] = sel.numpy()
+                for rr in r.tolist():
+                    ps, hh, tr = int(pos[rr]), int(head[rr]), int(tok[rr])
                     toks = [j for Jb in range(Dg + 1) if sel[Jb] for j in range(128 * Jb, min(128 * Jb + 128, L))
                             if j <= ps]
                     toks = torch.tensor(toks)
-                    lt = Q[s0 + ps, hh] @ K[toks, h].T / math.sqrt(D)
+                    lt = Q[tr, hh] @ K[toks, h].T / math.sqrt(D)
                     vals = V[toks, h]
                     if correction:
                         C = [Jb for Jb in range(Dg) if not sel[Jb]]
                         if C:
                             C = torch.tensor(C)
-                            lt = torch.cat([lt, Q[s0 + ps, hh] @ kbar[C, h].T / math.sqrt(D) + torch.log(cnt[C])])
+                            lt = torch.cat([lt, Q[tr, hh] @ kbar[C, h].T / math.sqrt(D) + torch.log(cnt[C])])
                             vals = torch.cat([vals, vbar[C, h]])
-                    out[s0 + ps, hh] = (torch.softmax(lt, 0) @ vals).numpy()
+                    out[tr, hh] = (torch.softmax(lt, 0) @ vals).numpy()
     return sels, out
 
 
@@ -356,7 +366,7 @@ def test_brute_force_agrees(hq, hkv, lengths, alpha, sink, window):
     seg = res["seg"]
     nonforced_pruned = 0
     for s in range(len(seg)):
-        key = (int(seg.b[s]), int(seg.h[s]), int(seg.t[s]))
+        key = (int(seg.b[s]), int(seg.h[s]), int(seg.T[s]))
         o = seg.full_off[s]
         mine = res["selection"].sel_full[o:o + seg.D[s] + 1]
         near = res["selection"].near_full[o:o + seg.D[s] + 1]
@@ -474,3 +484,151 @@ def test_tiles64_hand_example_and_token_enumeration():
         # closed form of the count: two tiles per block, one for a block with at most 64 tokens
         n = sum(2 if 128 * J + 64 < L[seg.b[s]] else 1 for J in idx[cu[s]:cu[s + 1]])
         assert tcu[s + 1] - tcu[s] == n
+
+
+# ------------------------------ P8: chunked prefill after a cached prefix (L^q < L^kv)
+
+PREFIX_CASES = [
+    # (L^q, L^kv) per request; g = 4 puts 32 positions in a tile
+    ((200, 77, 1, 0, 130), (456, 300, 129, 64, 130)),   # prefix on / off the tile grid, one query, empty chunk
+    ((300,), (1000,)),                                   # several prefix blocks, ragged KV tail
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("case", range(len(PREFIX_CASES)))
+def test_prefix_dense_matches_textbook_causal_attention(dtype, case):
+    # With alpha = 0 every causal block is exact, so each new query at absolute position L^kv - L^q + i
+    # must see exactly keys 0 .. L^kv - L^q + i of the whole KV (bottom-right aligned causal mask).
+    lq, lkv = PREFIX_CASES[case]
+    w = small_workload(lengths=lq, kv_lengths=lkv, hq=8, hkv=2, mu_scale=0.5, dtype=dtype, seed=11 + case)
+    p = oracle.Problem.from_workload(w)
+    ref = torch_dense_causal(p)
+    res = oracle.run(p, alpha=0.0, sink=1, window=1)
+    assert rel_err(res["O"], ref) < 1e-12
+    assert not np.isnan(res["O"]).any()
+    seg = res["seg"]
+    assert len(res["idx"]) == int((seg.D + 1).sum())
+    res2 = oracle.run(p, alpha=0.7, sink=0, window=0, dense=True)
+    assert rel_err(res2["O"], ref) < 1e-12
+
+
+def test_prefix_tile_geometry_hand_example():
+    # g = 4, L^q = 77 after a 223-token prefix: query rows are absolute packed rows [4 * 223, 4 * 300)
+    # = [892, 1200), i.e. tiles 6 .. 9 (tile 6 holds only position 223's 4 rows 892..895); tile T lies in
+    # block floor(32 T / 128): blocks 1, 1, 2, 2. 300 keys pool into 3 blocks (128, 128, 44 tokens).
+    w = small_workload(lengths=(77,), kv_lengths=(300,), hq=8, hkv=2, seed=4)
+    p = oracle.Problem.from_workload(w)
+    seg = oracle.segments(p)
+    assert list(seg.T) == [6, 7, 8, 9] * 2 and list(seg.t) == [0, 1, 2, 3] * 2
+    assert list(seg.D) == [1, 1, 2, 2] * 2
+    assert seg.total_blocks == 3
+    pooled = oracle.pool(p, seg)
+    assert list(pooled.cnt[:3]) == [128, 128, 44]
+    O, lse = oracle.attend(p, np.ones(seg.full_total, np.uint8), dense=True, seg=seg, seg_ids=[0, 3])
+    # tile 6: only rows 892 - 768 = 124 .. 127 are query rows; tile 9 (rows 1152..1279): 48 rows
+    assert [i for i in range(128) if lse[0, i] != 0] == [124, 125, 126, 127]
+    assert int((lse[1] != 0).sum()) == 1200 - 1152
+
+
+@pytest.mark.parametrize("hq,hkv,lq,lkv,alpha,sink,window", [
+    (8, 2, (77, 200), (300, 456), 0.05, 1, 1),
+    (4, 1, (260,), (777,), 0.1, 0, 0),
+    (2, 2, (129, 1), (640, 513), 0.02, 1, 2),
+])
+def test_prefix_brute_force_agrees(hq, hkv, lq, lkv, alpha, sink, window):
+    w = small_workload(lengths=lq, kv_lengths=lkv, hq=hq, hkv=hkv, mu_scale=0.6, seed=hq + sum(lq))
+    p = oracle.Problem.from_workload(w)
+    res = oracle.run(p, alpha=alpha, sink=sink, window=window)
+    sels, ref = brute_force(p, alpha, sink, window)
+    seg = res["seg"]
+    assert len(sels) == len(seg)
+    pruned = 0
+    for s in range(len(seg)):
+        key = (int(seg.b[s]), int(seg.h[s]), int(seg.T[s]))
+        o = seg.full_off[s]
+        mine = res["selection"].sel_full[o:o + seg.D[s] + 1]
+        near = res["selection"].near_full[o:o + seg.D[s] + 1]
+        assert not np.any((mine != sels[key].astype(np.uint8)) & (near == 0)), key
+        pruned += int((mine == 0).sum())
+    assert pruned > 0
+    assert rel_err(res["O"], ref) < 1e-12
+
+
+def test_chunked_prefill_reproduces_unchunked_tiles():
+    # A chunk run sees the same queries as the unchunked prefill of the whole sequence and the same keys up
+    # to the chunk's end, and its tiles sit on the same absolute grid: a tile of the chunk that holds only
+    # chunk rows and whose diagonal block is complete within the chunk has the same pooled means, energies,
+    # selection and output rows as that tile of the unchunked run. Every other row (the partial tile at the
+    # chunk's start, tiles whose diagonal block the chunk cuts short) agrees in dense mode.
+    full = small_workload(lengths=(700,), hq=8, hkv=2, mu_scale=0.6, seed=21)
+    pf = oracle.Problem.from_workload(full)
+    rf = oracle.run(pf, alpha=0.1, sink=1, window=1)
+    df = oracle.run(pf, alpha=0.0, sink=0, window=0, dense=True)
+    covered = np.zeros(700, bool)
+    n_same = 0
+    for lq_lo, lq_hi in [(0, 300), (300, 405), (405, 700)]:
+        # the chunk: queries lq_lo .. lq_hi - 1 against the first lq_hi keys of the same paged KV
+        pc = oracle.Problem(q=pf.q[lq_lo:lq_hi], k_pages=pf.k_pages, v_pages=pf.v_pages,
+                            cu_seqlens=np.array([0, lq_hi - lq_lo], np.int32), page_table=pf.page_table,
+                            hq=8, hkv=2, seqlens_kv=np.array([lq_hi], np.int32))
+        rc = oracle.run(pc, alpha=0.1, sink=1, window=1)
+        dc = oracle.run(pc, alpha=0.0, sink=0, window=0, dense=True)
+        sf, sc = rf["seg"], rc["seg"]
+        for s in range(len(sc)):
+            T, h = int(sc.T[s]), int(sc.h[s])
+            rows = np.arange(128 * T, 128 * T + 128)
+            pos = rows // 4
+            whole = pos.min() >= lq_lo
+            fs = int(np.nonzero((sf.T == T) & (sf.h == h))[0][0])
+            same = whole and pos.max() < lq_hi and 128 * (int(sc.D[s]) + 1) <= lq_hi
+            if same:
+                n_same += 1
+                a = rc["selection"].sel_full[sc.full_off[s]:sc.full_off[s] + sc.D[s] + 1]
+                b = rf["selection"].sel_full[sf.full_off[fs]:sf.full_off[fs] + sf.D[fs] + 1]
+                np.testing.assert_array_equal(a, b)
+            mine = (pos >= lq_lo) & (pos < lq_hi)
+            heads = h * 4 + rows % 4
+            for r in np.nonzero(mine)[0]:
+                np.testing.assert_allclose(dc["O"][pos[r] - lq_lo, heads[r]], df["O"][pos[r], heads[r]],
+                                           rtol=0, atol=1e-12)
+                if same:
+                    np.testing.assert_array_equal(rc["O"][pos[r] - lq_lo, heads[r]], rf["O"][pos[r], heads[r]])
+                covered[pos[r]] = True
+    assert covered.all() and n_same >= 20
+
+
+def test_prefix_identical_blocks_make_mean_correction_exact():
+    # Eq.7 with delta = 0 after a cached prefix: blocks of identical tokens make the corrected output equal
+    # to dense causal attention over prefix + chunk for any alpha; the uncorrected one (Eq.4) differs.
+    torch.manual_seed(6)
+    hq, hkv = 4, 1
+    lkv, lq = [900, 333], [250, 333]
+    ks, vs, qs = [], [], []
+    for L, n in zip(lkv, lq):
+        nb = (L + 127) // 128
+        kc, vc = torch.randn(nb, hkv, D), torch.randn(nb, hkv, D)
+        blk = torch.arange(L) // 128
+        ks.append(bf16_bits(kc[blk]))
+        vs.append(bf16_bits(vc[blk]))
+        qs.append((1.5 * kc[blk, 0][:, None, :] + 0.5 * torch.randn(L, hq, D))[L - n:])
+    full = paged_problem(bf16_bits(torch.cat(qs)), ks, vs, hq=hq, hkv=hkv, seed=3)
+    p = oracle.Problem(q=full.q, k_pages=full.k_pages, v_pages=full.v_pages,
+                       cu_seqlens=np.concatenate([[0], np.cumsum(lq)]).astype(np.int32), page_table=full.page_table,
+                       hq=hq, hkv=hkv, seqlens_kv=np.array(lkv, np.int32))
+    ref = torch_dense_causal(p)
+    for alpha in [0.3, 1.0]:
+        res = oracle.run(p, alpha=alpha, sink=0, window=0, correction=True)
+        assert rel_err(res["O"], ref) < 1e-12, alpha
+        assert len(res["idx"]) < int((res["seg"].D + 1).sum())
+        nocorr = oracle.run(p, alpha=alpha, sink=0, window=0, correction=False)
+        assert rel_err(nocorr["O"], ref) > 1e-6, alpha
+
+
+def test_prefix_validation_rejects_kv_shorter_than_queries():
+    w = small_workload(lengths=(100,), hq=4, hkv=1)
+    p = oracle.Problem.from_workload(w)
+    p.seqlens_kv = np.array([99], np.int32)
+    s = p.c_struct()
+    import ctypes
+    assert oracle.lib().orc_validate(ctypes.byref(s)) == -1
