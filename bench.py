@@ -87,11 +87,13 @@ def accounting(w, cu: np.ndarray, idx: np.ndarray):
     tile = 4.0 * 128 * 128 * 128
     executed = tile * float(np.sum(counts) + np.sum(chunks))
     d = 128
-    dense_equiv = 4.0 * d * w.hq * sum(L * (L + 1) / 2 for L in w.lengths)
+    kvl = kv_lengths_of(w)
+    # dense causal work: query i of a request sits at position L^kv - L^q + i and sees that many keys + 1
+    dense_equiv = 4.0 * d * w.hq * sum(Lq * (Lkv - Lq) + Lq * (Lq + 1) / 2 for Lq, Lkv in zip(w.lengths, kvl))
     eb = 2 if w.dtype == "bf16" else 1
     T = w.total_tokens
-    nblk = sum((L + 127) // 128 for L in w.lengths)
-    stage1_bytes = (T * w.hq * d * eb + 2 * T * w.hkv * d * eb      # Q, K, V read once
+    nblk = sum((L + 127) // 128 for L in kvl)
+    stage1_bytes = (T * w.hq * d * eb + 2 * sum(kvl) * w.hkv * d * eb  # Q, K, V read once
                     + nblk * w.hkv * d * (4 + 4 + 2 * eb)            # means written (fp32 + operand copies)
                     + 4 * (nseg + 1) + 4 * int(cu[-1]))              # CSR written
     causal_blocks = int(np.sum(D + 1))
@@ -100,15 +102,23 @@ def accounting(w, cu: np.ndarray, idx: np.ndarray):
                 corr_chunks=int(np.sum(chunks)), segments=nseg, rows=rows)
 
 
+def kv_lengths_of(w):
+    return list(w.kv_lengths) if getattr(w, "kv_lengths", None) is not None else list(w.lengths)
+
+
 def segments_of(w):
+    """Diagonal block and query-row count of every segment: tiles of 128 packed rows on the absolute grid
+    (row = g position + head mod g) that hold one of the request's query rows."""
     g = w.hq // w.hkv
     Ds, rows = [], []
-    for L in w.lengths:
-        nt = (g * L + 127) // 128
-        t = np.arange(nt)
+    for Lq, Lkv in zip(w.lengths, kv_lengths_of(w)):
+        if Lq == 0:
+            continue
+        t0 = g * (Lkv - Lq) // 128
+        T = np.arange(t0, (g * Lkv + 127) // 128)
         for _ in range(w.hkv):
-            Ds.append((t * 128 // g) // 128)
-            rows.append(np.minimum(128, g * L - 128 * t))
+            Ds.append((T * 128 // g) // 128)
+            rows.append(np.minimum(128, g * Lkv - 128 * T) - np.maximum(0, g * (Lkv - Lq) - 128 * T))
     cat = lambda x: np.concatenate(x) if x else np.zeros(0, np.int64)
     return dict(D=cat(Ds).astype(np.int64), rows=cat(rows).astype(np.int64))
 
@@ -181,7 +191,7 @@ def oracle_sample_time(w, cu: np.ndarray, idx: np.ndarray, target_s: float = 12.
     counts = np.diff(cu)
     # per-segment oracle work: scoring rows x (D+1) x d, attention rows x (exact keys + corrections) x 2d
     D = seg.D
-    rows = np.minimum(128, (w.hq // w.hkv) * np.asarray(w.lengths)[seg.b] - 128 * seg.t)
+    rows = segments_of(w)["rows"]
     work = rows * (D + 1) * 128 + rows * (counts * 128 + np.maximum(D - counts + 1, 0)) * 256
     rng = np.random.default_rng(1234)
     order = rng.permutation(len(seg))
@@ -313,8 +323,11 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     res = dict(metric=METRIC, value=ms_step / world, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
                ms_per_step=ms_step, higher_is_better=False, scaling="weak", vs_baseline=None,
                dtype=w.dtype, data="synthetic",
-               config=dict(workload=f"{args.workload}: batch {w.batch}, L={max(w.lengths)}, Hq={w.hq}, "
-                                    f"Hkv={w.hkv}, d=128, B=128, page 64, alpha={w.alpha}, sink 1, window 1",
+               config=dict(workload=f"{args.workload}: batch {w.batch}, L={max(w.lengths)}"
+                                    + (f" new tokens after a {max(kv_lengths_of(w)) - max(w.lengths)}-token prefix"
+                                       if w.kv_lengths is not None else "")
+                                    + f", Hq={w.hq}, Hkv={w.hkv}, d=128, B=128, page 64, alpha={w.alpha}, "
+                                    f"sink {w.sink_blocks}, window {w.window_blocks}",
                            tokens=w.total_tokens, inputs_larger_than_l2=True, l2_flush=False,
                            parallelism=f"replicas x{world}"),
                stage1_ms=s1_ms, stage2_ms=s2_ms,

@@ -45,6 +45,7 @@ class fp_problem(ctypes.Structure):
         ("dtype", ctypes.c_int32), ("c_q", ctypes.c_float), ("c_k", ctypes.c_float), ("c_v", ctypes.c_float),
         ("cu_seqlens", ctypes.c_void_p), ("page_table", ctypes.c_void_p), ("page_table_stride", ctypes.c_int32),
         ("num_pages", ctypes.c_int32), ("host_cu_seqlens", ctypes.c_void_p),
+        ("seqlens_kv", ctypes.c_void_p), ("host_seqlens_kv", ctypes.c_void_p),
     ]
 
 
@@ -76,13 +77,21 @@ lib = _load()
 
 
 class Problem:
-    """fp_problem plus the host copy of cu_seqlens it points to (kept alive here)."""
+    """fp_problem plus the host copies of cu_seqlens and seqlens_kv it points to (kept alive here).
+
+    seqlens_kv / host_seqlens_kv (optional, both or neither) give each request's KV length L^kv >= L^q:
+    the request's new tokens are then the last L^q of L^kv positions (chunked prefill after a cached prefix).
+    """
 
     def __init__(self, cu_seqlens: torch.Tensor, host_cu_seqlens, page_table: torch.Tensor, num_q_heads: int,
                  num_kv_heads: int, num_pages: int, page_size: int = 64, dtype: str = "bf16", c_q: float = 1.0,
-                 c_k: float = 1.0, c_v: float = 1.0, head_dim: int = 128, block_size: int = 128):
+                 c_k: float = 1.0, c_v: float = 1.0, head_dim: int = 128, block_size: int = 128,
+                 seqlens_kv: Optional[torch.Tensor] = None, host_seqlens_kv=None):
         self.host_cu = np.ascontiguousarray(np.asarray(host_cu_seqlens, dtype=np.int32))
+        self.host_kv = None if host_seqlens_kv is None else np.ascontiguousarray(
+            np.asarray(host_seqlens_kv, dtype=np.int32))
         self.cu_seqlens = cu_seqlens
+        self.seqlens_kv = seqlens_kv
         self.page_table = page_table
         s = fp_problem()
         s.batch = len(self.host_cu) - 1
@@ -95,13 +104,16 @@ class Problem:
         s.page_table_stride = int(page_table.shape[-1]) if page_table is not None and page_table.dim() == 2 else 0
         s.num_pages = num_pages
         s.host_cu_seqlens = self.host_cu.ctypes.data
+        s.seqlens_kv = seqlens_kv.data_ptr() if seqlens_kv is not None and seqlens_kv.numel() else None
+        s.host_seqlens_kv = self.host_kv.ctypes.data if self.host_kv is not None and self.host_kv.size else None
         self.c = s
         self.dtype = dtype
 
     @classmethod
     def from_workload(cls, w) -> "Problem":
         return cls(w.cu_seqlens, w.host_cu_seqlens, w.page_table, w.hq, w.hkv, w.num_pages,
-                   page_size=int(w.k_pages.shape[1]), dtype=w.dtype, c_q=w.c_q, c_k=w.c_k, c_v=w.c_v)
+                   page_size=int(w.k_pages.shape[1]), dtype=w.dtype, c_q=w.c_q, c_k=w.c_k, c_v=w.c_v,
+                   seqlens_kv=getattr(w, "seqlens_kv", None), host_seqlens_kv=getattr(w, "host_seqlens_kv", None))
 
     @property
     def ref(self):

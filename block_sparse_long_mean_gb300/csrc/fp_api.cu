@@ -14,7 +14,7 @@ int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
 }  // namespace
 
-// Validates the description; fills the sizes from host_cu_seqlens.
+// Validates the description; fills the sizes from host_cu_seqlens and host_seqlens_kv.
 fp_status describe(const fp_problem *p, Sizes *s) {
     if (!p || !p->host_cu_seqlens) return FP_ERR_INVALID_ARG;
     if (p->batch < 0 || p->num_q_heads <= 0 || p->num_kv_heads <= 0) return FP_ERR_INVALID_ARG;
@@ -28,28 +28,34 @@ fp_status describe(const fp_problem *p, Sizes *s) {
     if (p->dtype == FP_DTYPE_E4M3 && !(p->c_q > 0.f && p->c_k > 0.f && p->c_v > 0.f)) return FP_ERR_INVALID_ARG;
     if (p->num_pages < 0 || p->page_table_stride < 0) return FP_ERR_INVALID_ARG;
     if (p->host_cu_seqlens[0] != 0) return FP_ERR_INVALID_ARG;
+    if ((p->seqlens_kv == nullptr) != (p->host_seqlens_kv == nullptr)) return FP_ERR_INVALID_ARG;
     Sizes r;
     r.g = g;
     for (int b = 0; b < p->batch; ++b) {
         int64_t L = (int64_t)p->host_cu_seqlens[b + 1] - p->host_cu_seqlens[b];
-        if (L < 0) return FP_ERR_INVALID_ARG;
-        if (L > kMaxLen) return FP_ERR_UNSUPPORTED;
-        int64_t nb = (L + kBlock - 1) / kBlock;
-        int64_t nt = (g * L + kTileRows - 1) / kTileRows;
+        int64_t Lkv = p->host_seqlens_kv ? (int64_t)p->host_seqlens_kv[b] : L;
+        if (L < 0 || Lkv < L) return FP_ERR_INVALID_ARG;
+        if (Lkv > kMaxLen) return FP_ERR_UNSUPPORTED;
+        // tiles on the absolute packed-row grid that hold one of the request's g L query rows
+        int64_t t0 = g * (Lkv - L) / kTileRows;
+        int64_t nb = (Lkv + kBlock - 1) / kBlock;
+        int64_t nt = L > 0 ? (g * Lkv + kTileRows - 1) / kTileRows - t0 : 0;
         int64_t words = (nb + 31) / 32;
-        if ((L + p->page_size - 1) / p->page_size > p->page_table_stride) return FP_ERR_INVALID_ARG;
+        if ((Lkv + p->page_size - 1) / p->page_size > p->page_table_stride) return FP_ERR_INVALID_ARG;
         r.nseg += p->num_kv_heads * nt;
         r.nblocks += nb;
         r.mask_words += p->num_kv_heads * nt * words;
-        // sum over the request's tiles of (D + 1), D = floor(128 t / g / 128) = floor(t / g)
-        for (int64_t t = 0; t < nt; ++t) r.capacity += p->num_kv_heads * (t / g + 1);
+        // sum over the request's tiles of (D + 1), D = floor(128 T / g / 128) = floor(T / g), T = t0 + t
+        for (int64_t t = 0; t < nt; ++t) r.capacity += p->num_kv_heads * ((t0 + t) / g + 1);
         r.total_tokens += L;
-        if (L > r.max_len) r.max_len = (int32_t)L;
+        r.kv_tokens += Lkv;
+        if (Lkv > r.max_len) r.max_len = (int32_t)Lkv;
         if (nb > r.max_blocks) r.max_blocks = (int32_t)nb;
     }
     if (r.nseg >= INT32_MAX || r.nblocks >= INT32_MAX || r.mask_words >= INT32_MAX || r.total_tokens >= INT32_MAX)
         return FP_ERR_UNSUPPORTED;
-    if (r.total_tokens > 0 && (!p->cu_seqlens || !p->page_table)) return FP_ERR_INVALID_ARG;
+    if (r.kv_tokens >= INT32_MAX) return FP_ERR_UNSUPPORTED;
+    if ((r.total_tokens > 0 || r.kv_tokens > 0) && (!p->cu_seqlens || !p->page_table)) return FP_ERR_INVALID_ARG;
     *s = r;
     return FP_OK;
 }
@@ -188,7 +194,8 @@ fp_status fp_select(const fp_problem *p, const void *q, const void *k_pages, con
     if (st != FP_OK) return st;
     if (!(alpha >= 0.f) || sink_blocks < 0 || window_blocks < 0 || csr_idx_capacity < 0) return FP_ERR_INVALID_ARG;
     if (!csr_cu) return FP_ERR_INVALID_ARG;
-    if (c.s.total_tokens > 0 && (!q || !k_pages || !v_pages || !kbar || !vbar || !kbar_op || !vbar_op))
+    if ((c.s.total_tokens > 0 && !q) ||
+        (c.s.nblocks > 0 && (!k_pages || !v_pages || !kbar || !vbar || !kbar_op || !vbar_op)))
         return FP_ERR_INVALID_ARG;
     if (c.s.nseg > 0 && !csr_idx) return FP_ERR_INVALID_ARG;
     cudaError_t e = cudaMemsetAsync(c.status(), 0, 64 * 4, c.stream);
@@ -261,7 +268,7 @@ const char *fp_status_string(fp_status s) {
         case FP_ERR_DEVICE_CSR: return "device: malformed CSR segment";
         case FP_ERR_DEVICE_OVERFLOW: return "device: CSR index capacity exceeded";
         case FP_ERR_DEVICE_TIMEOUT: return "device: bounded wait expired";
-        case FP_ERR_DEVICE_SEQLEN: return "device: cu_seqlens differ from host copy";
+        case FP_ERR_DEVICE_SEQLEN: return "device: cu_seqlens or seqlens_kv differ from host copy";
     }
     return "unknown status";
 }

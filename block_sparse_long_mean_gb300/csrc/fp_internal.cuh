@@ -35,29 +35,37 @@ struct alignas(16) TileTask {
     int32_t n_chunks;   // correction chunks
     uint32_t chunk_lo, chunk_hi;
     int32_t csr_end;    // CSR offset one past the segment's last entry
-    int32_t b, h, t;    // request, KV head, tile
+    int32_t b, h;       // request, KV head
+    int32_t t;          // absolute packed tile: the tile's row i is absolute packed row 128 t + i
     int32_t D;          // diagonal block of the tile
-    int32_t rows;       // valid packed rows (<= 128)
-    int32_t q_start;    // first token of the request
-    int32_t len;        // request length
+    int32_t rows;       // query rows of the tile are [lo, rows) (rows <= 128)
+    int32_t q_start;    // token of q holding absolute position 0 (cu_seqlens[b] - (L^kv - L^q); may be < 0)
+    int32_t len;        // KV length L^kv
     int32_t blk_base;   // first pooled-mean row of the request
-    int32_t pad;
+    int32_t lo;         // first query row of the tile (> 0 only in a chunk's first tile)
     int64_t todo;       // first word of the segment's correction bitmap
 };
 static_assert(sizeof(TileTask) == 64, "TileTask is one 64-byte record");
 
-// Per-request table, built on the device from cu_seqlens at the start of each
-// call (the host mirrors it from host_cu_seqlens only to size buffers).
+// Per-request table, built on the device from cu_seqlens and seqlens_kv at the
+// start of each call (the host mirrors it from the host copies only to size
+// buffers). The request's L^q new tokens are the last of its L^kv positions;
+// packed rows are numbered by absolute position (r = g pos + head mod g) and
+// tiled 128 at a time from r = 0, so no tile straddles two blocks.
 struct ReqInfo {
-    int32_t q_start;    // cu_seqlens[b]
-    int32_t len;        // L_b
-    int32_t nblocks;    // ceil(L_b / 128)
-    int32_t ntiles;     // ceil(g L_b / 128) packed tiles per KV head
+    int32_t q_start;    // cu_seqlens[b]: token of q holding the first new query
+    int32_t len;        // L^q, new query tokens
+    int32_t kv_len;     // L^kv >= L^q: keys and values (cached prefix + new tokens)
+    int32_t t0;         // absolute tile of the request's first tile: floor(g (L^kv - L^q) / 128)
+    int32_t nblocks;    // ceil(L^kv / 128)
+    int32_t ntiles;     // packed tiles per KV head: ceil(g L^kv / 128) - t0, 0 if L^q = 0
     int32_t blk_base;   // first row of this request in the pooled-mean arrays
     int32_t seg_base;   // first CSR segment of this request (segments: h-major, then t)
     int32_t mask_base;  // first selection-mask word of this request
     int32_t words;      // selection-mask words per segment: ceil(nblocks / 32)
+    int32_t pad[2];
 };
+static_assert(sizeof(ReqInfo) == 48, "ReqInfo is three 16-byte words");
 
 // Status word slots in the workspace (int32 each).
 enum StatusSlot { kStatusCode = 0, kStatusDetail = 1 };
@@ -68,7 +76,7 @@ struct WsLayout {
 };
 
 struct Sizes {
-    int64_t nseg = 0, nblocks = 0, capacity = 0, mask_words = 0, total_tokens = 0;
+    int64_t nseg = 0, nblocks = 0, capacity = 0, mask_words = 0, total_tokens = 0, kv_tokens = 0;
     int32_t max_len = 0, max_blocks = 0, g = 1;
 };
 
@@ -126,7 +134,10 @@ __device__ __forceinline__ int find_req_by_block(const ReqInfo *req, int batch, 
 
 // Decoded coordinates of a CSR segment.
 struct SegCoord {
-    int b, h, t, D, rows;  // rows: valid packed rows of the tile (<= 128)
+    int b, h, t, D;  // request, KV head, tile within the request, diagonal block
+    int lo, rows;    // query rows of the tile: [lo, rows), rows <= 128
+    int row0;        // absolute packed row of the tile's row 0 (128 (t0 + t))
+    int q_pos;       // token of q holding the position of row 0 (below cu_seqlens[b] when lo > 0)
 };
 
 // Coordinates of segment `seg` of request b, whose record is r.
@@ -136,25 +147,18 @@ __device__ __forceinline__ SegCoord coord_in_req(const ReqInfo &r, int b, int g,
     int rem = (int)(seg - r.seg_base);
     c.h = rem / r.ntiles;
     c.t = rem - c.h * r.ntiles;
-    int r0 = c.t * kTileRows;
-    int total_rows = g * r.len;
-    c.rows = min(kTileRows, total_rows - r0);
-    c.D = (r0 / g) / kBlock;
+    const int shift = r.kv_len - r.len;
+    c.row0 = (r.t0 + c.t) * kTileRows;
+    c.lo = max(0, g * shift - c.row0);
+    c.rows = min(kTileRows, g * r.kv_len - c.row0);
+    c.D = (c.row0 / g) / kBlock;
+    c.q_pos = r.q_start - shift + c.row0 / g;
     return c;
 }
 
 __device__ __forceinline__ SegCoord decode_seg(const ReqInfo *req, int batch, int g, int64_t seg) {
-    SegCoord c;
-    c.b = find_req_by_seg(req, batch, seg);
-    const ReqInfo r = req[c.b];
-    int rem = (int)(seg - r.seg_base);
-    c.h = rem / r.ntiles;
-    c.t = rem - c.h * r.ntiles;
-    int r0 = c.t * kTileRows;
-    int total_rows = g * r.len;
-    c.rows = min(kTileRows, total_rows - r0);
-    c.D = (r0 / g) / kBlock;
-    return c;
+    const int b = find_req_by_seg(req, batch, seg);
+    return coord_in_req(req[b], b, g, seg);
 }
 
 template <int kDtype> struct Elem;

@@ -78,7 +78,8 @@ extern "C" fp_status fp_select_noalloc(const fp_problem *p, const void *q, const
     }
     if (!(alpha >= 0.f) || sink_blocks < 0 || window_blocks < 0 || csr_idx_capacity < 0) return FP_ERR_INVALID_ARG;
     if (!csr_cu) return FP_ERR_INVALID_ARG;
-    if (s.total_tokens > 0 && (!q || !k_pages || !v_pages || !kbar || !vbar || !kbar_op || !vbar_op))
+    if ((s.total_tokens > 0 && !q) ||
+        (s.nblocks > 0 && (!k_pages || !v_pages || !kbar || !vbar || !kbar_op || !vbar_op)))
         return FP_ERR_INVALID_ARG;
     if (s.nseg > 0 && !csr_idx) return FP_ERR_INVALID_ARG;
     char *scratch = nullptr;

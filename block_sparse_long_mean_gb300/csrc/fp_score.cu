@@ -202,9 +202,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 const int qb = tile_it & 1;
                 if (!mbar_wait(&sm.q_empty[qb], ((tile_it >> 1) & 1) ^ 1, ab)) break;
                 mbar_arrive_expect_tx(&sm.q_full[qb], C::kTile);
-                const int pos0 = r.q_start + (sc.t * kTileRows) / g;
+                // rows before sc.lo (a chunk's first tile) read other tokens or the zero fill; they are masked
                 for (int i = 0; i < C::kBoxes; ++i)
-                    tma_load_4d(sm.q[qb] + i * 16384, &tm_q, &sm.q_full[qb], i * C::kBoxElems, 0, sc.h, pos0);
+                    tma_load_4d(sm.q[qb] + i * 16384, &tm_q, &sm.q_full[qb], i * C::kBoxElems, 0, sc.h, sc.q_pos);
                 const int nch = sc.D / 128 + 1;
                 bool ok = true;
                 for (int cc = 0; cc < nch && ok; ++cc, ++chunk_it) {
@@ -309,11 +309,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 r_next = req[b_next];
             }
             const int ap = (tile_it >> 1) & 1;  // alternates between this set's consecutive tiles
-            const int D = sc.D, rows = sc.rows;
+            const int D = sc.D, rows = sc.rows, row_lo = sc.lo;
+            const bool my_row = j >= row_lo && j < rows;   // packed row j is one of the tile's query rows
+            const bool full = row_lo == 0 && rows == 128;
             const int qb = set;
             const int nch = D / 128 + 1;
             const float2 *ks_base = kstat + (int64_t)r.blk_base * hkv + sc.h;
-            const float lnrows = logf((float)rows);
+            const float lnrows = logf((float)(rows - row_lo));
             const int s_end = min(sink, D + 1), w_lo = max(D - window, 0);
             // mask words of this tile start as the forced set; thread k owns word k
             for (int k = rt; k < r.words; k += kRedThreads)
@@ -331,7 +333,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 // |q_r|_2 <= sqrt(d) max_i |q_ri|: the largest element magnitude of this thread's row,
                 // an integer maximum over the magnitude bits of the 16-byte chunks of the swizzled tile
                 uint32_t mx = 0;
-                if (j < rows) {
+                if (my_row) {
 #pragma unroll
                     for (int ch = 0; ch < 128 * SCfg<kDtype>::kEb / 16; ++ch) {
                         const int atom = ch >> 3, c16 = ch & 7;
@@ -378,7 +380,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     float pm[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-                    if (rows == 128) {
+                    if (full) {
 #pragma unroll
                         for (int x = 0; x < 128; x += 2)
                             pm[(x >> 1) & 7] = fmax3(pm[(x >> 1) & 7], __uint_as_float(v[x >> 5][x & 31]),
@@ -386,7 +388,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     } else {
 #pragma unroll
                         for (int x = 0; x < 128; ++x)
-                            pm[x & 7] = fmaxf(pm[x & 7], x < rows ? __uint_as_float(v[x >> 5][x & 31]) : -INFINITY);
+                            pm[x & 7] = fmaxf(pm[x & 7], x >= row_lo && x < rows ? __uint_as_float(v[x >> 5][x & 31])
+                                                                                 : -INFINITY);
                     }
                     const float m = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                           fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
@@ -402,14 +405,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
                             // a candidate: screened log-energy (operand-format kbar, fp32 sums)
                             const float k2 = scale * LOG2E;
                             float ps[4] = {0.f, 0.f, 0.f, 0.f};
-                            if (rows == 128) {
+                            if (full) {
 #pragma unroll
                                 for (int x = 0; x < 128; ++x)
                                     ps[x & 3] += ex2((__uint_as_float(v[x >> 5][x & 31]) - m) * k2);
                             } else {
 #pragma unroll
                                 for (int x = 0; x < 128; ++x)
-                                    if (x < rows) ps[x & 3] += ex2((__uint_as_float(v[x >> 5][x & 31]) - m) * k2);
+                                    if (x >= row_lo && x < rows)
+                                        ps[x & 3] += ex2((__uint_as_float(v[x >> 5][x & 31]) - m) * k2);
                             }
                             const float lE = ms + log2f((ps[0] + ps[1]) + (ps[2] + ps[3])) * LN2;
                             rs.lE[J] = lE;
@@ -484,7 +488,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 }
                 float qr[kHeadDim];
 #pragma unroll
-                for (int c = 0; c < kHeadDim; ++c) qr[c] = j < rows ? q_elem<kDtype>(sm.q[qb], j, c) * qscale : 0.f;
+                for (int c = 0; c < kHeadDim; ++c) qr[c] = my_row ? q_elem<kDtype>(sm.q[qb], j, c) * qscale : 0.f;
                 for (;;) {
                     if (rt == 0) rs.nlist = 0;
                     red_bar(set);
@@ -518,9 +522,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
                             dot = fmaf(qr[c + 2], k4.z, dot);
                             dot = fmaf(qr[c + 3], k4.w, dot);
                         }
-                        const float s = j < rows ? dot * inv_sqrt_d : -INFINITY;
+                        const float s = my_row ? dot * inv_sqrt_d : -INFINITY;
                         const float mxs = red_max(rs, set, s, 0);
-                        const float e = j < rows ? expf(s - mxs) : 0.f;
+                        const float e = my_row ? expf(s - mxs) : 0.f;
                         const float sum = red_sum(rs, set, e, 1);
                         if (rt == 0) {
                             rs.lE[J] = mxs + logf(sum);

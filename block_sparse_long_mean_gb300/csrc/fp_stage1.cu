@@ -48,17 +48,20 @@ __device__ void block_scan3(int32_t v[3], int32_t tot[3]) {
 
 // ------------------------------------------------------------------ prep kernel
 
-// Builds the per-request table from the device cu_seqlens and checks it
-// against the totals the host derived from host_cu_seqlens.
-__global__ void __launch_bounds__(1024) prep_kernel(const int32_t *__restrict__ cu, int batch, int hkv, int g,
-                                                    int64_t want_nseg, int64_t want_blocks, int64_t want_words,
-                                                    int64_t want_tokens, ReqInfo *__restrict__ req,
+// Builds the per-request table from the device cu_seqlens and seqlens_kv and
+// checks it against the totals the host derived from the host copies.
+__global__ void __launch_bounds__(1024) prep_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ kv,
+                                                    int batch, int hkv, int g, int64_t want_nseg,
+                                                    int64_t want_blocks, int64_t want_words, int64_t want_tokens,
+                                                    int64_t want_kv_tokens, ReqInfo *__restrict__ req,
                                                     int32_t *__restrict__ status) {
     __shared__ int32_t carry[3];
     __shared__ int bad;
+    __shared__ unsigned long long kv_sum;
     if (threadIdx.x == 0) {
         carry[0] = carry[1] = carry[2] = 0;
         bad = 0;
+        kv_sum = 0ull;
     }
     __syncthreads();
     for (int base = 0; base < batch; base += blockDim.x) {
@@ -68,14 +71,18 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t *__restrict__ 
         if (b < batch) {
             int32_t q0 = cu[b], q1 = cu[b + 1];
             int32_t L = q1 - q0;
-            if (q0 < 0 || L < 0 || L > kMaxLen || q1 > want_tokens) {
+            int32_t Lkv = kv ? kv[b] : L;
+            if (q0 < 0 || L < 0 || Lkv < L || Lkv > kMaxLen || q1 > want_tokens) {
                 bad = 1;
-                L = 0;
+                L = Lkv = 0;
             }
+            atomicAdd(&kv_sum, (unsigned long long)Lkv);
             r.q_start = q0;
             r.len = L;
-            r.nblocks = (L + kBlock - 1) / kBlock;
-            r.ntiles = (g * L + kTileRows - 1) / kTileRows;
+            r.kv_len = Lkv;
+            r.t0 = (g * (Lkv - L)) / kTileRows;
+            r.nblocks = (Lkv + kBlock - 1) / kBlock;
+            r.ntiles = L > 0 ? (g * Lkv + kTileRows - 1) / kTileRows - r.t0 : 0;
             r.words = (r.nblocks + 31) / 32;
             v[0] = r.nblocks;
             v[1] = hkv * r.ntiles;
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t *__restrict__ 
         s.mask_base = carry[2];
         req[batch] = s;
         if (bad || carry[0] != want_blocks || carry[1] != want_nseg || carry[2] != want_words ||
-            cu[batch] != want_tokens)
+            cu[batch] != want_tokens || kv_sum != (unsigned long long)want_kv_tokens)
             set_status(status, FP_ERR_DEVICE_SEQLEN);
     }
 }
@@ -132,7 +139,7 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ k
     const int b = find_req_by_block(req, batch, gb);
     const ReqInfo r = req[b];
     const int J = gb - r.blk_base;
-    const int n = min(kBlock, r.len - J * kBlock);
+    const int n = min(kBlock, r.kv_len - J * kBlock);
     const int row_bytes = hkv * kHeadDim * kEb;
     const int nvec = row_bytes / 16;
     const int TG = nvec >= 256 ? 1 : 256 / nvec;
@@ -277,8 +284,9 @@ __global__ void __launch_bounds__(256) csr_expand_kernel(const uint32_t *__restr
 
 cudaError_t launch_prep(const Ctx &c) {
     const int threads = 1024;
-    prep_kernel<<<1, threads, 0, c.stream>>>(c.p.cu_seqlens, c.p.batch, c.p.num_kv_heads, c.s.g, c.s.nseg,
-                                             c.s.nblocks, c.s.mask_words, c.s.total_tokens, c.req(), c.status());
+    prep_kernel<<<1, threads, 0, c.stream>>>(c.p.cu_seqlens, c.p.seqlens_kv, c.p.batch, c.p.num_kv_heads, c.s.g,
+                                             c.s.nseg, c.s.nblocks, c.s.mask_words, c.s.total_tokens,
+                                             c.s.kv_tokens, c.req(), c.status());
     return cudaGetLastError();
 }
 
@@ -318,7 +326,7 @@ __global__ void __launch_bounds__(256) tile_count_kernel(const ReqInfo *__restri
     for (int64_t i = cu[seg] + lane; i < cu[seg + 1]; i += 32) {
         const int J = idx[i];
         if (J < 0 || J >= r.nblocks) set_status(status, FP_ERR_DEVICE_CSR, (int32_t)seg);
-        else n += tiles_of_block(J, r.len);
+        else n += tiles_of_block(J, r.kv_len);
     }
     for (int o = 16; o; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
     if (lane == 0) count[seg] = n;
@@ -341,7 +349,7 @@ __global__ void __launch_bounds__(256) tile_expand_kernel(const ReqInfo *__restr
         int J = -1, n = 0;
         if (i < cu[seg + 1]) {
             J = idx[i];
-            if (J >= 0 && J < r.nblocks) n = tiles_of_block(J, r.len);
+            if (J >= 0 && J < r.nblocks) n = tiles_of_block(J, r.kv_len);
         }
         int incl = n;
         for (int o = 1; o < 32; o <<= 1) {

@@ -158,13 +158,13 @@ __global__ void __launch_bounds__(256) attn_scatter_kernel(const ReqInfo *__rest
     t.csr_end = (flags & FP_DENSE) ? 0 : cu[seg + 1];
     t.b = sc.b;
     t.h = sc.h;
-    t.t = sc.t;
+    t.t = sc.row0 / kTileRows;
     t.D = sc.D;
     t.rows = sc.rows;
-    t.q_start = r.q_start;
-    t.len = r.len;
+    t.q_start = r.q_start - (r.kv_len - r.len);
+    t.len = r.kv_len;
     t.blk_base = r.blk_base;
-    t.pad = 0;
+    t.lo = sc.lo;
     t.todo = (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
     tasks[atomicAdd(&hist[cost], 1)] = t;
 }
@@ -222,11 +222,11 @@ struct alignas(16) IterRec {
     int32_t J;      // block id; -1 - c for correction chunk c; kRecEnd after the last iteration
     int32_t tile;   // the CTA's tile counter (selects the Q buffers)
     int32_t flags;  // bit 0: first iteration of its tile, bit 1: last
-    int32_t row0;   // first packed row of the tile (t * 128)
+    int32_t row0;   // absolute packed row of the tile's row 0 (t * 128)
     int32_t D;      // diagonal block of the tile
     int32_t h;      // KV head
-    int32_t q_pos;  // first token of the tile's positions (Q rows, for its first iteration)
-    int32_t len;    // request length
+    int32_t q_pos;  // token of q holding row 0's position (Q rows, for its first iteration)
+    int32_t len;    // KV length of the request
     union {
         int32_t rows[16];  // block: pool row of each page chunk
         struct {
@@ -877,7 +877,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
             if (wn < P.nseg) nxt = P.tasks[wn];
             const int gr = cur.t * kTileRows + j;
             const int64_t rowi = (int64_t)(cur.q_start + gr / g) * P.hq + cur.h * g + gr % g;
-            const bool valid = j < cur.rows;
+            const bool valid = j >= cur.lo && j < cur.rows;
             if (task_live(cur)) {
                 if (!(ok = mbar_wait(&sm.o_full, ti & 1, ab))) break;
                 if (!(ok = mbar_wait(&sm.st_full, ti & 1, ab))) break;

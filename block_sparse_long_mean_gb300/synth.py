@@ -59,6 +59,10 @@ WORKLOADS = {
                      stripes=False),
     "varlen16_fp8": dict(lengths="loguniform16", hq=32, hkv=4, dtype="e4m3", alpha=0.2, paging="random",
                          stripes=False, base="varlen16"),
+    # chunked prefill: the last 8K tokens of the 128K Qwen3-30B-A3B-shaped sequence after its 120K-token
+    # cached prefix (the same keys, values and queries as qwen30b_128k)
+    "qwen30b_128k_chunk8k": dict(lengths=[8192], kv_lengths=[131072], hq=32, hkv=4, dtype="bf16", alpha=0.1,
+                                 paging="random", stripes=True, base="qwen30b_128k"),
 }
 # FP8 variants draw the same bf16 data as their base workload before quantising it
 WORKLOAD_INDEX = {name: i for i, name in enumerate(WORKLOADS)}
@@ -169,6 +173,8 @@ def make_workload(name: str, device="cpu", seed: int = BASE_SEED, lengths: Optio
     """
     spec = dict(WORKLOADS[name])
     cfg_id = WORKLOAD_INDEX[name]
+    if lengths is None and kv_lengths is None:
+        kv_lengths = spec.get("kv_lengths")
     if lengths is None:
         lengths = spec["lengths"]
         if lengths == "loguniform16":

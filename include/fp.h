@@ -29,31 +29,45 @@
  *     workspace's status word; the kernels never trap. fp_device_status
  *     reads it back.
  *
+ * Lengths (Sec.3.4, Alg.1 inputs): request b brings L_b^q = cu_seqlens[b+1] -
+ * cu_seqlens[b] new query tokens against L_b^kv >= L_b^q keys/values in the
+ * paged cache (seqlens_kv; L_b^kv = L_b^q without a cached prefix). The new
+ * tokens are the last L_b^q positions: query i of request b sits at absolute
+ * position L_b^kv - L_b^q + i and attends causally to keys 0 .. that position
+ * (chunked prefill, or prefill after a prefix-cache hit). Pooling, scoring and
+ * the correction cover the whole KV.
+ *
  * Layouts (row-major, innermost last)
  *   q          [T, Hq, 128] elements of `dtype`; T = cu_seqlens[batch]
  *   k_pages,   [num_pages, page_size, Hkv, 128] elements of `dtype`; token j
  *   v_pages      of request b lives in page page_table[b * stride + j / page_size]
  *                at slot j % page_size (Sec.3.3 "Paged and Variable-Length
- *                Execution", Eq.22). Slots past a request's length must hold
- *                finite values (they are multiplied by zero, never selected).
+ *                Execution", Eq.22), 0 <= j < L_b^kv. Slots past a request's KV
+ *                length must hold finite values (they are multiplied by zero,
+ *                never selected).
  *   out        [T, Hq, 128] bf16
  *   lse        [T, Hq] fp32, natural-log softmax denominator (optional)
  *   kbar, vbar [num_blocks, Hkv, 128] fp32 block means; request b's blocks
- *                are rows blk_base(b) .. blk_base(b) + ceil(L_b/128) - 1,
- *                blk_base(b) = sum_{b' < b} ceil(L_b'/128)
+ *                are rows blk_base(b) .. blk_base(b) + ceil(L_b^kv/128) - 1,
+ *                blk_base(b) = sum_{b' < b} ceil(L_b'^kv/128)
  *   kbar_op,   [num_blocks, Hkv, 128] the same means in the operand format:
  *   vbar_op      bf16, or E4M3 of mean / c_k (resp. mean / c_v) for FP8
  *   CSR        one segment per (request b, KV head h, packed tile t), in that
- *                order (Sec.3.3 "Index-Driven Sparse Traversal"); tile t holds
- *                packed rows [128 t, 128 t + 128) of Q' = PackGQA(Q), row r
- *                being position floor(r/g) of query head h*g + r mod g
- *                (Eq.12-13). csr_cu [num_segments + 1] int32 are offsets into
- *                csr_idx [capacity] int32, which lists each segment's selected
- *                128-token block ids (relative to the request) ascending.
+ *                order (Sec.3.3 "Index-Driven Sparse Traversal"). Packed row
+ *                r of Q' = PackGQA(Q) is absolute position floor(r/g) of query
+ *                head h*g + r mod g (Eq.12-13); tiles are 128 rows on that
+ *                absolute grid, so none straddles two blocks, and request b's
+ *                tiles are those holding a query row r in
+ *                [g (L_b^kv - L_b^q), g L_b^kv): tile t of the request is
+ *                absolute tile t0(b) + t, t0(b) = floor(g (L_b^kv - L_b^q) /
+ *                128) (t0 = 0 without a prefix). Its diagonal block is
+ *                D = floor((t0(b) + t) / g). csr_cu [num_segments + 1] int32
+ *                are offsets into csr_idx [capacity] int32, which lists each
+ *                segment's selected 128-token block ids (relative to the
+ *                request) ascending.
  *
  * Limits: head_dim = block_size = 128; g = Hq / Hkv a power of two <= 16;
- * page_size a power of two in [8, 128]; every request's query and KV lengths
- * are equal (prefill without a cached prefix) and at most 1,048,576 tokens.
+ * page_size a power of two in [8, 128]; 0 <= L_b^q <= L_b^kv <= 1,048,576.
  */
 #ifndef FP_H_
 #define FP_H_
@@ -81,7 +95,7 @@ typedef enum {
     FP_ERR_DEVICE_CSR = -17,      /* CSR segment malformed (ids outside [0, D] or not ascending) */
     FP_ERR_DEVICE_OVERFLOW = -18, /* selected blocks exceed the CSR index capacity */
     FP_ERR_DEVICE_TIMEOUT = -19,  /* a bounded pipeline wait expired */
-    FP_ERR_DEVICE_SEQLEN = -20    /* device cu_seqlens differ from host_cu_seqlens */
+    FP_ERR_DEVICE_SEQLEN = -20    /* device cu_seqlens / seqlens_kv differ from their host copies */
 } fp_status;
 
 typedef enum { FP_DTYPE_BF16 = 0, FP_DTYPE_E4M3 = 1 } fp_dtype;
@@ -103,9 +117,11 @@ typedef struct {
     float c_q, c_k, c_v;            /* per-tensor dequantisation scales (Eq.15); ignored for BF16 */
     const int32_t *cu_seqlens;      /* device [batch + 1], cu_seqlens[0] = 0, nondecreasing */
     const int32_t *page_table;      /* device [batch * page_table_stride] */
-    int32_t page_table_stride;      /* entries per request row, >= ceil(max L_b / page_size) */
+    int32_t page_table_stride;      /* entries per request row, >= ceil(max L_b^kv / page_size) */
     int32_t num_pages;              /* pages in the K/V pool (bounds checks) */
     const int32_t *host_cu_seqlens; /* host copy of cu_seqlens, read for sizing only */
+    const int32_t *seqlens_kv;      /* device [batch] L_b^kv >= L_b^q, or NULL: L_b^kv = L_b^q */
+    const int32_t *host_seqlens_kv; /* host copy of seqlens_kv (sizing only); NULL iff seqlens_kv is NULL */
 } fp_problem;
 
 /* Sizing (host only, no device work, no synchronisation). Each returns a
@@ -116,10 +132,11 @@ typedef struct {
  * the device must use distinct workspaces. */
 int64_t fp_workspace_bytes(const fp_problem *p);
 
-/* Number of CSR segments: sum_b Hkv * ceil(g * L_b / 128). */
+/* Number of CSR segments: sum_b Hkv * n_b, n_b = ceil(g L_b^kv / 128) - t0(b)
+ * tiles (0 when L_b^q = 0); without a prefix n_b = ceil(g L_b / 128). */
 int64_t fp_num_segments(const fp_problem *p);
 
-/* Rows of the pooled-mean arrays: sum_b ceil(L_b / 128). */
+/* Rows of the pooled-mean arrays: sum_b ceil(L_b^kv / 128). */
 int64_t fp_num_blocks(const fp_problem *p);
 
 /* Worst-case CSR index entries, sum over segments of (D + 1) where D is the
@@ -190,8 +207,8 @@ fp_status fp_select_noalloc(const fp_problem *p, const void *q, const void *k_pa
  * and attention backend index (Sec.3.4 "Serving Integration", Alg.1 step 5):
  * block J of a request becomes tiles 2J and 2J + 1, the second only when the
  * request holds a token at position (2J + 1) * 64, i.e. when
- * (2J + 1) * 64 < L_b. Segments keep their order and each stays ascending.
- *   csr_cu, csr_idx    a CSR from fp_select (block ids must lie in [0, ceil(L_b / 128));
+ * (2J + 1) * 64 < L_b^kv. Segments keep their order and each stays ascending.
+ *   csr_cu, csr_idx    a CSR from fp_select (block ids must lie in [0, ceil(L_b^kv / 128));
  *                      an id outside is skipped and reported as FP_ERR_DEVICE_CSR)
  *   tile_cu            out [num_segments + 1]
  *   tile_idx           out [tile_idx_capacity]; 2 * csr_cu[num_segments] always suffices;

@@ -29,22 +29,30 @@ def test_library_exports_every_declared_entry_point():
         assert callable(getattr(B, n)), n
 
 
-def problem(lengths, hq=32, hkv=4, page=64, dtype="bf16", **kw):
+def problem(lengths, hq=32, hkv=4, page=64, dtype="bf16", kv_lengths=None, **kw):
     cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
-    stride = max(1, max((L + page - 1) // page for L in lengths) if lengths else 1)
+    kvl = lengths if kv_lengths is None else kv_lengths
+    stride = max(1, max((L + page - 1) // page for L in kvl) if kvl else 1)
     pt = torch.zeros(len(lengths), stride, dtype=torch.int32)
+    if kv_lengths is not None:
+        kv = np.asarray(kv_lengths, dtype=np.int32)
+        kw.update(seqlens_kv=torch.from_numpy(kv.copy()), host_seqlens_kv=kv)
     return B.Problem(torch.from_numpy(cu), cu, pt, hq, hkv, num_pages=1 << 20, page_size=page, dtype=dtype, **kw)
 
 
-@pytest.mark.parametrize("lengths,hq,hkv", [
-    ([131072], 32, 4), ([32768], 32, 8), ([2048], 4, 1), ([300, 0, 129, 4096], 8, 2), ([1], 16, 1), ([], 8, 8),
+@pytest.mark.parametrize("lengths,hq,hkv,kv_lengths", [
+    ([131072], 32, 4, None), ([32768], 32, 8, None), ([2048], 4, 1, None), ([300, 0, 129, 4096], 8, 2, None),
+    ([1], 16, 1, None), ([], 8, 8, None),
+    # chunked prefill after a cached prefix: on and off the tile grid, one query, an empty chunk
+    ([8192], 32, 4, [131072]), ([77, 200, 1, 0, 130], 8, 2, [300, 456, 129, 64, 130]), ([5], 4, 4, [1000]),
 ])
-def test_sizing_matches_oracle_segments(lengths, hq, hkv):
-    p = problem(lengths, hq, hkv)
+def test_sizing_matches_oracle_segments(lengths, hq, hkv, kv_lengths):
+    p = problem(lengths, hq, hkv, kv_lengths=kv_lengths)
     op = oracle.Problem(q=np.zeros((1, hq, 128), np.uint16), k_pages=np.zeros((1, 64, hkv, 128), np.uint16),
                         v_pages=np.zeros((1, 64, hkv, 128), np.uint16),
                         cu_seqlens=np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32),
-                        page_table=np.zeros((max(len(lengths), 1), 1), np.int32), hq=hq, hkv=hkv)
+                        page_table=np.zeros((max(len(lengths), 1), 1), np.int32), hq=hq, hkv=hkv,
+                        seqlens_kv=None if kv_lengths is None else np.asarray(kv_lengths, np.int32))
     seg = oracle.segments(op)
     assert B.fp_num_segments(p) == len(seg)
     assert B.fp_num_blocks(p) == seg.total_blocks
@@ -96,6 +104,28 @@ def test_host_rejects_bad_arguments_before_any_device_work():
     p = problem([256], hq=8, hkv=2)
     p.c.cu_seqlens = None
     assert B.lib.fp_num_segments(p.ref) == -1
+
+
+def test_host_rejects_bad_kv_lengths():
+    # L^kv < L^q, one of the two seqlens_kv pointers missing, L^kv past the maximum, a page table too short
+    assert B.lib.fp_num_segments(problem([256], hq=8, hkv=2, kv_lengths=[255]).ref) == -1
+    p = problem([256], hq=8, hkv=2, kv_lengths=[512])
+    p.c.host_seqlens_kv = None
+    assert B.lib.fp_num_segments(p.ref) == -1
+    p = problem([256], hq=8, hkv=2, kv_lengths=[512])
+    p.c.seqlens_kv = None
+    assert B.lib.fp_num_segments(p.ref) == -1
+    assert B.lib.fp_num_segments(problem([256], hq=8, hkv=2, kv_lengths=[(1 << 20) + 1]).ref) == -2
+    p = problem([256], hq=8, hkv=2, kv_lengths=[512])
+    p.c.page_table_stride = 7                    # 512 keys need 8 pages of 64
+    assert B.lib.fp_num_segments(p.ref) == -1
+    # KV blocks but no query: pooling still needs the K/V buffers
+    p = problem([0], hq=8, hkv=2, kv_lengths=[300])
+    assert B.fp_num_segments(p) == 0 and B.fp_num_blocks(p) == 3
+    need = B.fp_workspace_bytes(p)
+    fake = ctypes.c_void_p(1 << 20)
+    assert B.lib.fp_select(p.ref, None, None, fake, 0.1, 1, 1, fake, None, 0, fake, fake, fake, fake, fake,
+                           need, None) == -1
 
 
 def test_status_strings():

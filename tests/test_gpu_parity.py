@@ -226,3 +226,84 @@ def test_paper_default_forced_set_parity(name):
     w.sink_blocks, w.window_blocks = 2, 4
     rep = compare(run_gpu(w), n_random=32)
     check_bf16(rep)
+
+
+# ------------------------------------------- chunked prefill after a cached prefix (L^q < L^kv)
+
+PREFIX_LQ = [1000, 77, 1, 0, 130, 333]
+PREFIX_LKV = [2600, 300, 129, 64, 130, 2048]   # prefixes on / off the tile grid, one query, empty chunk, none
+
+
+@pytest.mark.parametrize("g,hkv,page", [(8, 2, 64), (4, 1, 16), (1, 2, 128), (16, 1, 32)])
+def test_chunked_prefill_parity(g, hkv, page):
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=PREFIX_LQ, kv_lengths=PREFIX_LKV, hq=g * hkv,
+                            hkv=hkv, mu_scale=0.5, alpha=0.05, paging="random", page_size=page, seed=g + 40)
+    rep = compare(run_gpu(w))
+    check_bf16(rep)
+    assert rep.density > 0.3
+
+
+@pytest.mark.parametrize("flags,alpha", [(B.FP_DENSE, None), (B.FP_MEAN_CORRECTION, 0.0), (0, None)])
+def test_chunked_prefill_modes(flags, alpha):
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[700, 45], kv_lengths=[1900, 1000], hq=8, hkv=2,
+                            mu_scale=0.7, alpha=0.1)
+    rep = compare(run_gpu(w, flags=flags, alpha=alpha))
+    check_bf16(rep)
+    if alpha == 0.0:
+        assert rep.density == 1.0
+
+
+def test_chunked_prefill_fp8_parity():
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[1500, 77], kv_lengths=[3000, 1111], hq=8, hkv=2,
+                            dtype="e4m3", alpha=0.2, paging="random")
+    check_fp8(compare(run_gpu(w)))
+
+
+def _chunk(w, lo, hi):
+    """Queries lo .. hi - 1 of single-request workload w against its first hi keys (same paged KV)."""
+    return synth.Workload(**{**w.__dict__, "q": w.q[lo:hi].contiguous(),
+                             "cu_seqlens": torch.tensor([0, hi - lo], dtype=torch.int32, device="cuda"),
+                             "lengths": [hi - lo], "kv_lengths": [hi],
+                             "seqlens_kv": torch.tensor([hi], dtype=torch.int32, device="cuda")})
+
+
+def test_chunked_prefill_reproduces_unchunked_tiles_bit_exactly():
+    # Tiles sit on the absolute packed-row grid: a chunk tile that holds only chunk rows and whose diagonal
+    # block is complete within the chunk sees the same queries, keys and pooled means as that tile of the
+    # unchunked run, so its CSR segment and output rows are bit-identical.
+    g, hkv = 4, 2
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[3000], hq=g * hkv, hkv=hkv, mu_scale=0.6,
+                            alpha=0.05, paging="random")
+    full = run_gpu(w)
+    fcu = full.bufs.csr_cu.cpu().numpy()
+    fidx = full.bufs.csr_idx[:fcu[-1]].cpu().numpy()
+    nt_full = (g * 3000 + 127) // 128
+    same = 0
+    for lo, hi in [(0, 1024), (1024, 1100), (1100, 2333), (2333, 3000)]:
+        c = run_gpu(_chunk(w, lo, hi))
+        check_bf16(compare(c))
+        ccu = c.bufs.csr_cu.cpu().numpy()
+        cidx = c.bufs.csr_idx[:ccu[-1]].cpu().numpy()
+        t0 = g * lo // 128
+        nt = (g * hi + 127) // 128 - t0
+        for h in range(hkv):
+            for t in range(nt):
+                T = t0 + t
+                pos_lo, pos_hi = 128 * T // g, (128 * T + 127) // g
+                D = pos_lo // 128
+                if pos_lo < lo or pos_hi >= hi or 128 * (D + 1) > hi:
+                    continue
+                s, fs = h * nt + t, h * nt_full + T
+                assert np.array_equal(cidx[ccu[s]:ccu[s + 1]], fidx[fcu[fs]:fcu[fs + 1]]), (lo, hi, h, T)
+                rows = slice(pos_lo - lo, pos_hi + 1 - lo)
+                heads = slice(h * g, (h + 1) * g)
+                assert torch.equal(c.bufs.out[rows, heads], full.bufs.out[pos_lo:pos_hi + 1, heads]), (lo, hi, T)
+                same += 1
+    assert same >= 40
+
+
+def test_qwen30b_chunk_8k_after_120k_prefix_sampled_parity():
+    # the serving configuration of the paper's chunked-prefill experiment: an 8K chunk at the end of a
+    # 128K-token Qwen3-30B-A3B-shaped sequence
+    w = synth.make_workload("qwen30b_128k", device="cuda", lengths=[8192], kv_lengths=[131072])
+    check_bf16(compare(run_gpu(w), n_random=32))
