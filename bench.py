@@ -34,7 +34,14 @@ METRIC = "sparse prefill-attn ms/layer & dense-equiv TFLOP/s at 128K; tensor-pip
 UNIT = "ms/layer"
 DEFAULT_WORKLOAD = "qwen30b_128k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS_PER_STEP = 10  # fp_select: prep, pool, score, csr scan, csr expand; fp_attention: prep, meta, bucket, scatter, attention
+# fp_select: prep, pool, score, csr scan, csr expand; fp_attention: prep, meta, bucket, scatter, attention, and the
+# split combine when the tiles number fewer than 4 x SMs (the library's rule for enabling KV splits)
+KERNELS_PER_STEP = 10
+
+
+def kernels_per_step(nseg: int) -> int:
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return KERNELS_PER_STEP + (1 if nseg < 4 * sms else 0)
 
 # DRAM bytes (read + write) of one attention-kernel launch on this workload, from one ncu capture
 # (profiles/attn_tc_qwen30b_128k.md), valid while the kernel's sources are those the capture ran.
@@ -342,7 +349,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
                stage1_roofline=dict(bound="hbm", achieved=stage1_gbs, peak=float(pk.get("hbm_gbs", 6800.0)),
                                     unit="GB/s", frac=stage1_gbs / float(pk.get("hbm_gbs", 6800.0))),
                e2e=dict(value=e2e_ms, unit=UNIT, h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h)),
-               gpu_launches=KERNELS_PER_STEP * args.steps,
+               gpu_launches=kernels_per_step(acc["segments"]) * args.steps,
                clocks=clk)
     if args.dense_steps > 0:
         dstart, dstop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -67,11 +67,15 @@ WsLayout layout(const fp_problem *p, const Sizes &s) {
     w.req = o; o = align256(o + (int64_t)sizeof(ReqInfo) * (p->batch + 1));
     w.seg_count = o; o = align256(o + 4 * (s.nseg + 1));
     w.mask = o; o = align256(o + 4 * (s.mask_words + 1));
-    w.work = o; o = align256(o + (int64_t)sizeof(TileTask) * (s.nseg + 1));
+    w.work = o; o = align256(o + (int64_t)sizeof(TileTask) * (s.nseg + kMaxSlots + 1));
     w.hist = o; o = align256(o + 4 * (int64_t)(kCostBuckets + 2));
     w.counters = o; o = align256(o + 4 * 64);
     w.kstat = o; o = align256(o + 8 * (s.nblocks * p->num_kv_heads + 1));
     w.meta = o; o = align256(o + (int64_t)sizeof(SegMeta) * (s.nseg + 1));
+    w.splits = o; o = align256(o + (int64_t)sizeof(SplitRec) * kMaxSlots);
+    // partial outputs of split tiles (fp_attention only; the last region, so fp_select's scratch ends here)
+    w.part_lse = o; o = align256(o + 4 * (int64_t)kMaxSlots * kTileRows);
+    w.part_o = o; o = align256(o + 4 * (int64_t)kMaxSlots * kTileRows * kHeadDim);
     w.total = o;
     return w;
 }

@@ -20,6 +20,25 @@ constexpr int kMaxBlocks = kMaxLen / kBlock;
 constexpr int kMaxChunks = kMaxBlocks / 128;          // 128-block correction chunks per tile (64)
 constexpr int kCostBuckets = kMaxBlocks + kMaxChunks + 2;
 
+// KV splits (count-balanced, FlashPrefill V2 Eq.18): a tile whose iteration count exceeds the per-CTA
+// share C* = max(kMinSplitIters, ceil(total iterations / P)) is cut into U = ceil(n / C*) contiguous runs
+// of ceil(n / U) iterations, each run computed by its own work item into a partial-output slot and merged
+// by log-sum-exp. With P <= kSplitCtas CTAs the split tiles need at most 2 P slots.
+constexpr int kSplitCtas = 160;
+constexpr int kMaxSlots = 2 * kSplitCtas;
+constexpr int kMinSplitIters = 8;  // a run below 8 iterations costs more in pipeline fill and merge than it saves
+constexpr int kSplitTilesPerSm = 4;  // splits are enabled while tiles < 4 x SMs
+
+// Slots of the workspace counter array.
+enum CounterSlot { kCntSplitTarget = 0, kCntSlots = 1, kCntSplits = 2, kCntItems = 3 };
+
+// One split tile: its runs' partial outputs are in slots slot0 .. slot0 + nsplit - 1; the rest places
+// its rows in the output (as in TileTask).
+struct SplitRec {
+    int32_t slot0, nsplit;
+    int32_t t, h, q_start, lo, rows, pad;
+};
+
 // Per-segment Stage 2 schedule entry: iterations and correction chunks.
 struct SegMeta {
     int32_t n_exact;      // selected blocks walked exactly, -1 if the segment's CSR is malformed
@@ -43,9 +62,12 @@ struct alignas(16) TileTask {
     int32_t len;        // KV length L^kv
     int32_t blk_base;   // first pooled-mean row of the request
     int32_t lo;         // first query row of the tile (> 0 only in a chunk's first tile)
+    int32_t it_lo, it_hi;  // this work item's iterations [it_lo, it_hi) of the tile's sequence (Eq.18)
+    int32_t slot;       // partial-output slot of a split tile's run, -1 for a whole tile
+    int32_t split;      // the split tile's SplitRec, -1 for a whole tile
     int64_t todo;       // first word of the segment's correction bitmap
 };
-static_assert(sizeof(TileTask) == 64, "TileTask is one 64-byte record");
+static_assert(sizeof(TileTask) == 80, "TileTask is five 16-byte words");
 
 // Per-request table, built on the device from cu_seqlens and seqlens_kv at the
 // start of each call (the host mirrors it from the host copies only to size
@@ -72,7 +94,7 @@ enum StatusSlot { kStatusCode = 0, kStatusDetail = 1 };
 
 // Byte offsets of the workspace regions, derived on the host from the sizes.
 struct WsLayout {
-    int64_t status, req, seg_count, mask, work, hist, counters, kstat, meta, total;
+    int64_t status, req, seg_count, mask, work, hist, counters, kstat, meta, splits, part_lse, part_o, total;
 };
 
 struct Sizes {
@@ -97,6 +119,9 @@ struct Ctx {
     // per (pooled block, KV head): {|kbar - operand-format kbar|_2, |kbar|_2}
     float2 *kstat() const { return reinterpret_cast<float2 *>(wsbase + ws.kstat); }
     SegMeta *meta() const { return reinterpret_cast<SegMeta *>(wsbase + ws.meta); }
+    SplitRec *splits() const { return reinterpret_cast<SplitRec *>(wsbase + ws.splits); }
+    float *part_lse() const { return reinterpret_cast<float *>(wsbase + ws.part_lse); }  // [kMaxSlots, 128]
+    float *part_o() const { return reinterpret_cast<float *>(wsbase + ws.part_o); }      // [kMaxSlots, 128, 128]
 };
 
 // ----------------------------------------------------------------- device helpers

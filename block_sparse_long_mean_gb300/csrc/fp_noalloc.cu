@@ -69,11 +69,12 @@ extern "C" fp_status fp_select_noalloc(const fp_problem *p, const void *q, const
     fp_status st = describe(p, &s);
     if (st != FP_OK) return st;
     const WsLayout w = layout(p, s);
-    if (w.total > kNoAllocScratchBytes) {
+    // fp_select touches nothing from the split partial outputs on
+    if (w.part_lse > kNoAllocScratchBytes) {
         fprintf(stderr,
                 "libfp: fp_select_noalloc: this problem needs %lld bytes of scratch but the library's static "
                 "scratch holds %lld; use fp_select with a caller-provided workspace\n",
-                (long long)w.total, (long long)kNoAllocScratchBytes);
+                (long long)w.part_lse, (long long)kNoAllocScratchBytes);
         return FP_ERR_WORKSPACE;
     }
     if (!(alpha >= 0.f) || sink_blocks < 0 || window_blocks < 0 || csr_idx_capacity < 0) return FP_ERR_INVALID_ARG;

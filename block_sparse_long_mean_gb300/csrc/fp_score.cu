@@ -309,13 +309,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 r_next = req[b_next];
             }
             const int ap = (tile_it >> 1) & 1;  // alternates between this set's consecutive tiles
-            const int D = sc.D, rows = sc.rows, row_lo = sc.lo;
-            const bool my_row = j >= row_lo && j < rows;   // packed row j is one of the tile's query rows
-            const bool full = row_lo == 0 && rows == 128;
+            const int D = sc.D;
+            // query rows of the tile: [lo, rows) packed as rows | lo << 8 (128 for a full tile); the packed
+            // value, unpacked at each use, keeps the chunk loop within its registers
+            const int row_span = sc.rows | (sc.lo << 8);
             const int qb = set;
             const int nch = D / 128 + 1;
             const float2 *ks_base = kstat + (int64_t)r.blk_base * hkv + sc.h;
-            const float lnrows = logf((float)(rows - row_lo));
+            const float lnrows = logf((float)(sc.rows - sc.lo));
             const int s_end = min(sink, D + 1), w_lo = max(D - window, 0);
             // mask words of this tile start as the forced set; thread k owns word k
             for (int k = rt; k < r.words; k += kRedThreads)
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 // |q_r|_2 <= sqrt(d) max_i |q_ri|: the largest element magnitude of this thread's row,
                 // an integer maximum over the magnitude bits of the 16-byte chunks of the swizzled tile
                 uint32_t mx = 0;
-                if (my_row) {
+                if (j >= (row_span >> 8) && j < (row_span & 255)) {
 #pragma unroll
                     for (int ch = 0; ch < 128 * SCfg<kDtype>::kEb / 16; ++ch) {
                         const int atom = ch >> 3, c16 = ch & 7;
@@ -380,7 +381,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     float pm[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-                    if (full) {
+                    if (row_span == 128) {
 #pragma unroll
                         for (int x = 0; x < 128; x += 2)
                             pm[(x >> 1) & 7] = fmax3(pm[(x >> 1) & 7], __uint_as_float(v[x >> 5][x & 31]),
@@ -388,8 +389,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     } else {
 #pragma unroll
                         for (int x = 0; x < 128; ++x)
-                            pm[x & 7] = fmaxf(pm[x & 7], x >= row_lo && x < rows ? __uint_as_float(v[x >> 5][x & 31])
-                                                                                 : -INFINITY);
+                            pm[x & 7] = fmaxf(pm[x & 7], x >= (row_span >> 8) && x < (row_span & 255)
+                                                             ? __uint_as_float(v[x >> 5][x & 31]) : -INFINITY);
                     }
                     const float m = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                           fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
@@ -405,14 +406,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
                             // a candidate: screened log-energy (operand-format kbar, fp32 sums)
                             const float k2 = scale * LOG2E;
                             float ps[4] = {0.f, 0.f, 0.f, 0.f};
-                            if (full) {
+                            if (row_span == 128) {
 #pragma unroll
                                 for (int x = 0; x < 128; ++x)
                                     ps[x & 3] += ex2((__uint_as_float(v[x >> 5][x & 31]) - m) * k2);
                             } else {
 #pragma unroll
                                 for (int x = 0; x < 128; ++x)
-                                    if (x >= row_lo && x < rows)
+                                    if (x >= (row_span >> 8) && x < (row_span & 255))
                                         ps[x & 3] += ex2((__uint_as_float(v[x >> 5][x & 31]) - m) * k2);
                             }
                             const float lE = ms + log2f((ps[0] + ps[1]) + (ps[2] + ps[3])) * LN2;
@@ -488,7 +489,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 }
                 float qr[kHeadDim];
 #pragma unroll
-                for (int c = 0; c < kHeadDim; ++c) qr[c] = my_row ? q_elem<kDtype>(sm.q[qb], j, c) * qscale : 0.f;
+                for (int c = 0; c < kHeadDim; ++c) qr[c] = j >= (row_span >> 8) && j < (row_span & 255) ? q_elem<kDtype>(sm.q[qb], j, c) * qscale : 0.f;
                 for (;;) {
                     if (rt == 0) rs.nlist = 0;
                     red_bar(set);
@@ -522,9 +523,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
                             dot = fmaf(qr[c + 2], k4.z, dot);
                             dot = fmaf(qr[c + 3], k4.w, dot);
                         }
-                        const float s = my_row ? dot * inv_sqrt_d : -INFINITY;
+                        const float s = j >= (row_span >> 8) && j < (row_span & 255) ? dot * inv_sqrt_d : -INFINITY;
                         const float mxs = red_max(rs, set, s, 0);
-                        const float e = my_row ? expf(s - mxs) : 0.f;
+                        const float e = j >= (row_span >> 8) && j < (row_span & 255) ? expf(s - mxs) : 0.f;
                         const float sum = red_sum(rs, set, e, 1);
                         if (rt == 0) {
                             rs.lE[J] = mxs + logf(sum);

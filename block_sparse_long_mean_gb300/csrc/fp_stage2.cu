@@ -38,80 +38,115 @@ __global__ void __launch_bounds__(256) attn_meta_kernel(const ReqInfo *__restric
                                                         SegMeta *__restrict__ meta, uint32_t *__restrict__ todo,
                                                         int32_t *__restrict__ hist, int32_t *__restrict__ status) {
     __shared__ int cnt[8][kMaxChunks];
-    if (status_bad(status)) return;
+    __shared__ int cmax;
+    if (status_bad(status)) return;  // the same outcome in every thread (only the prep kernel sets that code)
     const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
     const int64_t seg = (int64_t)blockIdx.x * 8 + wl;
-    if (seg >= nseg) return;
-    const SegCoord sc = decode_seg(req, batch, g, seg);
-    const bool dense = flags & FP_DENSE;
-    const bool corr = (flags & FP_MEAN_CORRECTION) && !dense;
-    SegMeta m = {0, 0, 0u, 0u};
-    if (dense) {
-        m.n_exact = sc.D + 1;
-    } else {
-        const int64_t beg = cu[seg], end = cu[seg + 1];
-        int bad = (beg < 0 || end < beg || end > capacity) ? 1 : 0;
-        for (int c = lane; c < kMaxChunks; c += 32) cnt[wl][c] = 0;
-        __syncwarp();
-        if (!bad)
-            for (int64_t i = beg + lane; i < end; i += 32) {
-                const int J = idx[i];
-                if (J < 0 || J > sc.D || (i > beg && idx[i - 1] >= J)) bad = 1;
-                else if (J < sc.D) atomicAdd(&cnt[wl][J >> 7], 1);
-            }
-        bad = __any_sync(0xffffffffu, bad);
-        __syncwarp();
-        if (bad) {
-            m.n_exact = -1;
-            if (lane == 0) set_status(status, FP_ERR_DEVICE_CSR, (int32_t)seg);
+    if (threadIdx.x == 0) cmax = 0;
+    __syncthreads();
+    if (seg < nseg) {
+        const SegCoord sc = decode_seg(req, batch, g, seg);
+        const bool dense = flags & FP_DENSE;
+        const bool corr = (flags & FP_MEAN_CORRECTION) && !dense;
+        SegMeta m = {0, 0, 0u, 0u};
+        if (dense) {
+            m.n_exact = sc.D + 1;
         } else {
-            m.n_exact = (int)(end - beg);
-            if (corr) {
-                // correction bitmap over [0, D): every causal block fully visible to the tile, minus the
-                // selected ones (todo = valid & ~selected); read by the attention kernel per chunk
-                const ReqInfo r = req[sc.b];
-                uint32_t *tw = todo + (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
-                const int nw = (sc.D + 31) / 32;
-                for (int wd = lane; wd < nw; wd += 32) {
-                    const int left = sc.D - 32 * wd;
-                    tw[wd] = left >= 32 ? 0xffffffffu : ((1u << left) - 1u);
-                }
-                __syncwarp();
-                __threadfence_block();
+            const int64_t beg = cu[seg], end = cu[seg + 1];
+            int bad = (beg < 0 || end < beg || end > capacity) ? 1 : 0;
+            for (int c = lane; c < kMaxChunks; c += 32) cnt[wl][c] = 0;
+            __syncwarp();
+            if (!bad)
                 for (int64_t i = beg + lane; i < end; i += 32) {
                     const int J = idx[i];
-                    if (J < sc.D) atomicAnd(&tw[J >> 5], ~(1u << (J & 31)));
+                    if (J < 0 || J > sc.D || (i > beg && idx[i - 1] >= J)) bad = 1;
+                    else if (J < sc.D) atomicAdd(&cnt[wl][J >> 7], 1);
                 }
-                const int nch = (sc.D + 127) / 128;
-                for (int c0 = 0; c0 < kMaxChunks; c0 += 32) {
-                    const int c = c0 + lane;
-                    const bool need = c < nch && cnt[wl][c] < min(128, sc.D - 128 * c);
-                    const unsigned bal = __ballot_sync(0xffffffffu, need);
-                    if (c0 == 0) m.chunk_lo = bal; else m.chunk_hi = bal;
+            bad = __any_sync(0xffffffffu, bad);
+            __syncwarp();
+            if (bad) {
+                m.n_exact = -1;
+                if (lane == 0) set_status(status, FP_ERR_DEVICE_CSR, (int32_t)seg);
+            } else {
+                m.n_exact = (int)(end - beg);
+                if (corr) {
+                    // correction bitmap over [0, D): every causal block fully visible to the tile, minus the
+                    // selected ones (todo = valid & ~selected); read by the attention kernel per chunk
+                    const ReqInfo r = req[sc.b];
+                    uint32_t *tw = todo + (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
+                    const int nw = (sc.D + 31) / 32;
+                    for (int wd = lane; wd < nw; wd += 32) {
+                        const int left = sc.D - 32 * wd;
+                        tw[wd] = left >= 32 ? 0xffffffffu : ((1u << left) - 1u);
+                    }
+                    __syncwarp();
+                    __threadfence_block();
+                    for (int64_t i = beg + lane; i < end; i += 32) {
+                        const int J = idx[i];
+                        if (J < sc.D) atomicAnd(&tw[J >> 5], ~(1u << (J & 31)));
+                    }
+                    const int nch = (sc.D + 127) / 128;
+                    for (int c0 = 0; c0 < kMaxChunks; c0 += 32) {
+                        const int c = c0 + lane;
+                        const bool need = c < nch && cnt[wl][c] < min(128, sc.D - 128 * c);
+                        const unsigned bal = __ballot_sync(0xffffffffu, need);
+                        if (c0 == 0) m.chunk_lo = bal; else m.chunk_hi = bal;
+                    }
+                    m.n_chunks = __popc(m.chunk_lo) + __popc(m.chunk_hi);
                 }
-                m.n_chunks = __popc(m.chunk_lo) + __popc(m.chunk_hi);
             }
         }
+        if (lane == 0) {
+            meta[seg] = m;
+            const int cost = m.n_exact < 0 ? 0 : min(m.n_exact + m.n_chunks, kCostBuckets - 1);
+            atomicAdd(&hist[cost], 1);
+            atomicMax(&cmax, cost);
+        }
     }
-    if (lane == 0) {
-        meta[seg] = m;
-        const int cost = m.n_exact < 0 ? 0 : min(m.n_exact + m.n_chunks, kCostBuckets - 1);
-        atomicAdd(&hist[cost], 1);
-    }
+    // the largest cost, so that the bucket scan covers only [0, max]
+    __syncthreads();
+    if (threadIdx.x == 0 && cmax > 0) atomicMax(&hist[kCostBuckets], cmax);
 }
 
-// Turns the cost histogram into descending-cost bucket offsets (one CTA).
-__global__ void __launch_bounds__(1024) attn_bucket_kernel(int32_t *__restrict__ hist, int32_t *__restrict__ status) {
+// Number of runs a tile of `cost` iterations is cut into (count-balanced KV splits, Eq.18).
+__device__ __forceinline__ int num_splits(int cost, int target) { return cost > target ? (cost + target - 1) / target : 1; }
+
+// Turns the cost histogram into descending-cost offsets of the work list (one CTA). With splits
+// (ctas > 0) it first sums the iterations of all tiles and fixes the split target
+// C* = max(kMinSplitIters, ceil(total / ctas)); a bucket of cost c then takes num_splits(c, C*) work
+// items per tile. Without, every tile is one item.
+__global__ void __launch_bounds__(1024) attn_bucket_kernel(int32_t *__restrict__ hist, int32_t *__restrict__ counters,
+                                                           int ctas, int32_t *__restrict__ status) {
     __shared__ int32_t warp_sums[32];
-    __shared__ int32_t carry;
+    __shared__ long long warp_tot[32];
+    __shared__ int32_t carry, target;
     if (status_bad(status)) return;
-    if (threadIdx.x == 0) carry = 0;
-    __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int base = 0; base < kCostBuckets; base += 1024) {
+    const int nb = hist[kCostBuckets] + 1;  // buckets 0 .. the largest cost
+    long long tot = 0;
+    if (ctas > 0) {
+        for (int c = threadIdx.x; c < nb; c += 1024) tot += (long long)c * hist[c];
+        for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if (lane == 0) warp_tot[warp] = tot;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        long long all = 0;
+        if (ctas > 0)
+            for (int i = 0; i < 32; ++i) all += warp_tot[i];
+        const long long per = ctas > 0 ? (all + ctas - 1) / ctas : (long long)kCostBuckets;
+        target = (int)max((long long)kMinSplitIters, min(per, (long long)kCostBuckets));
+        counters[kCntSplitTarget] = target;
+        counters[kCntSlots] = 0;
+        counters[kCntSplits] = 0;
+        carry = 0;
+    }
+    __syncthreads();
+    const int tgt = target;
+    for (int base = 0; base < nb; base += 1024) {
         const int i = base + threadIdx.x;
-        const int bucket = kCostBuckets - 1 - i;  // descending cost
-        int32_t v = i < kCostBuckets ? hist[bucket] : 0;
+        const int bucket = nb - 1 - i;  // descending cost
+        int32_t v = i < nb ? hist[bucket] * num_splits(bucket, tgt) : 0;
         const int32_t own = v;
         for (int o = 1; o < 32; o <<= 1) {
             int32_t n = __shfl_up_sync(0xffffffffu, v, o);
@@ -131,23 +166,27 @@ __global__ void __launch_bounds__(1024) attn_bucket_kernel(int32_t *__restrict__
         const int32_t excl = carry + (warp ? warp_sums[warp - 1] : 0) + v - own;
         const int32_t total = warp_sums[31];
         __syncthreads();
-        if (i < kCostBuckets) hist[bucket] = excl;
+        if (i < nb) hist[bucket] = excl;
         if (threadIdx.x == 0) carry += total;
         __syncthreads();
     }
+    if (threadIdx.x == 0) counters[kCntItems] = carry;  // length of the work list
 }
 
-// Places every segment in the work list (descending cost) as a TileTask.
+// Places every segment in the work list (descending cost) as one TileTask, or as one per run when the
+// tile is split; a split tile also takes consecutive partial-output slots and a SplitRec.
 __global__ void __launch_bounds__(256) attn_scatter_kernel(const ReqInfo *__restrict__ req, int batch, int g,
                                                            const SegMeta *__restrict__ meta, int32_t nseg,
                                                            const int32_t *__restrict__ cu, int flags,
-                                                           int32_t *__restrict__ hist, TileTask *__restrict__ tasks,
+                                                           int32_t *__restrict__ hist, int32_t *__restrict__ counters,
+                                                           SplitRec *__restrict__ splits, TileTask *__restrict__ tasks,
                                                            int32_t *__restrict__ status) {
     if (status_bad(status)) return;
     const int64_t seg = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (seg >= nseg) return;
     const SegMeta m = meta[seg];
     const int cost = m.n_exact < 0 ? 0 : min(m.n_exact + m.n_chunks, kCostBuckets - 1);
+    const int nsplit = num_splits(cost, counters[kCntSplitTarget]);
     const SegCoord sc = decode_seg(req, batch, g, seg);
     const ReqInfo r = req[sc.b];
     TileTask t;
@@ -165,8 +204,84 @@ __global__ void __launch_bounds__(256) attn_scatter_kernel(const ReqInfo *__rest
     t.len = r.kv_len;
     t.blk_base = r.blk_base;
     t.lo = sc.lo;
+    t.it_lo = 0;
+    t.it_hi = m.n_exact < 0 ? 0 : m.n_exact + m.n_chunks;
+    t.slot = -1;
+    t.split = -1;
     t.todo = (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
-    tasks[atomicAdd(&hist[cost], 1)] = t;
+    const int pos = atomicAdd(&hist[cost], nsplit);
+    if (nsplit == 1) {
+        tasks[pos] = t;
+        return;
+    }
+    const int slot0 = atomicAdd(&counters[kCntSlots], nsplit);
+    const bool room = slot0 + nsplit <= kMaxSlots;  // always, by the choice of the split target
+    if (room) {
+        t.split = atomicAdd(&counters[kCntSplits], 1);
+        splits[t.split] = SplitRec{slot0, nsplit, t.t, t.h, t.q_start, t.lo, t.rows, 0};
+    } else {
+        set_status(status, FP_ERR_DEVICE_OVERFLOW, (int32_t)seg);
+        t.n_exact = -2;  // not run
+    }
+    const int per = (cost + nsplit - 1) / nsplit;
+    for (int u = 0; u < nsplit; ++u) {
+        t.it_lo = u * per;
+        t.it_hi = min(cost, (u + 1) * per);
+        t.slot = slot0 + u;
+        tasks[pos + u] = t;
+    }
+}
+
+// ------------------------------------------------------------ split combine
+
+// Merges the runs of every split tile (the LSE combine of split-KV attention): per query row,
+// lse = ln sum_u e^{lse_u} and O = sum_u e^{lse_u - lse} O_u over its runs' normalised outputs. CTA
+// 4 k + q takes rows 32 q .. 32 q + 31 of split tile k; thread i of it row 32 q + i / 32 and columns
+// 4 (i % 32) .. + 3, so a warp reads one 512-byte row of a run's partial output and every thread has only
+// its runs' loads to wait for. The grid is small (an empty launch costs little) and strides over the tiles.
+constexpr int kCombineThreads = 1024, kCombineTiles = 40;
+__global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const SplitRec *__restrict__ splits,
+                                                                       const int32_t *__restrict__ counters,
+                                                                       const float *__restrict__ part_o,
+                                                                       const float *__restrict__ part_lse,
+                                                                       __nv_bfloat16 *__restrict__ out,
+                                                                       float *__restrict__ lse, int hq, int g,
+                                                                       const int32_t *__restrict__ status) {
+    const int nsplit_tiles = counters[kCntSplits];
+    if (status_bad(status)) return;
+    const int j = 32 * (blockIdx.x & 3) + (threadIdx.x >> 5), cg = threadIdx.x & 31;
+    for (int k = blockIdx.x >> 2; k < nsplit_tiles; k += gridDim.x >> 2) {
+        const SplitRec sr = splits[k];
+        if (j < sr.lo || j >= sr.rows) continue;
+        const float *lp = part_lse + (int64_t)sr.slot0 * kTileRows + j;
+        const float4 *op = reinterpret_cast<const float4 *>(part_o + ((int64_t)sr.slot0 * kTileRows + j) * kHeadDim) + cg;
+        constexpr int64_t kRunStride4 = (int64_t)kTileRows * kHeadDim / 4;  // float4s between runs
+        float m = -INFINITY;
+#pragma unroll 4
+        for (int u = 0; u < sr.nsplit; ++u) m = fmaxf(m, lp[u * kTileRows]);
+        float sum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int u = 0; u < sr.nsplit; ++u) {
+            const float w = expf(lp[u * kTileRows] - m);
+            const float4 x = op[u * kRunStride4];
+            sum += w;
+            acc.x = fmaf(w, x.x, acc.x);
+            acc.y = fmaf(w, x.y, acc.y);
+            acc.z = fmaf(w, x.z, acc.z);
+            acc.w = fmaf(w, x.w, acc.w);
+        }
+        const float rs = 1.f / sum;
+        const int gr = sr.t * kTileRows + j;
+        const int64_t rowi = (int64_t)(sr.q_start + gr / g) * hq + sr.h * g + gr % g;
+        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x * rs, acc.y * rs);
+        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z * rs, acc.w * rs);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t *>(&lo2);
+        pk.y = *reinterpret_cast<const uint32_t *>(&hi2);
+        reinterpret_cast<uint2 *>(out + rowi * kHeadDim)[cg] = pk;
+        if (lse && cg == 0) lse[rowi] = m + logf(sum);
+    }
 }
 
 // --------------------------------------------------------------- attention
@@ -253,7 +368,7 @@ struct AttnSmem {
     uint64_t q_full, q_empty, k_full[kKStages], v_full[kVStages], grp[4], p_full[2], qk_done[2], o_full, o_empty,
         st_full, rec_full[kRing], rec_empty[kRing];
     uint32_t tmem_base;
-    int abort, skip;
+    int abort, skip, nitems;
 };
 
 static_assert(sizeof(AttnSmem<FP_DTYPE_BF16>) <= 232448, "attention shared memory exceeds the 227 KB opt-in limit");
@@ -290,14 +405,19 @@ struct AttnParams {
     float *lse;
     int hq, g, flags;
     float c_q, c_k, c_v;
-    int32_t nseg;
+    int32_t nseg;              // segments
+    const int32_t *nitems;     // work-list length with splits (written by the bucket kernel)
+    float *part_o, *part_lse;  // partial outputs of split tiles' runs
     uint32_t smem_bytes;
     int32_t *status;
 };
 
-__device__ __forceinline__ bool task_live(const TileTask &t) { return t.n_exact >= 0 && t.n_exact + t.n_chunks > 0; }
+template <bool kSplit>
+__device__ __forceinline__ bool task_live(const TileTask &t) {
+    return t.n_exact >= 0 && (kSplit ? t.it_hi > t.it_lo : t.n_exact + t.n_chunks > 0);
+}
 
-template <int kDtype>
+template <int kDtype, bool kSplit>
 __global__ void __launch_bounds__(kAThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
@@ -332,6 +452,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
             mbar_init(&sm.rec_empty[i], kRingUsers);
         }
         sm.abort = 0;
+        if (kSplit) sm.nitems = *P.nitems;
         // an earlier stage failed: every warp skips its role (one read, so the CTA agrees)
         sm.skip = status_bad(P.status) ? 1 : 0;
         fence_barrier_init();
@@ -385,20 +506,24 @@ __global__ void __launch_bounds__(kAThreads, 1)
             const int per = 32 / npc;  // block lookups per batch
             uint32_t ti = 0;
             int w = blockIdx.x;
+            const int nitems = kSplit ? sm.nitems : P.nseg;
             TileTask cur;
-            if (w < P.nseg) cur = P.tasks[w];
-            while (w < P.nseg && ok) {
+            if (w < nitems) cur = P.tasks[w];
+            while (w < nitems && ok) {
                 const int wn = w + gridDim.x;
                 TileTask nxt;
-                if (wn < P.nseg) nxt = P.tasks[wn];  // overlaps this tile
-                if (task_live(cur)) {
-                    const int n = cur.n_exact + cur.n_chunks;
-                    int it = 0;
+                if (wn < nitems) nxt = P.tasks[wn];  // overlaps this tile
+                if (task_live<kSplit>(cur)) {
+                    // this item's iterations [it_lo, it_hi) of the tile's sequence: the selected blocks
+                    // (iterations 0 .. n_exact - 1), then the correction chunks
+                    const int it_lo = kSplit ? cur.it_lo : 0, it_hi = kSplit ? cur.it_hi : cur.n_exact + cur.n_chunks;
+                    const int e_hi = min(it_hi, cur.n_exact);
+                    int it = it_lo;
                     // selected blocks, descending (Eq.17): lane l looks up block base + l / npc, page chunk l % npc
-                    for (int bs = 0; bs < cur.n_exact && ok; bs += per) {
+                    for (int bs = it_lo; bs < e_hi && ok; bs += per) {
                         const int my = bs + lane / npc, pc = lane % npc;
                         int Jl = 0, rowl = oob_row;
-                        if (my < cur.n_exact) {
+                        if (my < e_hi) {
                             Jl = dense ? cur.D - my : __ldg(P.csr_idx + cur.csr_end - 1 - my);
                             const int tok = Jl * kBlock + pc * ps_eff;
                             if (tok < cur.len) {
@@ -409,16 +534,17 @@ __global__ void __launch_bounds__(kAThreads, 1)
                                     set_status(status, FP_ERR_DEVICE_PAGE, page);
                             }
                         }
-                        const int cnt = min(per, cur.n_exact - bs);
+                        const int cnt = min(per, e_hi - bs);
                         for (int i = 0; i < cnt; ++i, ++it) {
                             const int J = __shfl_sync(0xffffffffu, Jl, i * npc);
                             const int row = __shfl_sync(0xffffffffu, rowl, i * npc + pc);
-                            const int fl = (it == 0 ? 1 : 0) | (it == n - 1 ? 2 : 0);
+                            const int fl = (it == it_lo ? 1 : 0) | (it == it_hi - 1 ? 2 : 0);
                             if (!(ok = emit(J, fl, (int)ti, cur, make_uint4(0, 0, 0, 0), row))) break;
                         }
                     }
                     // correction chunks, descending: list them, then look up 32 masks at a time
-                    if (cur.n_chunks > 0 && ok) {
+                    const int c_lo = max(it_lo - cur.n_exact, 0), c_hi = it_hi - cur.n_exact;
+                    if (c_hi > c_lo && ok) {
                         const uint32_t hi = cur.chunk_hi, lo = cur.chunk_lo;
                         const unsigned below = (1u << lane) - 1u;
                         const bool in_hi = (hi >> (31 - lane)) & 1u, in_lo = (lo >> (31 - lane)) & 1u;
@@ -428,10 +554,10 @@ __global__ void __launch_bounds__(kAThreads, 1)
                         if (in_lo) sm.chunk_list[__popc(hi) + __popc(blo & below)] = (uint8_t)(31 - lane);
                         __syncwarp();
                         const int nw = (cur.D + 31) / 32;
-                        for (int bs = 0; bs < cur.n_chunks && ok; bs += 32) {
+                        for (int bs = c_lo; bs < c_hi && ok; bs += 32) {
                             int cl = 0;
                             uint4 ml = make_uint4(0, 0, 0, 0);
-                            if (bs + lane < cur.n_chunks) {
+                            if (bs + lane < c_hi) {
                                 cl = sm.chunk_list[bs + lane];
                                 const uint32_t *tw = P.todo + cur.todo + 4 * cl;
                                 ml.x = 4 * cl + 0 < nw ? __ldg(tw + 0) : 0u;
@@ -439,7 +565,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
                                 ml.z = 4 * cl + 2 < nw ? __ldg(tw + 2) : 0u;
                                 ml.w = 4 * cl + 3 < nw ? __ldg(tw + 3) : 0u;
                             }
-                            const int cnt = min(32, cur.n_chunks - bs);
+                            const int cnt = min(32, c_hi - bs);
                             for (int i = 0; i < cnt; ++i, ++it) {
                                 const int c = __shfl_sync(0xffffffffu, cl, i);
                                 uint4 mk;
@@ -447,7 +573,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
                                 mk.y = __shfl_sync(0xffffffffu, ml.y, i);
                                 mk.z = __shfl_sync(0xffffffffu, ml.z, i);
                                 mk.w = __shfl_sync(0xffffffffu, ml.w, i);
-                                const int fl = (it == 0 ? 1 : 0) | (it == n - 1 ? 2 : 0);
+                                const int fl = (it == it_lo ? 1 : 0) | (it == it_hi - 1 ? 2 : 0);
                                 if (!(ok = emit(-1 - c, fl, (int)ti, cur, mk, 0))) break;
                             }
                         }
@@ -869,22 +995,25 @@ __global__ void __launch_bounds__(kAThreads, 1)
         bool ok = true;
         uint32_t ti = 0;
         int w = blockIdx.x;
+        const int nitems = kSplit ? sm.nitems : P.nseg;
         TileTask cur;
-        if (w < P.nseg) cur = P.tasks[w];
-        while (w < P.nseg && ok) {
+        if (w < nitems) cur = P.tasks[w];
+        while (w < nitems && ok) {
             const int wn = w + gridDim.x;
             TileTask nxt;
-            if (wn < P.nseg) nxt = P.tasks[wn];
+            if (wn < nitems) nxt = P.tasks[wn];
             const int gr = cur.t * kTileRows + j;
             const int64_t rowi = (int64_t)(cur.q_start + gr / g) * P.hq + cur.h * g + gr % g;
             const bool valid = j >= cur.lo && j < cur.rows;
-            if (task_live(cur)) {
+            if (task_live<kSplit>(cur)) {
                 if (!(ok = mbar_wait(&sm.o_full, ti & 1, ab))) break;
                 if (!(ok = mbar_wait(&sm.st_full, ti & 1, ab))) break;
                 tc_fence_after();
                 const float mx = sm.stat_m[j], l = sm.stat_l[j];
                 const float inv = l > 0.f ? P.c_v / l : 0.f;
+                const bool part = kSplit && cur.slot >= 0;  // one run of a split tile: fp32 partial output
                 __nv_bfloat16 *orow = P.out + rowi * kHeadDim;
+                float *prow = P.part_o + ((int64_t)cur.slot * kTileRows + j) * kHeadDim;
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) {
                     uint32_t ov[2][32];
@@ -899,7 +1028,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&sm.o_empty);
                     }
-                    if (valid) {
+                    if (valid && !part) {
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
@@ -916,9 +1045,24 @@ __global__ void __launch_bounds__(kAThreads, 1)
                                 *reinterpret_cast<uint4 *>(orow + q2 * 64 + hh * 32 + e) = pk;
                             }
                         }
+                    } else if (valid) {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4)
+                                *reinterpret_cast<float4 *>(prow + q2 * 64 + hh * 32 + e) =
+                                    make_float4(__uint_as_float(ov[hh][e]) * inv, __uint_as_float(ov[hh][e + 1]) * inv,
+                                                __uint_as_float(ov[hh][e + 2]) * inv,
+                                                __uint_as_float(ov[hh][e + 3]) * inv);
                     }
                 }
-                if (valid && P.lse) P.lse[rowi] = (mx + log2f(l) - pshift) * 0.6931471805599453f;
+                if (!part) {
+                    if (valid && P.lse) P.lse[rowi] = (mx + log2f(l) - pshift) * 0.6931471805599453f;
+                } else {
+                    if (valid)
+                        P.part_lse[cur.slot * kTileRows + j] =
+                            l > 0.f ? (mx + log2f(l) - pshift) * 0.6931471805599453f : -INFINITY;
+                }
                 ++ti;
             } else if (cur.n_exact == 0 && cur.n_chunks == 0 && valid) {
                 // a well-formed segment with nothing to attend: zero rows
@@ -957,14 +1101,20 @@ cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, c
                              const int32_t *csr_cu, const int32_t *csr_idx, int64_t capacity, const void *kbar_op,
                              const void *vbar_op, int flags, void *out, float *lse) {
     const int32_t nseg = (int32_t)c.s.nseg;
-    cudaError_t e = cudaMemsetAsync(c.hist(), 0, sizeof(int32_t) * kCostBuckets, c.stream);
+    // the histogram and, past it, the largest cost
+    cudaError_t e = cudaMemsetAsync(c.hist(), 0, sizeof(int32_t) * (kCostBuckets + 1), c.stream);
     if (e != cudaSuccess) return e;
     attn_meta_kernel<<<(nseg + 7) / 8, 256, 0, c.stream>>>(c.req(), c.p.batch, c.s.g, nseg, csr_cu, csr_idx,
                                                             capacity, flags, c.meta(), c.mask(), c.hist(),
                                                             c.status());
-    attn_bucket_kernel<<<1, 1024, 0, c.stream>>>(c.hist(), c.status());
+    // KV splits pay off only when the tiles do not fill the GPU several times over; larger problems run the
+    // kernel without the split path (every tile one work item)
+    const bool split = nseg < kSplitTilesPerSm * num_sms();
+    const int split_ctas = !split ? 0 : num_sms() < kSplitCtas ? num_sms() : kSplitCtas;
+    attn_bucket_kernel<<<1, 1024, 0, c.stream>>>(c.hist(), c.counters(), split_ctas, c.status());
     attn_scatter_kernel<<<(nseg + 255) / 256, 256, 0, c.stream>>>(c.req(), c.p.batch, c.s.g, c.meta(), nseg, csr_cu,
-                                                                   flags, c.hist(), c.tasks(), c.status());
+                                                                   flags, c.hist(), c.counters(), c.splits(),
+                                                                   c.tasks(), c.status());
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
     const bool fp8 = c.p.dtype == FP_DTYPE_E4M3;
@@ -996,7 +1146,8 @@ cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, c
         if (!make_tmap(&tm_kb, kb, fp8, 3, dims, strides, box)) return cudaErrorInvalidValue;
         if (!make_tmap(&tm_vb, vb, fp8, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    const int grid = nseg < num_sms() ? nseg : num_sms();
+    // with splits every SM: the work list may hold more runs than segments
+    const int grid = split || nseg > num_sms() ? num_sms() : nseg;
     AttnParams prm;
     prm.pt = c.p.page_table;
     prm.pt_stride = c.p.page_table_stride;
@@ -1014,22 +1165,28 @@ cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, c
     prm.c_k = fp8 ? c.p.c_k : 1.f;
     prm.c_v = fp8 ? c.p.c_v : 1.f;
     prm.nseg = nseg;
+    prm.nitems = c.counters() + kCntItems;
+    prm.part_o = c.part_o();
+    prm.part_lse = c.part_lse();
     prm.status = c.status();
-    if (fp8) {
-        const size_t smem = smem_request(sizeof(AttnSmem<FP_DTYPE_E4M3>));
+    auto launch = [&](auto kernel, size_t layout) -> cudaError_t {
+        const size_t smem = smem_request(layout);
         prm.smem_bytes = (uint32_t)smem;
-        e = cudaFuncSetAttribute(attn_tc_kernel<FP_DTYPE_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        attn_tc_kernel<FP_DTYPE_E4M3><<<grid, kAThreads, smem, c.stream>>>(tm_q, tm_k, tm_v, tm_kb, tm_vb, prm);
-    } else {
-        const size_t smem = smem_request(sizeof(AttnSmem<FP_DTYPE_BF16>));
-        prm.smem_bytes = (uint32_t)smem;
-        e = cudaFuncSetAttribute(attn_tc_kernel<FP_DTYPE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        attn_tc_kernel<FP_DTYPE_BF16><<<grid, kAThreads, smem, c.stream>>>(tm_q, tm_k, tm_v, tm_kb, tm_vb, prm);
-    }
+        cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        kernel<<<grid, kAThreads, smem, c.stream>>>(tm_q, tm_k, tm_v, tm_kb, tm_vb, prm);
+        return cudaSuccess;
+    };
+    if (fp8)
+        e = split ? launch(attn_tc_kernel<FP_DTYPE_E4M3, true>, sizeof(AttnSmem<FP_DTYPE_E4M3>))
+                  : launch(attn_tc_kernel<FP_DTYPE_E4M3, false>, sizeof(AttnSmem<FP_DTYPE_E4M3>));
+    else
+        e = split ? launch(attn_tc_kernel<FP_DTYPE_BF16, true>, sizeof(AttnSmem<FP_DTYPE_BF16>))
+                  : launch(attn_tc_kernel<FP_DTYPE_BF16, false>, sizeof(AttnSmem<FP_DTYPE_BF16>));
+    if (e != cudaSuccess) return e;
+    if (split)
+        attn_combine_kernel<<<4 * kCombineTiles, kCombineThreads, 0, c.stream>>>(
+            c.splits(), c.counters(), c.part_o(), c.part_lse(), (__nv_bfloat16 *)out, lse, hq, g, c.status());
     return cudaGetLastError();
 }
 

@@ -270,18 +270,22 @@ def _chunk(w, lo, hi):
 def test_chunked_prefill_reproduces_unchunked_tiles_bit_exactly():
     # Tiles sit on the absolute packed-row grid: a chunk tile that holds only chunk rows and whose diagonal
     # block is complete within the chunk sees the same queries, keys and pooled means as that tile of the
-    # unchunked run, so its CSR segment and output rows are bit-identical.
+    # unchunked run, so its CSR segment is bit-identical, and so are its output rows unless one of the two
+    # runs split the tile into KV runs: each run rounds its probabilities to bf16 against its own running
+    # maximum, so split and whole tiles differ at the bf16 rounding level (both still meet the oracle bar).
     g, hkv = 4, 2
     w = synth.make_workload("tiny_2k", device="cuda", lengths=[3000], hq=g * hkv, hkv=hkv, mu_scale=0.6,
                             alpha=0.05, paging="random")
     full = run_gpu(w)
+    ftarget, fcost = _split_plan(full)
     fcu = full.bufs.csr_cu.cpu().numpy()
     fidx = full.bufs.csr_idx[:fcu[-1]].cpu().numpy()
     nt_full = (g * 3000 + 127) // 128
-    same = 0
+    same = exact = 0
     for lo, hi in [(0, 1024), (1024, 1100), (1100, 2333), (2333, 3000)]:
         c = run_gpu(_chunk(w, lo, hi))
         check_bf16(compare(c))
+        ctarget, ccost = _split_plan(c)
         ccu = c.bufs.csr_cu.cpu().numpy()
         cidx = c.bufs.csr_idx[:ccu[-1]].cpu().numpy()
         t0 = g * lo // 128
@@ -297,9 +301,15 @@ def test_chunked_prefill_reproduces_unchunked_tiles_bit_exactly():
                 assert np.array_equal(cidx[ccu[s]:ccu[s + 1]], fidx[fcu[fs]:fcu[fs + 1]]), (lo, hi, h, T)
                 rows = slice(pos_lo - lo, pos_hi + 1 - lo)
                 heads = slice(h * g, (h + 1) * g)
-                assert torch.equal(c.bufs.out[rows, heads], full.bufs.out[pos_lo:pos_hi + 1, heads]), (lo, hi, T)
+                a, b = c.bufs.out[rows, heads].float(), full.bufs.out[pos_lo:pos_hi + 1, heads].float()
+                unsplit = (ctarget is None or ccost[s] <= ctarget) and (ftarget is None or fcost[fs] <= ftarget)
+                if unsplit:
+                    assert torch.equal(a, b), (lo, hi, T)
+                    exact += 1
+                else:
+                    assert float((a - b).abs().max()) <= 1.5e-2, (lo, hi, T)
                 same += 1
-    assert same >= 40
+    assert same >= 40 and exact >= 10, (same, exact)
 
 
 def test_qwen30b_chunk_8k_after_120k_prefix_sampled_parity():
@@ -307,3 +317,61 @@ def test_qwen30b_chunk_8k_after_120k_prefix_sampled_parity():
     # 128K-token Qwen3-30B-A3B-shaped sequence
     w = synth.make_workload("qwen30b_128k", device="cuda", lengths=[8192], kv_lengths=[131072])
     check_bf16(compare(run_gpu(w), n_random=32))
+
+
+# ------------------------------------------------------ count-balanced KV splits (Eq.18)
+
+def _split_plan(r):
+    """The split rule applied to the GPU's own CSR on the host: splits are on while the tiles number fewer than
+    4 x SMs; then C* = max(8, ceil(total iterations / P)), P = min(SMs, 160), and a tile of n > C* iterations
+    runs as ceil(n / C*) pieces. Returns (C* or None when splits are off, per-segment iteration counts)."""
+    import oracle
+    cu = r.bufs.csr_cu.cpu().numpy().astype(np.int64)
+    idx = r.bufs.csr_idx[:cu[-1]].cpu().numpy()
+    seg = oracle.segments(oracle.Problem.from_workload(r.w))
+    dense = bool(r.flags & B.FP_DENSE)
+    corr = bool(r.flags & B.FP_MEAN_CORRECTION) and not dense
+    cost = []
+    for s in range(len(seg)):
+        D = int(seg.D[s])
+        if dense:
+            cost.append(D + 1)
+            continue
+        ids = idx[cu[s]:cu[s + 1]]
+        chunks = 0
+        if corr and D > 0:
+            full = np.bincount(ids[ids < D] // 128, minlength=(D + 127) // 128)
+            chunks = int(np.sum(full < np.minimum(128, D - 128 * np.arange((D + 127) // 128))))
+        cost.append(len(ids) + chunks)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if len(seg) >= 4 * sms:
+        return None, np.array(cost)
+    target = max(8, -(-sum(cost) // min(sms, 160)))
+    return target, np.array(cost)
+
+
+@pytest.mark.parametrize("flags,alpha", [(B.FP_DENSE, None), (B.FP_MEAN_CORRECTION, 0.0),
+                                         (B.FP_MEAN_CORRECTION, 0.02), (0, 0.02)])
+def test_kv_splits_parity_when_tiles_are_few(flags, alpha):
+    # one 8K request with one head (64 tiles, fewer than the SMs): the heavy last tiles are cut into
+    # count-balanced runs whose partial outputs are merged by log-sum-exp inside the attention kernel
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[8192], hq=1, hkv=1, mu_scale=0.5)
+    r = run_gpu(w, flags=flags, alpha=alpha)
+    target, cost = _split_plan(r)
+    assert target is not None and cost.max() > target, (cost.max(), target)
+    check_bf16(compare(r))
+
+
+def test_kv_splits_fp8_and_chunked_prefill():
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[640, 33], kv_lengths=[6000, 2100], hq=2, hkv=1,
+                            dtype="e4m3", alpha=0.05, mu_scale=0.5)
+    r = run_gpu(w)
+    target, cost = _split_plan(r)
+    assert target is not None and cost.max() > target, (cost.max(), target)
+    check_fp8(compare(r))
+
+
+def test_kv_splits_are_deterministic():
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[4096], hq=2, hkv=1, mu_scale=0.5, alpha=0.02)
+    a, b = run_gpu(w), run_gpu(w)
+    assert torch.equal(a.bufs.out, b.bufs.out) and torch.equal(a.bufs.lse, b.bufs.lse)
