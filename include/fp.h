@@ -129,7 +129,8 @@ typedef struct {
 
 /* Bytes of device workspace fp_select and fp_attention need (256-byte aligned
  * base). One workspace may serve both calls of a layer; calls that overlap on
- * the device must use distinct workspaces. */
+ * the device must use distinct workspaces. It includes 21 MB for the partial
+ * outputs of KV splits (320 slots of 128 x 128 fp32). */
 int64_t fp_workspace_bytes(const fp_problem *p);
 
 /* Number of CSR segments: sum_b Hkv * n_b, n_b = ceil(g L_b^kv / 128) - t0(b)
@@ -167,6 +168,14 @@ fp_status fp_select(const fp_problem *p, const void *q, const void *k_pages, con
  * "Implementation"), all in one online softmax; the epilogue divides by the
  * accumulated denominator. FP8 computes S = c_q c_k (Q~K~^T), quantises
  * P~ = e4m3(256 exp(S - m)) and O = c_v sum P~V~ / sum P~ (Eq.15).
+ * When the problem has fewer packed tiles than four times the GPU's SMs, a
+ * tile of n > C* iterations (selected blocks, then correction chunks) is cut
+ * into U = ceil(n / C*) contiguous runs of ceil(n / U) iterations
+ * (count-balanced KV splits, Sec.3.3 Eq.18), C* = max(8, ceil(total
+ * iterations / min(SMs, 160))); each run writes a normalised fp32 partial
+ * output and its LSE to the workspace, and a combine kernel merges them:
+ * lse = ln sum_u e^{lse_u}, O = sum_u e^{lse_u - lse} O_u. The result equals
+ * the unsplit one up to rounding.
  *   csr_cu, csr_idx   a CSR in fp_select's format (ignored with FP_DENSE); every
  *                     segment is checked (ids in [0, D], ascending, within
  *                     csr_idx_capacity) and a malformed one is skipped and
@@ -186,7 +195,8 @@ fp_status fp_attention(const fp_problem *p, const void *q, const void *k_pages, 
  * packaging variant of fp_select that computes the same outputs, bit for bit.
  * Scratch comes from a fixed 16 MiB device array inside the library, which
  * every GPU that loads the library holds until the process exits.
- *   - Problems whose workspace (fp_workspace_bytes) exceeds 16 MiB are
+ *   - Problems whose fp_select scratch (fp_workspace_bytes less the 21 MB of
+ *     split partial outputs that only fp_attention uses) exceeds 16 MiB are
  *     rejected with FP_ERR_WORKSPACE before anything is enqueued.
  *   - It calls no allocator. The first call on each device looks up the
  *     array's device address with that device current; make that first call
