@@ -119,7 +119,9 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t *__restrict__ 
 // One CTA per (request, block): the means of its <= 128 tokens for every KV
 // head (Eq.5). Each thread accumulates one 16-byte column vector of the
 // token rows over a strided subset of tokens in fp32; a shared-memory pass
-// sums the token groups. FP8 elements are descaled before summing.
+// sums the token groups. FP8 elements are descaled before summing. The
+// block's page ids are looked up once per CTA, and the per-head rounding
+// statistics are reduced within each warp before their shared atomics.
 template <int kDtype>
 __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ kp, const uint8_t *__restrict__ vp,
                                                    const int32_t *__restrict__ page_table, int pt_stride,
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ k
     constexpr int kEpv = 16 / kEb;  // elements per 16-byte vector
     __shared__ float red[2][256 * kEpv];
     __shared__ float kst[2][64];  // per KV head: squared rounding error and squared norm of kbar
+    __shared__ int32_t pages[kBlock / 8];  // the block's page ids (page_size >= 8), -1 if out of range
     if (status_bad(status)) return;
     if (threadIdx.x < 64) kst[0][threadIdx.x] = kst[1][threadIdx.x] = 0.f;
     const int gb = blockIdx.x;
@@ -140,6 +143,14 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ k
     const ReqInfo r = req[b];
     const int J = gb - r.blk_base;
     const int n = min(kBlock, r.kv_len - J * kBlock);
+    const int npg = (n + page_size - 1) / page_size;  // pages holding the block's tokens (blocks start on a page)
+    if (threadIdx.x < npg) {
+        const int page = page_table[(int64_t)b * pt_stride + (J * kBlock) / page_size + threadIdx.x];
+        const bool ok = page >= 0 && page < num_pages;
+        if (!ok) set_status(status, FP_ERR_DEVICE_PAGE, page);
+        pages[threadIdx.x] = ok ? page : -1;
+    }
+    __syncthreads();
     const int row_bytes = hkv * kHeadDim * kEb;
     const int nvec = row_bytes / 16;
     const int TG = nvec >= 256 ? 1 : 256 / nvec;
@@ -154,15 +165,11 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ k
         for (int e = 0; e < kEpv; ++e) ak[e] = av[e] = 0.f;
         if (col < nvec && tg < TG) {
             for (int j = tg; j < n; j += TG) {
-                const int tok = J * kBlock + j;
-                const int page = page_table[(int64_t)b * pt_stride + tok / page_size];
-                if (page < 0 || page >= num_pages) {
-                    set_status(status, FP_ERR_DEVICE_PAGE, page);
-                    continue;
-                }
-                const int64_t off = ((int64_t)page * page_size + tok % page_size) * row_bytes + (int64_t)col * 16;
-                const uint4 kraw = *reinterpret_cast<const uint4 *>(kp + off);
-                const uint4 vraw = *reinterpret_cast<const uint4 *>(vp + off);
+                const int page = pages[j / page_size];
+                if (page < 0) continue;
+                const int64_t off = ((int64_t)page * page_size + j % page_size) * row_bytes + (int64_t)col * 16;
+                const uint4 kraw = __ldg(reinterpret_cast<const uint4 *>(kp + off));
+                const uint4 vraw = __ldg(reinterpret_cast<const uint4 *>(vp + off));
                 const typename E::T *ke = reinterpret_cast<const typename E::T *>(&kraw);
                 const typename E::T *ve = reinterpret_cast<const typename E::T *>(&vraw);
 #pragma unroll
@@ -182,6 +189,7 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ k
         for (int x = threadIdx.x; x < cols * kEpv; x += 256) {
             const int lc = x / kEpv, e = x % kEpv;
             const int colx = c0 + lc;
+            // element c0 kEpv + x: the bound hkv * 128 is a multiple of 32, so whole warps skip together
             if (colx >= nvec) continue;
             float sk_ = 0.f, sv_ = 0.f;
             for (int t = 0; t < TG; ++t) {
@@ -204,9 +212,18 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ k
                 reinterpret_cast<__nv_bfloat16 *>(vbar_op)[oi] = __float2bfloat16_rn(mv);
                 kq = __bfloat162float(k16);
             }
-            const int head = (colx * kEpv + e) / kHeadDim;
-            atomicAdd(&kst[0][head], (mk - kq) * (mk - kq));
-            atomicAdd(&kst[1][head], mk * mk);
+            // a warp's 32 consecutive elements lie in one head: reduce them before the shared atomics
+            float e2 = (mk - kq) * (mk - kq), n2 = mk * mk;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                e2 += __shfl_xor_sync(0xffffffffu, e2, o);
+                n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+            }
+            if ((threadIdx.x & 31) == 0) {
+                const int head = (colx * kEpv + e) / kHeadDim;
+                atomicAdd(&kst[0][head], e2);
+                atomicAdd(&kst[1][head], n2);
+            }
         }
         __syncthreads();
     }
@@ -216,26 +233,63 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ k
 
 // ------------------------------------------------------------------ CSR kernels
 
-// Exclusive scan of the per-segment counts into csr_cu (one CTA).
+// Exclusive scan of the per-segment counts into csr_cu (one CTA). In rounds of
+// 32 warps x 1024 counts, warp w scans its own 1024 consecutive counts, 32 at
+// a time with coalesced loads and stores, and the CTA offsets the warps by a
+// scan of their totals.
 __global__ void __launch_bounds__(1024) csr_scan_kernel(const int32_t *__restrict__ count, int32_t nseg,
                                                         int64_t capacity, int32_t *__restrict__ cu,
                                                         int32_t *__restrict__ status) {
+    constexpr int kRows = 32;  // rows of 32 counts per warp and round
+    __shared__ int32_t wsum[32];
     __shared__ int32_t carry;
-    if (threadIdx.x == 0) carry = 0;
-    __syncthreads();
     if (status_bad(status)) {
         if (threadIdx.x == 0) cu[0] = 0;
         return;
     }
-    for (int base = 0; base < nseg; base += blockDim.x) {
-        const int i = base + threadIdx.x;
-        int32_t v[3] = {i < nseg ? count[i] : 0, 0, 0};
-        const int32_t own = v[0];
-        int32_t tot[3];
-        block_scan3(v, tot);
-        if (i < nseg) cu[i] = carry + v[0] - own;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry = 0;
+    for (int base = 0; base < nseg; base += 32 * 32 * kRows) {
+        const int cs = base + warp * 32 * kRows;
+        int32_t v[kRows];
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+            const int i = cs + 32 * q + lane;
+            v[q] = i < nseg ? count[i] : 0;
+        }
+        int32_t run = 0;  // the warp's running total; v[q] becomes the exclusive prefix within the warp's counts
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+            int32_t x = v[q];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t n = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += n;
+            }
+            const int32_t own = v[q];
+            v[q] = run + x - own;
+            run += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) wsum[warp] = run;
         __syncthreads();
-        if (threadIdx.x == 0) carry += tot[0];
+        if (warp == 0) {
+            int32_t w = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t n = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += n;
+            }
+            wsum[lane] = w;
+        }
+        __syncthreads();
+        const int32_t off = carry + (warp ? wsum[warp - 1] : 0);
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) {
+            const int i = cs + 32 * q + lane;
+            if (i < nseg) cu[i] = off + v[q];
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) carry += wsum[31];
         __syncthreads();
     }
     if (threadIdx.x == 0) {

@@ -30,82 +30,92 @@ using namespace sm100;
 
 // ------------------------------------------------------------ schedule prep
 
-// One warp per segment: validates its CSR, counts selected blocks per
-// 128-block chunk, and records the iteration counts and chunk mask.
+// One warp per segment (a CTA takes 32, four per warp): validates its CSR,
+// counts selected blocks per 128-block chunk, and records the iteration
+// counts and chunk mask. The CTA's 32 costs enter the histogram with one
+// atomic per distinct cost: most tiles share a handful of costs, and
+// same-address atomics from every segment would serialise.
+constexpr int kMetaSegs = 32;
 __global__ void __launch_bounds__(256) attn_meta_kernel(const ReqInfo *__restrict__ req, int batch, int g,
                                                         int32_t nseg, const int32_t *__restrict__ cu,
                                                         const int32_t *__restrict__ idx, int64_t capacity, int flags,
                                                         SegMeta *__restrict__ meta, uint32_t *__restrict__ todo,
                                                         int32_t *__restrict__ hist, int32_t *__restrict__ status) {
     __shared__ int cnt[8][kMaxChunks];
-    __shared__ int cmax;
+    __shared__ int scost[kMetaSegs];
     if (status_bad(status)) return;  // the same outcome in every thread (only the prep kernel sets that code)
     const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
-    const int64_t seg = (int64_t)blockIdx.x * 8 + wl;
-    if (threadIdx.x == 0) cmax = 0;
-    __syncthreads();
-    if (seg < nseg) {
-        const SegCoord sc = decode_seg(req, batch, g, seg);
-        const bool dense = flags & FP_DENSE;
-        const bool corr = (flags & FP_MEAN_CORRECTION) && !dense;
-        SegMeta m = {0, 0, 0u, 0u};
-        if (dense) {
-            m.n_exact = sc.D + 1;
-        } else {
-            const int64_t beg = cu[seg], end = cu[seg + 1];
-            int bad = (beg < 0 || end < beg || end > capacity) ? 1 : 0;
-            for (int c = lane; c < kMaxChunks; c += 32) cnt[wl][c] = 0;
-            __syncwarp();
-            if (!bad)
-                for (int64_t i = beg + lane; i < end; i += 32) {
-                    const int J = idx[i];
-                    if (J < 0 || J > sc.D || (i > beg && idx[i - 1] >= J)) bad = 1;
-                    else if (J < sc.D) atomicAdd(&cnt[wl][J >> 7], 1);
-                }
-            bad = __any_sync(0xffffffffu, bad);
-            __syncwarp();
-            if (bad) {
-                m.n_exact = -1;
-                if (lane == 0) set_status(status, FP_ERR_DEVICE_CSR, (int32_t)seg);
+    for (int k = 0; k < kMetaSegs / 8; ++k) {
+        const int64_t seg = (int64_t)blockIdx.x * kMetaSegs + 8 * k + wl;
+        int cost = -1;
+        if (seg < nseg) {
+            const SegCoord sc = decode_seg(req, batch, g, seg);
+            const bool dense = flags & FP_DENSE;
+            const bool corr = (flags & FP_MEAN_CORRECTION) && !dense;
+            SegMeta m = {0, 0, 0u, 0u};
+            if (dense) {
+                m.n_exact = sc.D + 1;
             } else {
-                m.n_exact = (int)(end - beg);
-                if (corr) {
-                    // correction bitmap over [0, D): every causal block fully visible to the tile, minus the
-                    // selected ones (todo = valid & ~selected); read by the attention kernel per chunk
-                    const ReqInfo r = req[sc.b];
-                    uint32_t *tw = todo + (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
-                    const int nw = (sc.D + 31) / 32;
-                    for (int wd = lane; wd < nw; wd += 32) {
-                        const int left = sc.D - 32 * wd;
-                        tw[wd] = left >= 32 ? 0xffffffffu : ((1u << left) - 1u);
-                    }
-                    __syncwarp();
-                    __threadfence_block();
+                const int64_t beg = cu[seg], end = cu[seg + 1];
+                int bad = (beg < 0 || end < beg || end > capacity) ? 1 : 0;
+                for (int c = lane; c < kMaxChunks; c += 32) cnt[wl][c] = 0;
+                __syncwarp();
+                if (!bad)
                     for (int64_t i = beg + lane; i < end; i += 32) {
                         const int J = idx[i];
-                        if (J < sc.D) atomicAnd(&tw[J >> 5], ~(1u << (J & 31)));
+                        if (J < 0 || J > sc.D || (i > beg && idx[i - 1] >= J)) bad = 1;
+                        else if (J < sc.D) atomicAdd(&cnt[wl][J >> 7], 1);
                     }
-                    const int nch = (sc.D + 127) / 128;
-                    for (int c0 = 0; c0 < kMaxChunks; c0 += 32) {
-                        const int c = c0 + lane;
-                        const bool need = c < nch && cnt[wl][c] < min(128, sc.D - 128 * c);
-                        const unsigned bal = __ballot_sync(0xffffffffu, need);
-                        if (c0 == 0) m.chunk_lo = bal; else m.chunk_hi = bal;
+                bad = __any_sync(0xffffffffu, bad);
+                __syncwarp();
+                if (bad) {
+                    m.n_exact = -1;
+                    if (lane == 0) set_status(status, FP_ERR_DEVICE_CSR, (int32_t)seg);
+                } else {
+                    m.n_exact = (int)(end - beg);
+                    if (corr) {
+                        // correction bitmap over [0, D): every causal block fully visible to the tile, minus the
+                        // selected ones (todo = valid & ~selected); read by the attention kernel per chunk
+                        const ReqInfo r = req[sc.b];
+                        uint32_t *tw = todo + (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
+                        const int nw = (sc.D + 31) / 32;
+                        for (int wd = lane; wd < nw; wd += 32) {
+                            const int left = sc.D - 32 * wd;
+                            tw[wd] = left >= 32 ? 0xffffffffu : ((1u << left) - 1u);
+                        }
+                        __syncwarp();
+                        __threadfence_block();
+                        for (int64_t i = beg + lane; i < end; i += 32) {
+                            const int J = idx[i];
+                            if (J < sc.D) atomicAnd(&tw[J >> 5], ~(1u << (J & 31)));
+                        }
+                        const int nch = (sc.D + 127) / 128;
+                        for (int c0 = 0; c0 < kMaxChunks; c0 += 32) {
+                            const int c = c0 + lane;
+                            const bool need = c < nch && cnt[wl][c] < min(128, sc.D - 128 * c);
+                            const unsigned bal = __ballot_sync(0xffffffffu, need);
+                            if (c0 == 0) m.chunk_lo = bal; else m.chunk_hi = bal;
+                        }
+                        m.n_chunks = __popc(m.chunk_lo) + __popc(m.chunk_hi);
                     }
-                    m.n_chunks = __popc(m.chunk_lo) + __popc(m.chunk_hi);
                 }
             }
+            if (lane == 0) meta[seg] = m;
+            cost = m.n_exact < 0 ? 0 : min(m.n_exact + m.n_chunks, kCostBuckets - 1);
+            __syncwarp();
         }
-        if (lane == 0) {
-            meta[seg] = m;
-            const int cost = m.n_exact < 0 ? 0 : min(m.n_exact + m.n_chunks, kCostBuckets - 1);
-            atomicAdd(&hist[cost], 1);
-            atomicMax(&cmax, cost);
-        }
+        if (lane == 0) scost[8 * k + wl] = cost;
     }
-    // the largest cost, so that the bucket scan covers only [0, max]
     __syncthreads();
-    if (threadIdx.x == 0 && cmax > 0) atomicMax(&hist[kCostBuckets], cmax);
+    if (wl == 0) {
+        const int c = scost[lane];
+        const unsigned peers = __match_any_sync(0xffffffffu, c);
+        if (c >= 0 && lane == __ffs(peers) - 1) atomicAdd(&hist[c], __popc(peers));
+        // the largest cost, so that the bucket scan covers only [0, max]
+        int mx = c;
+        for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0 && mx > 0) atomicMax(&hist[kCostBuckets], mx);
+    }
 }
 
 // Number of runs a tile of `cost` iterations is cut into (count-balanced KV splits, Eq.18).
@@ -209,7 +219,12 @@ __global__ void __launch_bounds__(256) attn_scatter_kernel(const ReqInfo *__rest
     t.slot = -1;
     t.split = -1;
     t.todo = (int64_t)r.mask_base + (int64_t)(sc.h * r.ntiles + sc.t) * r.words;
-    const int pos = atomicAdd(&hist[cost], nsplit);
+    // one atomic per distinct cost in the warp (equal costs take equal run counts)
+    const unsigned peers = __match_any_sync(__activemask(), cost);
+    const int lane = threadIdx.x & 31, leader = __ffs(peers) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(&hist[cost], nsplit * __popc(peers));
+    const int pos = __shfl_sync(peers, base, leader) + nsplit * __popc(peers & ((1u << lane) - 1));
     if (nsplit == 1) {
         tasks[pos] = t;
         return;
@@ -1104,7 +1119,7 @@ cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, c
     // the histogram and, past it, the largest cost
     cudaError_t e = cudaMemsetAsync(c.hist(), 0, sizeof(int32_t) * (kCostBuckets + 1), c.stream);
     if (e != cudaSuccess) return e;
-    attn_meta_kernel<<<(nseg + 7) / 8, 256, 0, c.stream>>>(c.req(), c.p.batch, c.s.g, nseg, csr_cu, csr_idx,
+    attn_meta_kernel<<<(nseg + kMetaSegs - 1) / kMetaSegs, 256, 0, c.stream>>>(c.req(), c.p.batch, c.s.g, nseg, csr_cu, csr_idx,
                                                             capacity, flags, c.meta(), c.mask(), c.hist(),
                                                             c.status());
     // KV splits pay off only when the tiles do not fill the GPU several times over; larger problems run the
