@@ -38,11 +38,12 @@ namespace {
 
 using namespace sm100;
 
-// warp 0: TMA, warp 1: MMA + TMEM, warps 2-3 idle; warps 4-7 and 8-11: two reduction / selection sets
-// that take alternate tiles, so one tile's selection overlaps the next tile's scores
+// Two independent pipelines ("sets") take the CTA's tiles alternately, so that one tile's selection overlaps
+// the other set's scores and neither set's pace holds up the other. Set s: warp 2 s loads its Q tiles
+// (lane 1) and pooled-key chunks (lane 0) by TMA, warp 2 s + 1 issues its MMAs into its own TMEM columns,
+// and warps 4 + 4 s .. 7 + 4 s reduce and select. Warp 1 also owns the TMEM allocation.
 constexpr int kSWarps = 12;
 constexpr int kSThreads = 32 * kSWarps;
-constexpr int kSStages = 2;  // pooled-key chunk stages
 // registers per thread: 64K over the CTA at launch, then 48 for the TMA/MMA warpgroup and 224 for each set
 constexpr int kSRegsLaunch = (65536 / kSThreads) & ~7;
 constexpr int kSRegsProducer = 48, kSRegsReduce = 224;
@@ -65,28 +66,50 @@ struct SCfg {
         instr_desc(kDtype == FP_DTYPE_BF16 ? 1u : 0u, kDtype == FP_DTYPE_BF16 ? 1u : 0u, false, false, 128, 128);
 };
 
-// Scratch of one reduction set.
-struct RedScratch {
-    float lE[kMaxBlocks];       // screened log-energy, upper bound, or refined value
-    uint8_t state[kMaxBlocks];  // see kSt* below
+// Fixed-size scratch of one reduction set.
+struct RedFixed {
     int32_t list[kRefineList];
-    uint32_t words[kMaxBlocks / 32];  // selection mask of the current tile
-    int32_t cand[kCand];              // blocks with a screened log-energy
+    int32_t cand[kCand];  // blocks with a screened log-energy
     float red[2][4];
     float red3[3][4];
     int nlist, ncand, nsel;
     int any2[2];  // per tile of the set, alternately: some candidate was left open (read after the tile's last barrier)
 };
 
-template <int kDtype>
-struct ScoreSmem {
-    alignas(1024) uint8_t q[2][SCfg<kDtype>::kTile];  // Q buffer s belongs to set s
-    alignas(1024) uint8_t k[kSStages][SCfg<kDtype>::kTile];
-    RedScratch rs[2];
-    uint64_t q_full[2], q_empty[2], k_full[kSStages], k_empty[kSStages], s_full[2][2], s_empty[2][2];
+// Barriers of the two sets (index [set] or [set][stage / S buffer]).
+struct ScoreBars {
+    uint64_t q_full[2], q_empty[2], k_full[2][2], k_empty[2][2], s_full[2][2], s_empty[2][2];
     uint32_t tmem_base;
     int abort;
 };
+
+// Shared-memory layout (byte offsets from a 1024-byte aligned base): Q buffer per set, nst chunk stages per
+// set, the barriers, then each set's scratch with per-block arrays for nb blocks (a multiple of 128).
+struct SLayout {
+    uint32_t q, k, bars, fixed[2], lE[2], words[2], state[2], total;
+};
+__host__ __device__ inline SLayout score_layout(int tile, int nst, int nb) {
+    SLayout L;
+    uint32_t o = 0;
+    L.q = o;
+    o += 2 * tile;
+    L.k = o;
+    o += 2 * nst * tile;
+    L.bars = o;
+    o += (sizeof(ScoreBars) + 15) & ~15u;
+    for (int s = 0; s < 2; ++s) {
+        L.fixed[s] = o;
+        o += (sizeof(RedFixed) + 15) & ~15u;
+        L.lE[s] = o;
+        o += 4 * nb;
+        L.words[s] = o;
+        o += nb / 8;
+        L.state[s] = o;
+        o += (nb + 15) & ~15;
+    }
+    L.total = o;
+    return L;
+}
 
 // state bits
 constexpr uint8_t kStBound = 1;      // lE holds only an upper bound (block certainly pruned)
@@ -123,7 +146,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Max over the 128 threads of reduction set `set`; slot selects the smem buffer.
-__device__ __forceinline__ float red_max(RedScratch &rs, int set, float v, int slot) {
+__device__ __forceinline__ float red_max(RedFixed &rs, int set, float v, int slot) {
     v = warp_max(v);
     const int w = (threadIdx.x >> 5) & 3;
     if ((threadIdx.x & 31) == 0) rs.red[slot][w] = v;
@@ -131,24 +154,12 @@ __device__ __forceinline__ float red_max(RedScratch &rs, int set, float v, int s
     const float r = fmaxf(fmaxf(rs.red[slot][0], rs.red[slot][1]), fmaxf(rs.red[slot][2], rs.red[slot][3]));
     return r;
 }
-__device__ __forceinline__ float red_sum(RedScratch &rs, int set, float v, int slot) {
+__device__ __forceinline__ float red_sum(RedFixed &rs, int set, float v, int slot) {
     v = warp_sum(v);
     const int w = (threadIdx.x >> 5) & 3;
     if ((threadIdx.x & 31) == 0) rs.red[slot][w] = v;
     red_bar(set);
     return (rs.red[slot][0] + rs.red[slot][1]) + (rs.red[slot][2] + rs.red[slot][3]);
-}
-
-// Element (row r, column c) of a 128x128 tile stored by TMA with 128-byte swizzling.
-template <int kDtype>
-__device__ __forceinline__ float q_elem(const uint8_t *tile, int r, int c) {
-    if (kDtype == FP_DTYPE_BF16) {
-        const int off = (c >> 6) * 16384 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + ((c & 7) << 1);
-        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + off));
-    } else {
-        const int off = r * 128 + (((c >> 4) ^ (r & 7)) << 4) + (c & 15);
-        return float(*reinterpret_cast<const __nv_fp8_e4m3 *>(tile + off));
-    }
 }
 
 template <int kDtype>
@@ -157,11 +168,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     const float *__restrict__ kbar, const float2 *__restrict__ kstat,
                     const ReqInfo *__restrict__ req, int batch, int hkv, int g, int mode, float log_alpha, int sink,
                     int window, float qscale, float kscale, int32_t nseg, int32_t *__restrict__ seg_count,
-                    uint32_t *__restrict__ mask, int32_t *__restrict__ status) {
+                    uint32_t *__restrict__ mask, const uint8_t *__restrict__ qg, int hq, int nst, int nb,
+                    int32_t *__restrict__ status) {
     using C = SCfg<kDtype>;
     extern __shared__ uint8_t smem_raw[];
-    ScoreSmem<kDtype> &sm = *reinterpret_cast<ScoreSmem<kDtype> *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *const base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const SLayout L = score_layout(C::kTile, nst, nb);
+    ScoreBars &sm = *reinterpret_cast<ScoreBars *>(base + L.bars);
+    uint8_t *const qbase = base + L.q, *const kbase = base + L.k;
+    auto qbuf = [=](int set) { return qbase + set * C::kTile; };
+    auto kbuf = [=](int set, int st) { return kbase + (set * nst + st) * C::kTile; };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (status_bad(status)) return;
 
@@ -172,11 +188,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
             for (int b = 0; b < 2; ++b) {
                 mbar_init(&sm.s_full[i][b], 1);
                 mbar_init(&sm.s_empty[i][b], 4);  // one arrival per warp of the set
+                mbar_init(&sm.k_full[i][b], 1);
+                mbar_init(&sm.k_empty[i][b], 1);
             }
-        }
-        for (int i = 0; i < kSStages; ++i) {
-            mbar_init(&sm.k_full[i], 1);
-            mbar_init(&sm.k_empty[i], 1);
         }
         sm.abort = 0;
         fence_barrier_init();
@@ -189,83 +203,86 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const uint32_t tmem = sm.tmem_base;
     const bool scoring = mode == kModeScore;
 
-    if (warp == 0) {
+    if (warp < 4 && (warp & 1) == 0) {
         sregs_set<kSRegsProducer>();
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && scoring) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            uint32_t tile_it = 0, chunk_it = 0;
-            for (int w = blockIdx.x; w < nseg; w += gridDim.x, ++tile_it) {
+        // ------------------------------------------------------------ TMA producers of set warp / 2
+        // lane 0: the set's pooled-key chunks; lane 1: its Q tiles, each as soon as the set's previous tile
+        // is done with the Q buffer (its MMAs complete and its reduction past the Q maximum)
+        const int set = warp >> 1;
+        if (lane < 2 && scoring) {
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_k);
+            }
+            uint32_t tile_it = 0, chunk_it = 0;  // this set's tiles and chunks
+            for (int w = blockIdx.x + set * gridDim.x; w < nseg; w += 2 * gridDim.x, ++tile_it) {
                 const SegCoord sc = decode_seg(req, batch, g, nseg - 1 - w);
-                const ReqInfo r = req[sc.b];
-                const int qb = tile_it & 1;
-                if (!mbar_wait(&sm.q_empty[qb], ((tile_it >> 1) & 1) ^ 1, ab)) break;
-                mbar_arrive_expect_tx(&sm.q_full[qb], C::kTile);
-                // rows before sc.lo (a chunk's first tile) read other tokens or the zero fill; they are masked
-                for (int i = 0; i < C::kBoxes; ++i)
-                    tma_load_4d(sm.q[qb] + i * 16384, &tm_q, &sm.q_full[qb], i * C::kBoxElems, 0, sc.h, sc.q_pos);
+                if (lane == 1) {
+                    if (!mbar_wait(&sm.q_empty[set], (tile_it & 1) ^ 1, ab)) break;
+                    mbar_arrive_expect_tx(&sm.q_full[set], C::kTile);
+                    // rows before sc.lo (a chunk's first tile) read other tokens or the zero fill; they are masked
+                    for (int i = 0; i < C::kBoxes; ++i)
+                        tma_load_4d(qbuf(set) + i * 16384, &tm_q, &sm.q_full[set], i * C::kBoxElems, 0, sc.h,
+                                    sc.q_pos);
+                    continue;
+                }
+                const int blk_base = req[sc.b].blk_base;
                 const int nch = sc.D / 128 + 1;
                 bool ok = true;
                 for (int cc = 0; cc < nch && ok; ++cc, ++chunk_it) {
                     const int c = nch - 1 - cc;
-                    const int st = chunk_it % kSStages;
-                    if (!(ok = mbar_wait(&sm.k_empty[st], ((chunk_it / kSStages) & 1) ^ 1, ab))) break;
-                    mbar_arrive_expect_tx(&sm.k_full[st], C::kTile);
+                    const int st = chunk_it % nst;
+                    if (!(ok = mbar_wait(&sm.k_empty[set][st], ((chunk_it / nst) & 1) ^ 1, ab))) break;
+                    mbar_arrive_expect_tx(&sm.k_full[set][st], C::kTile);
                     for (int i = 0; i < C::kBoxes; ++i)
-                        tma_load_3d(sm.k[st] + i * 16384, &tm_k, &sm.k_full[st], i * C::kBoxElems, sc.h,
-                                    r.blk_base + 128 * c);
+                        tma_load_3d(kbuf(set, st) + i * 16384, &tm_k, &sm.k_full[set][st], i * C::kBoxElems, sc.h,
+                                    blk_base + 128 * c);
                 }
                 if (!ok) break;
             }
         }
-    } else if (warp == 1) {
+    } else if (warp < 4) {
         sregs_set<kSRegsProducer>();
-        // --------------------------------------------------------------- MMA issue
+        // --------------------------------------------------------------- MMA issue of set warp / 2
         // The whole warp runs the loop (descriptors stay warp-uniform) and one elected lane issues:
         // issued from a lone lane, every MMA costs tens of cycles more. Waits end alike in all lanes.
+        const int set = warp >> 1;
         if (scoring) {
             auto wait_w = [&](uint64_t *bar, uint32_t parity) -> bool {
                 return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab));
             };
             uint32_t tile_it = 0, chunk_it = 0;
-            uint32_t set_chunk[2] = {0, 0};  // chunks issued into each set's S buffers
-            for (int w = blockIdx.x; w < nseg; w += gridDim.x, ++tile_it) {
+            for (int w = blockIdx.x + set * gridDim.x; w < nseg; w += 2 * gridDim.x, ++tile_it) {
                 const SegCoord sc = decode_seg(req, batch, g, nseg - 1 - w);
-                const int qb = tile_it & 1;  // = the set that reduces this tile
-                if (!wait_w(&sm.q_full[qb], (tile_it >> 1) & 1)) break;
+                if (!wait_w(&sm.q_full[set], tile_it & 1)) break;
                 const int nch = sc.D / 128 + 1;
                 bool ok = true;
                 for (int cc = 0; cc < nch; ++cc, ++chunk_it) {
-                    const int st = chunk_it % kSStages;
-                    const uint32_t sc_it = set_chunk[qb]++;
-                    const int sb = sc_it & 1;
-                    if (!(ok = wait_w(&sm.k_full[st], (chunk_it / kSStages) & 1))) break;
-                    if (!(ok = wait_w(&sm.s_empty[qb][sb], ((sc_it >> 1) & 1) ^ 1))) break;
+                    const int st = chunk_it % nst, sb = chunk_it & 1;
+                    if (!(ok = wait_w(&sm.k_full[set][st], (chunk_it / nst) & 1))) break;
+                    if (!(ok = wait_w(&sm.s_empty[set][sb], ((chunk_it >> 1) & 1) ^ 1))) break;
                     if (elect_one()) {
                         tc_fence_after();
-                        const uint32_t abase = smem_addr(sm.k[st]), bbase = smem_addr(sm.q[qb]);
+                        const uint32_t abase = smem_addr(kbuf(set, st)), bbase = smem_addr(qbuf(set));
 #pragma unroll
                         for (int k = 0; k < C::kNumK; ++k) {
                             const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
                             const uint64_t ad = sw128_desc(abase + off, 16, 1024);
                             const uint64_t bd = sw128_desc(bbase + off, 16, 1024);
                             if (kDtype == FP_DTYPE_BF16)
-                                umma_f16_ss(tmem + qb * 256 + sb * 128, ad, bd, C::kIdesc, k > 0);
+                                umma_f16_ss(tmem + set * 256 + sb * 128, ad, bd, C::kIdesc, k > 0);
                             else
-                                umma_f8_ss(tmem + qb * 256 + sb * 128, ad, bd, C::kIdesc, k > 0);
+                                umma_f8_ss(tmem + set * 256 + sb * 128, ad, bd, C::kIdesc, k > 0);
                         }
-                        umma_commit(&sm.k_empty[st]);
-                        umma_commit(&sm.s_full[qb][sb]);
-                        if (cc == nch - 1) umma_commit(&sm.q_empty[qb]);
+                        umma_commit(&sm.k_empty[set][st]);
+                        umma_commit(&sm.s_full[set][sb]);
+                        if (cc == nch - 1) umma_commit(&sm.q_empty[set]);
                     }
                     __syncwarp();
                 }
                 if (!ok) break;
             }
         }
-    } else if (warp < 4) {
-        sregs_set<kSRegsProducer>();  // idle
     } else {
         sregs_set<kSRegsReduce>();
         // --------------------------------------------------- reduction / selection
@@ -276,7 +293,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
         // the threshold interval, and any candidate the interval cannot settle sends the tile through the
         // exact fp32 path. Mask words start from the forced blocks (sink, window, diagonal).
         const int set = (warp - 4) >> 2;               // this set takes the CTA's tiles k with k % 2 == set
-        RedScratch &rs = sm.rs[set];
+        // the set's scratch: the fixed part and per-block arrays for the longest request
+        // (selects rather than indexes L, so that L stays in registers)
+        RedFixed &rs = *reinterpret_cast<RedFixed *>(base + (set ? L.fixed[1] : L.fixed[0]));
+        float *const blE = reinterpret_cast<float *>(base + (set ? L.lE[1] : L.lE[0]));  // log-energy, bound or refined
+        uint8_t *const bstate = base + (set ? L.state[1] : L.state[0]);                 // kSt* bits per block
+        uint32_t *const words = reinterpret_cast<uint32_t *>(base + (set ? L.words[1] : L.words[0]));  // tile's mask
         const int rt = (threadIdx.x - 128) & 127;     // 0..127 within the set
         const int j = 32 * (warp & 3) + lane;         // TMEM lane = block in chunk = tile row
         const uint32_t tlane = (static_cast<uint32_t>(32 * (warp & 3)) << 16) + set * 256;
@@ -320,7 +342,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
             const int s_end = min(sink, D + 1), w_lo = max(D - window, 0);
             // mask words of this tile start as the forced set; thread k owns word k
             for (int k = rt; k < r.words; k += kRedThreads)
-                rs.words[k] = range_bits(k, 0, s_end) | range_bits(k, w_lo, D) | range_bits(k, D, D + 1);
+                words[k] = range_bits(k, 0, s_end) | range_bits(k, w_lo, D) | range_bits(k, D, D + 1);
             if (rt == 0) {
                 rs.ncand = 0;
                 rs.nsel = 0;
@@ -338,7 +360,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
                     for (int ch = 0; ch < 128 * SCfg<kDtype>::kEb / 16; ++ch) {
                         const int atom = ch >> 3, c16 = ch & 7;
-                        const uint4 u = *reinterpret_cast<const uint4 *>(sm.q[qb] + atom * 16384 + j * 128 +
+                        const uint4 u = *reinterpret_cast<const uint4 *>(qbuf(qb) + atom * 16384 + j * 128 +
                                                                          ((c16 ^ (j & 7)) << 4));
                         if (kDtype == FP_DTYPE_BF16) {
                             mx = __vmaxu2(mx, __vmaxu2(u.x & 0x7fff7fffu, u.y & 0x7fff7fffu));
@@ -357,6 +379,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     amax = float(*reinterpret_cast<const __nv_fp8_e4m3 *>(&b));
                 }
                 const float qmax = red_max(rs, set, amax, 0) * qscale * sqrtf((float)kHeadDim);
+                // the set is done with the Q tile in shared memory (the rare exact path reads Q from global
+                // memory): once the tile's MMAs are complete too, the next tile's Q may load into the buffer
+                if (rt == 0) mbar_arrive(&sm.q_empty[qb]);
                 // rounding statistics of this thread's block, loaded one chunk ahead
                 float2 ks_next = (128 * (nch - 1) + j <= D) ? __ldg(ks_base + (int64_t)(128 * (nch - 1) + j) * hkv)
                                                             : make_float2(0.f, 0.f);
@@ -417,16 +442,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
                                         ps[x & 3] += ex2((__uint_as_float(v[x >> 5][x & 31]) - m) * k2);
                             }
                             const float lE = ms + log2f((ps[0] + ps[1]) + (ps[2] + ps[3])) * LN2;
-                            rs.lE[J] = lE;
-                            rs.state[J] = 0;
+                            blE[J] = lE;
+                            bstate[J] = 0;
                             mlo = fmaxf(mlo, lE - eps);
                             mhi = fmaxf(mhi, lE + eps);
                             const int slot = atomicAdd(&rs.ncand, 1);
                             if (slot < kCand) rs.cand[slot] = J;
                         } else {
                             // certainly pruned and certainly not the maximum: hi < ln(alpha) + m_run
-                            rs.lE[J] = hi;
-                            rs.state[J] = kStBound;
+                            blE[J] = hi;
+                            bstate[J] = kStBound;
                             mhi = fmaxf(mhi, hi);
                         }
                     }
@@ -463,9 +488,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
                         const int J = rs.cand[i];
                         const bool forced = J < sink || (J >= D - window && J < D) || J == D;
                         if (forced) continue;
-                        const float lE = rs.lE[J];
+                        const float lE = blE[J];
                         if (lE - eps_tile >= thr_hi) {
-                            atomicOr(&rs.words[J >> 5], 1u << (J & 31));
+                            atomicOr(&words[J >> 5], 1u << (J & 31));
                             atomicAdd(&rs.nsel, 1);
                         } else if (lE + eps_tile >= thr_lo) {
                             rs.any2[ap] = 1;
@@ -478,26 +503,47 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 // fp32 recomputation of every unsettled block and every candidate for the maximum
                 for (int J = rt; J <= D; J += kRedThreads) {
                     const bool forced = J < sink || (J >= D - window && J < D) || J == D;
-                    const bool bound = rs.state[J] & kStBound;
-                    const float lo = bound ? -INFINITY : rs.lE[J] - eps_tile;
-                    const float hi = bound ? rs.lE[J] : rs.lE[J] + eps_tile;
+                    const bool bound = bstate[J] & kStBound;
+                    const float lo = bound ? -INFINITY : blE[J] - eps_tile;
+                    const float hi = bound ? blE[J] : blE[J] + eps_tile;
                     uint8_t st = 0;
                     if (forced || lo >= thr_hi) st |= kStSelected;
                     else if (!(hi < thr_lo)) st |= kStUncertain;
                     if (hi >= mlo) st |= kStMaxCand;
-                    rs.state[J] = st;
+                    bstate[J] = st;
                 }
                 float qr[kHeadDim];
+                if (j >= (row_span >> 8) && j < (row_span & 255)) {
+                    // row j of the tile: position q_pos + j / g, query head h g + j % g
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        qg + (((int64_t)(sc.q_pos + j / g) * hq + sc.h * g + j % g) * kHeadDim) * SCfg<kDtype>::kEb);
+                    constexpr int kPer = 16 / SCfg<kDtype>::kEb;
 #pragma unroll
-                for (int c = 0; c < kHeadDim; ++c) qr[c] = j >= (row_span >> 8) && j < (row_span & 255) ? q_elem<kDtype>(sm.q[qb], j, c) * qscale : 0.f;
+                    for (int v = 0; v < kHeadDim / kPer; ++v) {
+                        const uint4 x = __ldg(src + v);
+                        const uint8_t *b = reinterpret_cast<const uint8_t *>(&x);
+#pragma unroll
+                        for (int e = 0; e < kPer; ++e) {
+                            float f;
+                            if (kDtype == FP_DTYPE_BF16)
+                                f = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(b + 2 * e));
+                            else
+                                f = float(*reinterpret_cast<const __nv_fp8_e4m3 *>(b + e));
+                            qr[v * kPer + e] = f * qscale;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kHeadDim; ++c) qr[c] = 0.f;
+                }
                 for (;;) {
                     if (rt == 0) rs.nlist = 0;
                     red_bar(set);
                     // collect up to kRefineList pending candidates, in order
                     for (int J0 = 0; J0 <= D; J0 += kRedThreads) {
                         const int J = J0 + rt;
-                        const bool need = J <= D && (rs.state[J] & (kStUncertain | kStMaxCand)) &&
-                                          !(rs.state[J] & kStRefined);
+                        const bool need = J <= D && (bstate[J] & (kStUncertain | kStMaxCand)) &&
+                                          !(bstate[J] & kStRefined);
                         const unsigned bal = __ballot_sync(0xffffffffu, need);
                         int base = 0;
                         if (lane == 0 && bal) base = atomicAdd(&rs.nlist, __popc(bal));
@@ -528,8 +574,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
                         const float e = j >= (row_span >> 8) && j < (row_span & 255) ? expf(s - mxs) : 0.f;
                         const float sum = red_sum(rs, set, e, 1);
                         if (rt == 0) {
-                            rs.lE[J] = mxs + logf(sum);
-                            rs.state[J] |= kStRefined;
+                            blE[J] = mxs + logf(sum);
+                            bstate[J] |= kStRefined;
                         }
                         red_bar(set);
                     }
@@ -538,19 +584,19 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 // every candidate for the maximum is now exact
                 float mex = -INFINITY;
                 for (int J = rt; J <= D; J += kRedThreads)
-                    if (rs.state[J] & kStMaxCand) mex = fmaxf(mex, rs.lE[J]);
+                    if (bstate[J] & kStMaxCand) mex = fmaxf(mex, blE[J]);
                 mex = red_max(rs, set, mex, 0);
                 const float thr = log_alpha + mex;
                 for (int J = rt; J <= D; J += kRedThreads) {
-                    const uint8_t st = rs.state[J];
-                    if ((st & kStUncertain) && rs.lE[J] >= thr) rs.state[J] = st | kStSelected;
+                    const uint8_t st = bstate[J];
+                    if ((st & kStUncertain) && blE[J] >= thr) bstate[J] = st | kStSelected;
                 }
                 red_bar(set);
                 // rebuild the mask words from the final states
                 int cnt = 0;
                 for (int J0 = 32 * (warp & 3); J0 < 32 * r.words; J0 += kRedThreads) {
                     const int J = J0 + lane;
-                    const bool sel = J <= D && (rs.state[J] & kStSelected);
+                    const bool sel = J <= D && (bstate[J] & kStSelected);
                     const unsigned bits = __ballot_sync(0xffffffffu, sel);
                     if (lane == 0) mask[wbase + (J0 >> 5)] = bits;
                     cnt += __popc(bits);
@@ -562,7 +608,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 // settled by bounds: forced blocks plus the selected candidates
                 if (!scoring) red_bar(set);  // the forced words are complete
                 for (int k = rt; k < r.words; k += kRedThreads) {
-                    uint32_t wv = rs.words[k];
+                    uint32_t wv = words[k];
                     if (mode == kModeAll) wv = range_bits(k, 0, D + 1);
                     mask[wbase + k] = wv;
                 }
@@ -571,7 +617,6 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     seg_count[seg] = mode == kModeAll ? D + 1 : forced_cnt + (scoring ? rs.nsel : 0);
                 }
             }
-            if (scoring && rt == 0) mbar_arrive(&sm.q_empty[qb]);
         }
     }
 
@@ -607,23 +652,32 @@ cudaError_t launch_score(const Ctx &c, const void *q, const float *kbar, const v
         if (!make_tmap(&tm_k, kbar_op, fp8, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
     const int grid = (int)(c.s.nseg < num_sms() ? c.s.nseg : num_sms());
+    // per-block scratch for the longest request; two chunk stages per set when they fit, else one
+    const int nb = ((c.s.max_blocks > 0 ? c.s.max_blocks : 1) + 127) / 128 * 128;
+    const int tile = fp8 ? SCfg<FP_DTYPE_E4M3>::kTile : SCfg<FP_DTYPE_BF16>::kTile;
+    int dev = 0, cap = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&cap, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || cap <= 0)
+        cap = 232448;
+    int nst = 2;
+    if (score_layout(tile, nst, nb).total + 1024 > (uint32_t)cap) nst = 1;
+    const size_t smem = score_layout(tile, nst, nb).total + 1024;
+    if (smem > (size_t)cap) return cudaErrorInvalidConfiguration;
     cudaError_t e;
     if (fp8) {
-        const size_t smem = sizeof(ScoreSmem<FP_DTYPE_E4M3>) + 1024;
         e = cudaFuncSetAttribute(score_tc_kernel<FP_DTYPE_E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
         score_tc_kernel<FP_DTYPE_E4M3><<<grid, kSThreads, smem, c.stream>>>(
             tm_q, tm_k, kbar, c.kstat(), c.req(), c.p.batch, hkv, g, mode, log_alpha, sink, window, c.p.c_q,
-            c.p.c_k, (int32_t)c.s.nseg, c.seg_count(), c.mask(), c.status());
+            c.p.c_k, (int32_t)c.s.nseg, c.seg_count(), c.mask(), (const uint8_t *)q, hq, nst, nb, c.status());
     } else {
-        const size_t smem = sizeof(ScoreSmem<FP_DTYPE_BF16>) + 1024;
         e = cudaFuncSetAttribute(score_tc_kernel<FP_DTYPE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
         score_tc_kernel<FP_DTYPE_BF16><<<grid, kSThreads, smem, c.stream>>>(
             tm_q, tm_k, kbar, c.kstat(), c.req(), c.p.batch, hkv, g, mode, log_alpha, sink, window, 1.f, 1.f,
-            (int32_t)c.s.nseg, c.seg_count(), c.mask(), c.status());
+            (int32_t)c.s.nseg, c.seg_count(), c.mask(), (const uint8_t *)q, hq, nst, nb, c.status());
     }
     return cudaGetLastError();
 }
