@@ -677,9 +677,10 @@ __global__ void __launch_bounds__(kAThreads, 1)
             auto fetch = [&](It &x) -> bool {
                 const int slot = nrec % kRing;
                 if (!wait_w(&sm.rec_full[slot], (nrec / kRing) & 1)) return false;
-                const int J = sm.ring[slot].J;
-                x.tile = sm.ring[slot].tile;
-                x.fl = sm.ring[slot].flags;
+                const int4 hd = *reinterpret_cast<const int4 *>(&sm.ring[slot]);  // J, tile, flags, row0
+                const int J = hd.x;
+                x.tile = hd.y;
+                x.fl = hd.z;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.rec_empty[slot]);
                 x.valid = J != kRecEnd;
@@ -756,13 +757,19 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 // group i + 2: PV(i), then QK^T(i + 2) if that iteration exists. Its inputs other than
                 // P(i) are probed together (the probes' latencies overlap); only a missing one is waited for.
                 const uint32_t i2 = i + 2;
-                bool ready = mbar_test(&sm.v_full[i % kVStages], (i / kVStages) & 1);
-                if (a.fl & 1) ready &= mbar_test(&sm.o_empty, (a.tile & 1) ^ 1);
-                if (c.valid) {
-                    ready &= mbar_test(&sm.k_full[i2 % kKStages], (i2 / kKStages) & 1);
-                    if (c.fl & 1)
-                        ready &= mbar_test(&sm.q_full, c.tile & 1) &
-                                 mbar_test(&sm.qk_done[c.tile & 1], ((c.tile >> 1) & 1) ^ 1);
+                bool ready;
+                {
+                    // V(i); O free for a tile's first PV; K(i + 2); Q and its TMEM buffer for a new tile
+                    const uint32_t bv = smem_addr(&sm.v_full[i % kVStages]), pv = (i / kVStages) & 1;
+                    const bool nt = c.valid && (c.fl & 1);
+                    ready = mbar_test5(bv, pv,                                                       //
+                                       (a.fl & 1) ? smem_addr(&sm.o_empty) : bv,                     //
+                                       (a.fl & 1) ? ((a.tile & 1) ^ 1) : pv,                         //
+                                       c.valid ? smem_addr(&sm.k_full[i2 % kKStages]) : bv,          //
+                                       c.valid ? (i2 / kKStages) & 1 : pv,                           //
+                                       nt ? smem_addr(&sm.q_full) : bv, nt ? (c.tile & 1) : pv,      //
+                                       nt ? smem_addr(&sm.qk_done[c.tile & 1]) : bv,                 //
+                                       nt ? ((c.tile >> 1) & 1) ^ 1 : pv);
                 }
                 if (!__all_sync(0xffffffffu, ready)) {
                     if (c.valid && !(ok = qk_ready(i2, c))) break;

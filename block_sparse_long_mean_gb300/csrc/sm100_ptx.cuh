@@ -87,6 +87,28 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Five non-blocking probes issued back to back (their latencies overlap), combined by AND. A probe
+// that is not wanted repeats another one.
+__device__ __forceinline__ bool mbar_test5(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2,
+                                           uint32_t p2, uint32_t b3, uint32_t p3, uint32_t b4, uint32_t p4) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred q0, q1, q2, q3, q4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q3, [%7], %8;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q4, [%9], %10;\n\t"
+        "and.pred q0, q0, q1;\n\t"
+        "and.pred q2, q2, q3;\n\t"
+        "and.pred q0, q0, q4;\n\t"
+        "and.pred q0, q0, q2;\n\t"
+        "selp.u32 %0, 1, 0, q0;\n\t}"
+        : "=r"(ok)
+        : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2), "r"(b3), "r"(p3), "r"(b4), "r"(p4)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
