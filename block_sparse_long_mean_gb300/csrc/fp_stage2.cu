@@ -960,23 +960,49 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 // four e4m3 per column: column 2k + c4 / 2 holds keys 8k + 4 (c4 / 2) .. + 3, of row ra for an
                 // even c4 (own pair + the odd neighbour's) and of row rb for an odd c4 (.16x64b layout)
                 uint32_t pw[16];
+                // the pair exchange moves two columns per shuffle; byte selectors for own/partner halves
+                const bool odd = c4 & 1;
+                const uint32_t sel_lo = odd ? 0x1054u : 0x5410u, sel_hi = odd ? 0x3276u : 0x7632u;
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sv[h][4 * k]), sl2, offa));
-                        const float p1 = ex2(fmaf(__uint_as_float(sv[h][4 * k + 1]), sl2, offa));
-                        const float p2 = ex2(fmaf(__uint_as_float(sv[h][4 * k + 2]), sl2, offb));
-                        const float p3 = ex2(fmaf(__uint_as_float(sv[h][4 * k + 3]), sl2, offb));
-                        const __nv_fp8x2_e4m3 qa(make_float2(p0, p1)), qb(make_float2(p2, p3));
-                        const float2 fa2 = float2(qa), fb2 = float2(qb);  // Eq.15: the sum uses the quantised values
+                    for (int k4 = 0; k4 < 2; ++k4) {
+                        uint32_t ua[4], ub[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int k = 4 * k4 + j;
+                            float y0, y1, y2, y3;
+                            f2unpack(ffma2(f2pack(__uint_as_float(sv[h][4 * k]), __uint_as_float(sv[h][4 * k + 1])), sl2x2,
+                                           offa2),
+                                     y0, y1);
+                            f2unpack(ffma2(f2pack(__uint_as_float(sv[h][4 * k + 2]), __uint_as_float(sv[h][4 * k + 3])),
+                                           sl2x2, offb2),
+                                     y2, y3);
+                            const __nv_fp8x2_e4m3 qa(make_float2(ex2(y0), ex2(y1))), qb(make_float2(ex2(y2), ex2(y3)));
+                            ua[j] = qa.__x;
+                            ub[j] = qb.__x;
+                        }
+                        // Eq.15: the sum uses the quantised values; four of them (E4M3 -> f16 is exact) are summed
+                        // in f16 (exact unless their exponents lie more than 7 apart), then in fp32
+                        __half2 sa = __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ua[0], __NV_E4M3)),
+                                             __half2(__nv_cvt_fp8x2_to_halfraw2(ua[1], __NV_E4M3)));
+                        __half2 sb = __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ub[0], __NV_E4M3)),
+                                             __half2(__nv_cvt_fp8x2_to_halfraw2(ub[1], __NV_E4M3)));
+                        sa = __hadd2(sa, __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ua[2], __NV_E4M3)),
+                                                 __half2(__nv_cvt_fp8x2_to_halfraw2(ua[3], __NV_E4M3))));
+                        sb = __hadd2(sb, __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ub[2], __NV_E4M3)),
+                                                 __half2(__nv_cvt_fp8x2_to_halfraw2(ub[3], __NV_E4M3))));
+                        const float2 fa2 = __half22float2(sa), fb2 = __half22float2(sb);
                         acca = fadd2(acca, f2pack(fa2.x, fa2.y));
                         accb = fadd2(accb, f2pack(fb2.x, fb2.y));
-                        const uint32_t ua = *reinterpret_cast<const uint16_t *>(&qa);
-                        const uint32_t ub = *reinterpret_cast<const uint16_t *>(&qb);
-                        const uint32_t give = (c4 & 1) ? ua : ub;
-                        const uint32_t got = __shfl_xor_sync(0xffffffffu, give, 1);
-                        pw[8 * h + k] = (c4 & 1) ? (got | (ub << 16)) : (ua | (got << 16));
+#pragma unroll
+                        for (int j = 0; j < 4; j += 2) {
+                            const uint32_t A = ua[j] | (ua[j + 1] << 16), B = ub[j] | (ub[j + 1] << 16);
+                            const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? A : B, 1);
+                            const uint32_t own = odd ? B : A;
+                            pw[8 * h + 4 * k4 + j] = __byte_perm(own, got, sel_lo);
+                            pw[8 * h + 4 * k4 + j + 1] = __byte_perm(own, got, sel_hi);
+                        }
                     }
                 tmem_st_16x64b_x16(tS, pw);
             }
