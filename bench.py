@@ -45,8 +45,8 @@ def kernels_per_step(nseg: int) -> int:
 
 # DRAM bytes (read + write) of one attention-kernel launch on this workload, from one ncu capture
 # (profiles/attn_tc_qwen30b_128k.md), valid while the kernel's sources are those the capture ran.
-ATTN_TRAFFIC = {"workload": "qwen30b_128k", "bytes": 1.361433e9 + 1.029945e9,
-                "sources_sha256": "b66c592fca65c860178a6b60ff576beeddf04953747b7e173bf6d94f1e96a506"}
+ATTN_TRAFFIC = {"workload": "qwen30b_128k", "bytes": 1.362735e9 + 1.029140e9,
+                "sources_sha256": "9ec1379571af6e930303562307057c612f48208472448c66891ac42809ccfadb"}
 
 
 def attn_traffic(workload: str):

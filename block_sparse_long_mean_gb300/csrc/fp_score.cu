@@ -353,32 +353,46 @@ __global__ void __launch_bounds__(kSThreads, 1)
             float m_run = -INFINITY;                 // proven lower bound of max_J lE_J
             if (scoring) {
                 if (!(ok = mbar_wait(&sm.q_full[qb], (tile_it >> 1) & 1, ab))) break;
-                // |q_r|_2 <= sqrt(d) max_i |q_ri|: the largest element magnitude of this thread's row,
-                // an integer maximum over the magnitude bits of the 16-byte chunks of the swizzled tile
-                uint32_t mx = 0;
+                // a bound of |q_r|_2 over the tile's rows. BF16: sqrt(d) max_i |q_ri|, the largest element
+                // magnitude of this thread's row (an integer maximum over the magnitude bits of the 16-byte chunks
+                // of the swizzled tile). E4M3, whose operand-format means round coarsely and so weigh the bound
+                // more: the row's own norm, from the squares of its elements (exact products of the exactly
+                // widened values, summed in fp32), raised by 2^-12 to cover the rounding of the sum and the root.
+                float qbound = 0.f;
                 if (j >= (row_span >> 8) && j < (row_span & 255)) {
+                    if (kDtype == FP_DTYPE_BF16) {
+                        uint32_t mx = 0;
 #pragma unroll
-                    for (int ch = 0; ch < 128 * SCfg<kDtype>::kEb / 16; ++ch) {
-                        const int atom = ch >> 3, c16 = ch & 7;
-                        const uint4 u = *reinterpret_cast<const uint4 *>(qbuf(qb) + atom * 16384 + j * 128 +
-                                                                         ((c16 ^ (j & 7)) << 4));
-                        if (kDtype == FP_DTYPE_BF16) {
+                        for (int ch = 0; ch < 16; ++ch) {
+                            const int atom = ch >> 3, c16 = ch & 7;
+                            const uint4 u = *reinterpret_cast<const uint4 *>(qbuf(qb) + atom * 16384 + j * 128 +
+                                                                             ((c16 ^ (j & 7)) << 4));
                             mx = __vmaxu2(mx, __vmaxu2(u.x & 0x7fff7fffu, u.y & 0x7fff7fffu));
                             mx = __vmaxu2(mx, __vmaxu2(u.z & 0x7fff7fffu, u.w & 0x7fff7fffu));
-                        } else {
-                            mx = __vmaxu4(mx, __vmaxu4(u.x & 0x7f7f7f7fu, u.y & 0x7f7f7f7fu));
-                            mx = __vmaxu4(mx, __vmaxu4(u.z & 0x7f7f7f7fu, u.w & 0x7f7f7f7fu));
                         }
+                        qbound = __uint_as_float(max(mx & 0xffffu, mx >> 16) << 16) * sqrtf((float)kHeadDim);
+                    } else {
+                        uint64_t ss2 = f2pack(0.f, 0.f);
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const uint4 u = *reinterpret_cast<const uint4 *>(qbuf(qb) + j * 128 + ((ch ^ (j & 7)) << 4));
+                            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                                for (int hh = 0; hh < 2; ++hh) {
+                                    const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(
+                                        (__nv_fp8x2_storage_t)(uw[q] >> (16 * hh)), __NV_E4M3)));
+                                    const uint64_t x2 = f2pack(f.x, f.y);
+                                    ss2 = ffma2(x2, x2, ss2);
+                                }
+                        }
+                        float s0, s1;
+                        f2unpack(ss2, s0, s1);
+                        qbound = sqrtf(s0 + s1) * 1.000244140625f;
                     }
                 }
-                float amax;
-                if (kDtype == FP_DTYPE_BF16) {
-                    amax = __uint_as_float(max(mx & 0xffffu, mx >> 16) << 16);
-                } else {
-                    const uint32_t b = max(max(mx & 0xffu, (mx >> 8) & 0xffu), max((mx >> 16) & 0xffu, mx >> 24));
-                    amax = float(*reinterpret_cast<const __nv_fp8_e4m3 *>(&b));
-                }
-                const float qmax = red_max(rs, set, amax, 0) * qscale * sqrtf((float)kHeadDim);
+                const float qmax = red_max(rs, set, qbound, 0) * qscale;  // bounds |q_r|_2 (real units), every row
                 // the set is done with the Q tile in shared memory (the rare exact path reads Q from global
                 // memory): once the tile's MMAs are complete too, the next tile's Q may load into the buffer
                 if (rt == 0) mbar_arrive(&sm.q_empty[qb]);
