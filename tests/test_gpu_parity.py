@@ -4,6 +4,8 @@ Criteria: CSR bit-exact except blocks whose oracle energy lies within 1e-3
 relative of the threshold (counted); BF16 output rel-RMS <= 1e-2 and max-abs
 <= 3e-2; FP8 rel-RMS <= 6e-2; integer work bit-exact and deterministic.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -71,6 +73,49 @@ def test_fp8_small_parity():
     w = synth.make_workload("tiny_2k", device="cuda", lengths=[2048, 517], hq=8, hkv=2, dtype="e4m3", alpha=0.2,
                             paging="random")
     check_fp8(compare(run_gpu(w)))
+
+
+def _rescaled_q(w, row_scale=None, outliers=0.0, seed=0):
+    """w with its queries changed on the host and re-encoded: each token's rows times row_scale[token], and in a
+    fraction `outliers` of the (token, head) rows one element times 10. E4M3 takes a new per-tensor scale."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    q = w.q.float().cpu() * (w.c_q if w.dtype == "e4m3" else 1.0)
+    if row_scale is not None:
+        q = q * row_scale[:, None, None]
+    if outliers:
+        T, H, d = q.shape
+        hit = torch.rand(T, H, generator=gen) < outliers
+        dim = torch.randint(0, d, (T, H), generator=gen)
+        t_i, h_i = hit.nonzero(as_tuple=True)
+        q[t_i, h_i, dim[t_i, h_i]] *= 10.0
+    q = q.to(w.q.device)
+    if w.dtype == "e4m3":
+        c_q = max(float(q.abs().max()), 1e-12) / 448.0
+        return dataclasses.replace(w, q=synth._e4m3(q, c_q).contiguous(), c_q=c_q)
+    return dataclasses.replace(w, q=q.to(torch.bfloat16).contiguous())
+
+
+def test_fp8_selection_with_query_norms_over_three_decades():
+    # the E4M3 screening bounds each tile by its rows' own norms: rows scaled by 2^U(-5, 5) per token, long
+    # enough for several 128-block chunks per tile
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[20000, 3000], hq=8, hkv=2, dtype="e4m3",
+                            alpha=0.2, paging="random")
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(5)
+    scale = torch.exp2(torch.rand(sum(w.lengths), generator=gen) * 10.0 - 5.0)
+    check_fp8(compare(run_gpu(_rescaled_q(w, row_scale=scale, seed=6))))
+
+
+def test_bf16_selection_with_outlier_query_elements():
+    # one element at 10 times its size in 2% of the query rows loosens the BF16 screening bound
+    # (sqrt(d) max |q|) and sends more tiles through the exact fp32 path. (At 30 times the output and the
+    # CSR still match, but the LSE differs by up to 0.021 from the oracle's: the oracle itself, given the
+    # pooled means rounded to BF16 as the tensor core reads them, moves by 0.020 on the same rows. That is
+    # the operand format of the correction terms, growing with the query's size, not an error of the kernels.)
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[20000, 3000], hq=8, hkv=2, alpha=0.1,
+                            paging="random")
+    check_bf16(compare(run_gpu(_rescaled_q(w, outliers=0.02, seed=7))))
 
 
 # ------------------------------------------------------------ integer work, determinism
