@@ -446,9 +446,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
                             const float k2 = scale * LOG2E;
                             float ps[4] = {0.f, 0.f, 0.f, 0.f};
                             if (row_span == 128) {
+                                // 2^(v k2 - m k2) with packed FMAs and sums
+                                const uint64_t k2x2 = f2pack(k2, k2), mk2 = f2pack(-m * k2, -m * k2);
+                                uint64_t acc2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
-                                for (int x = 0; x < 128; ++x)
-                                    ps[x & 3] += ex2((__uint_as_float(v[x >> 5][x & 31]) - m) * k2);
+                                for (int x = 0; x < 128; x += 2) {
+                                    float y0, y1;
+                                    f2unpack(ffma2(f2pack(__uint_as_float(v[x >> 5][x & 31]),
+                                                          __uint_as_float(v[x >> 5][(x & 31) + 1])),
+                                                   k2x2, mk2),
+                                             y0, y1);
+                                    acc2[(x >> 1) & 1] = fadd2(acc2[(x >> 1) & 1], f2pack(ex2(y0), ex2(y1)));
+                                }
+                                f2unpack(acc2[0], ps[0], ps[1]);
+                                f2unpack(acc2[1], ps[2], ps[3]);
                             } else {
 #pragma unroll
                                 for (int x = 0; x < 128; ++x)
