@@ -130,6 +130,43 @@ __device__ __forceinline__ void sregs_set() {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
+// tcgen05.ld of 128 columns (.32x32b.x128) that also returns the largest of the 128 values this thread loads
+// (.red.max, sm_103a); r[q][i] is column 32 q + i. Like the loaded registers, the maximum is valid once
+// tcgen05.wait::ld has returned.
+__device__ __forceinline__ void tmem_ld128_max(uint32_t taddr, uint32_t (&r)[4][32], float &mx) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x128.max.f32 "
+        "{"
+        "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, "
+        "%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, "
+        "%80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, "
+        "%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, "
+        "%112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127"
+        "}, %128, [%129];"
+        : "=r"(r[0][0]), "=r"(r[0][1]), "=r"(r[0][2]), "=r"(r[0][3]), "=r"(r[0][4]), "=r"(r[0][5]), "=r"(r[0][6]), "=r"(r[0][7]),
+          "=r"(r[0][8]), "=r"(r[0][9]), "=r"(r[0][10]), "=r"(r[0][11]), "=r"(r[0][12]), "=r"(r[0][13]), "=r"(r[0][14]), "=r"(r[0][15]),
+          "=r"(r[0][16]), "=r"(r[0][17]), "=r"(r[0][18]), "=r"(r[0][19]), "=r"(r[0][20]), "=r"(r[0][21]), "=r"(r[0][22]), "=r"(r[0][23]),
+          "=r"(r[0][24]), "=r"(r[0][25]), "=r"(r[0][26]), "=r"(r[0][27]), "=r"(r[0][28]), "=r"(r[0][29]), "=r"(r[0][30]), "=r"(r[0][31]),
+          "=r"(r[1][0]), "=r"(r[1][1]), "=r"(r[1][2]), "=r"(r[1][3]), "=r"(r[1][4]), "=r"(r[1][5]), "=r"(r[1][6]), "=r"(r[1][7]),
+          "=r"(r[1][8]), "=r"(r[1][9]), "=r"(r[1][10]), "=r"(r[1][11]), "=r"(r[1][12]), "=r"(r[1][13]), "=r"(r[1][14]), "=r"(r[1][15]),
+          "=r"(r[1][16]), "=r"(r[1][17]), "=r"(r[1][18]), "=r"(r[1][19]), "=r"(r[1][20]), "=r"(r[1][21]), "=r"(r[1][22]), "=r"(r[1][23]),
+          "=r"(r[1][24]), "=r"(r[1][25]), "=r"(r[1][26]), "=r"(r[1][27]), "=r"(r[1][28]), "=r"(r[1][29]), "=r"(r[1][30]), "=r"(r[1][31]),
+          "=r"(r[2][0]), "=r"(r[2][1]), "=r"(r[2][2]), "=r"(r[2][3]), "=r"(r[2][4]), "=r"(r[2][5]), "=r"(r[2][6]), "=r"(r[2][7]),
+          "=r"(r[2][8]), "=r"(r[2][9]), "=r"(r[2][10]), "=r"(r[2][11]), "=r"(r[2][12]), "=r"(r[2][13]), "=r"(r[2][14]), "=r"(r[2][15]),
+          "=r"(r[2][16]), "=r"(r[2][17]), "=r"(r[2][18]), "=r"(r[2][19]), "=r"(r[2][20]), "=r"(r[2][21]), "=r"(r[2][22]), "=r"(r[2][23]),
+          "=r"(r[2][24]), "=r"(r[2][25]), "=r"(r[2][26]), "=r"(r[2][27]), "=r"(r[2][28]), "=r"(r[2][29]), "=r"(r[2][30]), "=r"(r[2][31]),
+          "=r"(r[3][0]), "=r"(r[3][1]), "=r"(r[3][2]), "=r"(r[3][3]), "=r"(r[3][4]), "=r"(r[3][5]), "=r"(r[3][6]), "=r"(r[3][7]),
+          "=r"(r[3][8]), "=r"(r[3][9]), "=r"(r[3][10]), "=r"(r[3][11]), "=r"(r[3][12]), "=r"(r[3][13]), "=r"(r[3][14]), "=r"(r[3][15]),
+          "=r"(r[3][16]), "=r"(r[3][17]), "=r"(r[3][18]), "=r"(r[3][19]), "=r"(r[3][20]), "=r"(r[3][21]), "=r"(r[3][22]), "=r"(r[3][23]),
+          "=r"(r[3][24]), "=r"(r[3][25]), "=r"(r[3][26]), "=r"(r[3][27]), "=r"(r[3][28]), "=r"(r[3][29]), "=r"(r[3][30]), "=r"(r[3][31]),
+          "=f"(mx)
+        : "r"(taddr)
+        : "memory");
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -409,30 +446,32 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     if (!(ok = mbar_wait(&sm.s_full[set][sb], (chunk_it >> 1) & 1, ab))) break;
                     tc_fence_after();
                     uint32_t v[4][32];
+                    float m = -INFINITY;  // full tiles: the block's maximum, taken by the load itself
+                    if (row_span == 128) {
+                        tmem_ld128_max(tmem + tlane + sb * 128, v, m);
+                    } else {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tmem + tlane + sb * 128 + q4 * 32, v[q4]);
+                        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tmem + tlane + sb * 128 + q4 * 32, v[q4]);
+                    }
                     tmem_ld_wait();
+                    asm volatile("" : "+f"(m));
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) reg_fence32(v[q4]);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sm.s_empty[set][sb]);
-                    float pm[8];
+                    if (row_span != 128) {
+                        // a partial tile: only the rows [lo, rows) count
+                        float pm[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-                    if (row_span == 128) {
-#pragma unroll
-                        for (int x = 0; x < 128; x += 2)
-                            pm[(x >> 1) & 7] = fmax3(pm[(x >> 1) & 7], __uint_as_float(v[x >> 5][x & 31]),
-                                                     __uint_as_float(v[x >> 5][(x & 31) + 1]));
-                    } else {
+                        for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
 #pragma unroll
                         for (int x = 0; x < 128; ++x)
                             pm[x & 7] = fmaxf(pm[x & 7], x >= (row_span >> 8) && x < (row_span & 255)
                                                              ? __uint_as_float(v[x >> 5][x & 31]) : -INFINITY);
+                        m = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                  fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
                     }
-                    const float m = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                          fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
                     const float eps = valid ? qmax * (ks.x + 2.44140625e-4f * ks.y) * inv_sqrt_d + 2e-4f : 0.f;
                     const float ms = m * scale;
                     // the first chunk holds the diagonal block (usually the maximum): one block-wide max of the
