@@ -485,7 +485,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
                             const float k2 = scale * LOG2E;
                             float ps[4] = {0.f, 0.f, 0.f, 0.f};
                             if (row_span == 128) {
-                                // 2^(v k2 - m k2) with packed FMAs and sums
+                                // 2^(v k2 - m k2) with packed FMAs and sums; the rounding of m k2 (|logit| 2^-24)
+                                // lies far inside the bound's relative term (2^-12 |q||kbar| >= 2^-12 |logit|)
                                 const uint64_t k2x2 = f2pack(k2, k2), mk2 = f2pack(-m * k2, -m * k2);
                                 uint64_t acc2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
