@@ -23,6 +23,7 @@ from .build import build as _build_lib, LIB_PATH
 
 ORC_CORRECTION = 1
 ORC_DENSE = 2
+ORC_EQ15 = 4
 
 
 class _Problem(ctypes.Structure):
@@ -52,6 +53,7 @@ def lib():
         L.orc_decode_bf16.argtypes = [ctypes.c_uint16]
         L.orc_decode_e4m3.restype = ctypes.c_double
         L.orc_decode_e4m3.argtypes = [ctypes.c_uint8]
+        L.orc_round_e4m3_n.argtypes = [vp, vp, ctypes.c_int64]
         L.orc_validate.argtypes = [P]
         L.orc_pool.argtypes = [P, ctypes.c_int, ctypes.c_int, vp, vp, vp]
         L.orc_pool_all.argtypes = [P, vp, vp, vp, vp]
@@ -81,6 +83,14 @@ def _raw(x) -> np.ndarray:
     if x.dtype == torch.float8_e4m3fn:
         return x.view(torch.uint8).numpy()
     raise TypeError(f"unsupported element type {x.dtype}")
+
+
+def round_e4m3(x) -> np.ndarray:
+    """The E4M3 values nearest to x (ties to even, saturating at +-448), elementwise."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    y = np.empty_like(x)
+    lib().orc_round_e4m3_n(_ptr(x), _ptr(y), x.size)
+    return y
 
 
 @dataclasses.dataclass
@@ -318,8 +328,12 @@ def tiles64_from_csr(p: Problem, seg: Segments, cu: np.ndarray, idx: np.ndarray)
 
 def attend(p: Problem, sel_full: np.ndarray, correction: bool = True, dense: bool = False,
            seg: Optional[Segments] = None, pooled: Optional[Pooled] = None, seg_ids: Optional[Sequence[int]] = None,
-           nthreads: Optional[int] = None):
+           nthreads: Optional[int] = None, eq15: bool = False):
     """Mean-corrected block-sparse attention (Eq.6; Eq.4 without correction) of the listed segments.
+
+    eq15 (E4M3 problems only): the online softmax of [V2] Sec.3.3 "FP8 Execution", Eq.15, with its probabilities
+    quantised to E4M3 against the running row maximum, over the iterations of Eq.17 (selected blocks descending,
+    then chunks of 128 correction means descending), the means in E4M3 operand format.
 
     Returns (O [n, tile_rows, d], lse [n, tile_rows]) for the n listed segments."""
     seg = seg or segments(p)
@@ -327,7 +341,7 @@ def attend(p: Problem, sel_full: np.ndarray, correction: bool = True, dense: boo
     ids = np.arange(len(seg), dtype=np.int64) if seg_ids is None else np.asarray(seg_ids, dtype=np.int64)
     O = np.zeros((len(ids), p.tile_rows, p.d))
     lse = np.zeros((len(ids), p.tile_rows))
-    flags = (ORC_CORRECTION if correction else 0) | (ORC_DENSE if dense else 0)
+    flags = (ORC_CORRECTION if correction else 0) | (ORC_DENSE if dense else 0) | (ORC_EQ15 if eq15 else 0)
     s = p.c_struct()
     sel_full = np.ascontiguousarray(sel_full, dtype=np.uint8)
     rc = lib().orc_run_segments(ctypes.byref(s), _ptr(ids), len(ids), _ptr(seg.b), _ptr(seg.h), _ptr(seg.t),
@@ -360,14 +374,14 @@ def tile_rows_to_tokens(p: Problem, seg: Segments, seg_ids: Sequence[int], O_til
 
 
 def run(p: Problem, alpha: float, sink: int, window: int, correction: bool = True, dense: bool = False,
-        nthreads: Optional[int] = None):
-    """The whole layer: returns dict(cu, idx, sel, O [T,hq,d], lse [T,hq], pooled, seg)."""
+        nthreads: Optional[int] = None, eq15: bool = False):
+    """The whole layer: returns dict(cu, idx, sel, O [T,hq,d], lse [T,hq], pooled, seg); eq15 as in attend."""
     seg = segments(p)
     pooled = pool(p, seg)
     selection = select(p, alpha, sink, window, seg=seg, pooled=pooled, nthreads=nthreads)
     cu, idx = csr_from_selection(seg, selection)
     ids = np.arange(len(seg))
     Ot, lt = attend(p, selection.sel_full, correction=correction, dense=dense, seg=seg, pooled=pooled,
-                    nthreads=nthreads)
+                    nthreads=nthreads, eq15=eq15)
     O, lse = tile_rows_to_tokens(p, seg, ids, Ot, lt)
     return dict(cu=cu, idx=idx, selection=selection, O=O, lse=lse, pooled=pooled, seg=seg)

@@ -83,6 +83,27 @@ double orc_decode_e4m3(uint8_t x) {
     return sign ? -v : v;
 }
 
+/* The E4M3 value nearest to x, ties to even, saturating at +-448 (the same
+ * format: 3 mantissa bits, so within the binade [2^e, 2^(e+1)) the spacing is
+ * 2^(e-3); below 2^-6 the subnormal spacing 2^-9 continues the lowest binade's).
+ * The division by the spacing is exact, and nearbyint rounds ties to even in
+ * the default rounding mode. */
+double orc_round_e4m3(double x) {
+    double a = fabs(x);
+    if (a == 0.0 || isnan(x)) return x;
+    int e;
+    frexp(a, &e); /* a = f 2^e with f in [0.5, 1): a lies in [2^(e-1), 2^e) */
+    int lo = e - 1 < -6 ? -6 : e - 1;
+    double spacing = ldexp(1.0, lo - 3);
+    double r = nearbyint(a / spacing) * spacing;
+    if (r > 448.0) r = 448.0;
+    return copysign(r, x);
+}
+
+void orc_round_e4m3_n(const double *x, double *y, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) y[i] = orc_round_e4m3(x[i]);
+}
+
 static double elem(const orc_problem *p, const void *base, size_t i, double scale) {
     if (p->dtype == 0) return orc_decode_bf16(((const uint16_t *)base)[i]);
     return scale * orc_decode_e4m3(((const uint8_t *)base)[i]);
@@ -273,6 +294,122 @@ int orc_select(const double *E, int D, double alpha, int sink, int window, uint8
 
 #define ORC_CORRECTION 1 /* add mean-correction terms for pruned blocks */
 #define ORC_DENSE 2      /* ignore `sel`: every causal block is exact */
+#define ORC_EQ15 4       /* E4M3 problems: quantised probabilities of Eq.15 (below) */
+
+/* [V2] Sec.3.3 "FP8 Execution", Eq.15, taken literally: the online softmax
+ * runs over the iterations of Eq.17 (the selected blocks J = D .. 0 in
+ * descending order, each one iteration; then, by Alg.1 step 9, the correction
+ * terms appended as chunks of 128 consecutive blocks, chunk c covering blocks
+ * 128c .. 128c + 127, in descending order). m is the running row maximum after
+ * each iteration; when it grows, the running numerator and denominator are
+ * multiplied by e^{m_old - m}; then every term of the iteration adds
+ * P~ = e4m3(2^8 e^{s - m}) to the denominator and P~ v to the numerator. The
+ * 2^8 offset leaves O unchanged and is taken out of the LSE. The means enter
+ * as the tensor cores read them (reading of the design notes): the mean of
+ * the block's E4M3 codes, kbar / c_k (exactly: sums of E4M3 values are exact
+ * in fp64, and a full block divides by 128), rounded to E4M3, times c_k; the
+ * same for the values with c_v. */
+static void eq15_step(const double *s, const double *const *v, int n, int d, double *m, double *l, double *o) {
+    double mi = *m;
+    for (int i = 0; i < n; ++i)
+        if (s[i] > mi) mi = s[i];
+    if (mi > *m) {
+        double f = *m == -INFINITY ? 0.0 : exp(*m - mi);
+        *l *= f;
+        for (int c = 0; c < d; ++c) o[c] *= f;
+        *m = mi;
+    }
+    for (int i = 0; i < n; ++i) {
+        double w = orc_round_e4m3(256.0 * exp(s[i] - *m));
+        *l += w;
+        for (int c = 0; c < d; ++c) o[c] += w * v[i][c];
+    }
+}
+
+static int attend_tile_eq15(const orc_problem *p, const int32_t *cnt, int b, int h, int t, const uint8_t *sel,
+                            int flags, double *O, double *lse) {
+    int g = group(p), d = p->d, B = p->block, L = kv_len(p, b);
+    long r0, r1;
+    tile_rows(p, b, t, &r0, &r1);
+    long row_base = (first_tile(p, b) + t) * p->tile_rows;
+    int D = orc_tile_diag(p, b, t);
+    double inv_sqrt_d = 1.0 / sqrt((double)d);
+    /* one iteration holds at most B keys or B means */
+    double *s = (double *)malloc(sizeof(double) * (size_t)B);
+    const double **v = (const double **)malloc(sizeof(double *) * (size_t)B);
+    double *vals = (double *)malloc(sizeof(double) * (size_t)B * d);   /* values of exact keys */
+    double *kop = (double *)malloc(sizeof(double) * (size_t)(D + 1) * d); /* operand-format means */
+    double *vop = (double *)malloc(sizeof(double) * (size_t)(D + 1) * d);
+    double *q = (double *)malloc(sizeof(double) * (size_t)d);
+    int rc = ORC_OK;
+    if (!s || !v || !vals || !kop || !vop || !q) {
+        rc = ORC_ENOMEM;
+        goto done;
+    }
+    for (int J = 0; J < D; ++J) { /* the correction blocks are full and lie below the diagonal */
+        if (sel[J] || !(flags & ORC_CORRECTION) || (flags & ORC_DENSE)) continue;
+        double *kj = kop + (size_t)J * d, *vj = vop + (size_t)J * d;
+        for (int c = 0; c < d; ++c) kj[c] = vj[c] = 0.0;
+        for (int j = J * B; j < (J + 1) * B; ++j) {
+            size_t ko = kv_offset(p, b, j, h);
+            for (int c = 0; c < d; ++c) {
+                kj[c] += elem(p, p->k_pages, ko + c, 1.0);
+                vj[c] += elem(p, p->v_pages, ko + c, 1.0);
+            }
+        }
+        for (int c = 0; c < d; ++c) {
+            kj[c] = p->c_k * orc_round_e4m3(kj[c] / cnt[J]);
+            vj[c] = p->c_v * orc_round_e4m3(vj[c] / cnt[J]);
+        }
+    }
+    memset(O, 0, sizeof(double) * (size_t)p->tile_rows * d);
+    for (int i = 0; i < p->tile_rows; ++i) lse[i] = 0.0;
+    for (long r = r0; r < r1; ++r) {
+        long pos = r / g;
+        size_t qo = q_offset(p, b, r, h);
+        for (int c = 0; c < d; ++c) q[c] = elem(p, p->q, qo + c, p->c_q);
+        double m = -INFINITY, l = 0.0;
+        double *o = O + (size_t)(r - row_base) * d;
+        for (int J = D; J >= 0; --J) {
+            if (!((flags & ORC_DENSE) || sel[J])) continue;
+            int n = 0;
+            int jend = (J + 1) * B < L ? (J + 1) * B : L;
+            for (int j = J * B; j < jend && j <= pos; ++j, ++n) {
+                size_t ko = kv_offset(p, b, j, h);
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c) acc += q[c] * elem(p, p->k_pages, ko + c, p->c_k);
+                s[n] = acc * inv_sqrt_d;
+                for (int c = 0; c < d; ++c) vals[(size_t)n * d + c] = elem(p, p->v_pages, ko + c, p->c_v);
+                v[n] = vals + (size_t)n * d;
+            }
+            eq15_step(s, v, n, d, &m, &l, o);
+        }
+        if ((flags & ORC_CORRECTION) && !(flags & ORC_DENSE) && D > 0) {
+            for (int ch = (D - 1) / B; ch >= 0; --ch) {
+                int n = 0;
+                for (int J = ch * B; J < (ch + 1) * B && J < D; ++J) {
+                    if (sel[J]) continue;
+                    const double *kb = kop + (size_t)J * d;
+                    double acc = 0.0;
+                    for (int c = 0; c < d; ++c) acc += q[c] * kb[c];
+                    s[n] = acc * inv_sqrt_d + log((double)cnt[J]);
+                    v[n++] = vop + (size_t)J * d;
+                }
+                if (n) eq15_step(s, v, n, d, &m, &l, o);
+            }
+        }
+        for (int c = 0; c < d; ++c) o[c] /= l;
+        lse[r - row_base] = m + log(l) - log(256.0);
+    }
+done:
+    free(s);
+    free(v);
+    free(vals);
+    free(kop);
+    free(vop);
+    free(q);
+    return rc;
+}
 
 /* Output of packed tile t of (b, h) given its selected set sel[0..D]
  * ([V2] Sec.3.2 Eq.6; Eq.4 when the correction is off). For each row r at
@@ -284,6 +421,10 @@ int orc_select(const double *E, int D, double alpha, int sink, int window, uint8
  * row 128 (first tile + t) + i; rows that are not query rows stay 0. */
 int orc_attend_tile(const orc_problem *p, const double *kbar, const double *vbar, long kstride, const int32_t *cnt,
                     int b, int h, int t, const uint8_t *sel, int flags, double *O, double *lse) {
+    if (flags & ORC_EQ15) {
+        if (p->dtype != 1) return ORC_EINVAL;
+        return attend_tile_eq15(p, cnt, b, h, t, sel, flags, O, lse);
+    }
     int g = group(p), d = p->d, B = p->block, L = kv_len(p, b);
     long r0, r1;
     tile_rows(p, b, t, &r0, &r1);

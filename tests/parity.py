@@ -71,7 +71,7 @@ def sample_segments(seg: oracle.Segments, n_random: int, seed: int = 0) -> np.nd
 
 
 def compare(run: GpuRun, seg_ids: Optional[Sequence[int]] = None, n_random: int = 48,
-            check_means: bool = True) -> Report:
+            check_means: bool = True, eq15: bool = False) -> Report:
     w, bufs = run.w, run.bufs
     code = B.fp_device_status(bufs.workspace)
     assert code == B.FP_OK, B.STATUS.get(code, code)
@@ -106,7 +106,7 @@ def compare(run: GpuRun, seg_ids: Optional[Sequence[int]] = None, n_random: int 
     else:
         gpu_sel = np.ones(max(seg.full_total, 1), np.uint8)
     O_t, lse_t = oracle.attend(op, gpu_sel, correction=bool(run.flags & B.FP_MEAN_CORRECTION), dense=dense,
-                               seg=seg, pooled=pooled, seg_ids=ids)
+                               seg=seg, pooled=pooled, seg_ids=ids, eq15=eq15)
     O_ref, lse_ref = oracle.tile_rows_to_tokens(op, seg, ids, O_t, lse_t)
     have = ~np.isnan(lse_ref)
     out = bufs.out.float().cpu().double().numpy()

@@ -107,6 +107,21 @@ def test_fp8_selection_with_query_norms_over_three_decades():
     check_fp8(compare(run_gpu(_rescaled_q(w, row_scale=scale, seed=6))))
 
 
+def test_fp8_tracks_the_eq15_quantised_oracle():
+    # the oracle with Eq.15 taken literally (P~ = e4m3(2^8 e^{s - m}) against the running maximum, in the Eq.17
+    # order, means in E4M3 operand format) against the exact one: the kernel computes the former, so it must sit
+    # far closer to it. 15K tokens at g = 4 make 938 tiles, more than 4 x SMs, so no tile is split into runs.
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[12000, 3000], hq=8, hkv=2, dtype="e4m3",
+                            alpha=0.2, paging="random")
+    r = run_gpu(w)
+    exact = compare(r)
+    quant = compare(r, eq15=True)
+    print("FP8 rel-RMS vs the exact oracle", exact.rel_rms, "vs the Eq.15 oracle", quant.rel_rms)
+    check_fp8(quant)
+    # measured on GB300: 1.7e-3 against the Eq.15 oracle, 2.0e-2 against the exact one
+    assert quant.rel_rms <= 5e-3 and quant.rel_rms < exact.rel_rms / 4
+
+
 def test_bf16_selection_with_outlier_query_elements():
     # one element at 10 times its size in 2% of the query rows loosens the BF16 screening bound
     # (sqrt(d) max |q|) and sends more tiles through the exact fp32 path. (At 30 times the output and the

@@ -632,3 +632,136 @@ def test_prefix_validation_rejects_kv_shorter_than_queries():
     s = p.c_struct()
     import ctypes
     assert oracle.lib().orc_validate(ctypes.byref(s)) == -1
+
+
+# -------------------------------------- P13: quantised FP8 probabilities (Eq.15)
+
+def q8(x: torch.Tensor) -> torch.Tensor:
+    """torch's E4M3 conversion (round to nearest even; finite for |x| <= 464) of fp64 values, via float32."""
+    return x.float().to(torch.float8_e4m3fn).double()
+
+
+def test_round_e4m3_matches_torch_conversion():
+    codes = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double()
+    vals = codes[torch.isfinite(codes)].unique().sort().values    # every finite E4M3 value
+    mids = (vals[1:] + vals[:-1]) / 2                             # the ties, exact in float32
+    rng = np.random.default_rng(3)
+    wide = torch.from_numpy(rng.uniform(-464, 464, 20000)).float().double()
+    small = torch.from_numpy(rng.uniform(-0.03, 0.03, 5000)).float().double()
+    x = torch.cat([vals, mids, wide, small, torch.tensor([455.0, 464.0, -464.0])])
+    np.testing.assert_array_equal(oracle.round_e4m3(x.numpy()), q8(x).numpy())
+    assert oracle.round_e4m3([465.0, 1e6, -1e6]).tolist() == [448.0, 448.0, -448.0]  # saturating
+
+
+def _eq15_step(m, l, o, s, v):
+    """One iteration of the online softmax of Eq.15 over logits s [n] and values v [n, d] (torch, fp64)."""
+    mi = torch.maximum(m, s.max())
+    f = torch.exp(m - mi) if torch.isfinite(m) else torch.tensor(0.0, dtype=torch.float64)
+    w = q8(256.0 * torch.exp(s - mi))
+    return mi, l * f + w.sum(), o * f + w @ v
+
+
+def test_eq15_one_iteration_is_the_quantised_softmax():
+    # requests of at most one block: every tile runs one iteration (its diagonal block), so
+    # O = sum P~ v / sum P~ and LSE = m + ln sum P~ - ln 256 with P~ = e4m3(2^8 e^{s - max s})
+    w = small_workload(lengths=(128, 77), hq=8, hkv=2, dtype="e4m3")
+    p = oracle.Problem.from_workload(w)
+    res = oracle.run(p, alpha=0.0, sink=0, window=0, eq15=True)
+    Q = dequant(p, p.q, p.c_q)
+    for b in range(p.batch):
+        s0, e0 = int(p.cu_seqlens[b]), int(p.cu_seqlens[b + 1])
+        K, V = gathered(p, b)
+        L = e0 - s0
+        for hh in range(p.hq):
+            logits = Q[s0:e0, hh] @ K[:, hh // p.g].T / math.sqrt(D)
+            logits = logits.masked_fill(~torch.ones(L, L, dtype=torch.bool).tril(), float("-inf"))
+            m = logits.max(-1, keepdim=True).values
+            wts = q8(256.0 * torch.exp(logits - m))
+            ref = (wts @ V[:, hh // p.g]) / wts.sum(-1, keepdim=True)
+            assert rel_err(res["O"][s0:e0, hh], ref.numpy()) < 1e-12
+            lse = m[:, 0] + torch.log(wts.sum(-1)) - math.log(256.0)
+            np.testing.assert_allclose(res["lse"][s0:e0, hh], lse.numpy(), rtol=0, atol=1e-12)
+
+
+def test_eq15_blocks_run_in_descending_order():
+    # g = 1, one 256-token request, dense: tile 1 (positions 128..255) runs block 1, then block 0 (Eq.17). The
+    # probabilities of block 1 are quantised against block 1's maximum and only rescaled when block 0 raises it;
+    # the ascending order quantises differently, and the oracle must match the descending one only.
+    w = small_workload(lengths=(256,), hq=1, hkv=1, dtype="e4m3", mu_scale=0.5, seed=4)
+    p = oracle.Problem.from_workload(w)
+    res = oracle.run(p, alpha=0.0, sink=0, window=0, eq15=True)
+    Q = dequant(p, p.q, p.c_q)[:, 0]
+    K, V = gathered(p, 0)
+    K, V = K[:, 0], V[:, 0]
+    worst_desc, best_asc = 0.0, 0.0
+    for r in range(128, 256):
+        s = Q[r] @ K[:r + 1].T / math.sqrt(D)
+        out = []
+        for order in ((1, 0), (0, 1)):
+            m, l, o = torch.tensor(float("-inf"), dtype=torch.float64), torch.tensor(0.0, dtype=torch.float64), 0.0
+            for J in order:
+                sl = slice(128 * J, min(128 * J + 128, r + 1))
+                m, l, o = _eq15_step(m, l, o, s[sl], V[sl])
+            out.append((o / l).numpy())
+        worst_desc = max(worst_desc, rel_err(res["O"][r, 0], out[0]))
+        best_asc = max(best_asc, rel_err(res["O"][r, 0], out[1]))
+    assert worst_desc < 1e-12
+    assert best_asc > 1e-6
+
+
+def test_eq15_correction_chunks_descending_with_operand_format_means():
+    # g = 1, 130 blocks: the last tile (D = 129) appends its pruned blocks as two chunks of means, chunk 1
+    # (block 128) before chunk 0 (blocks 0..127), each mean rounded to E4M3 with its tensor's scale and its
+    # logit shifted by ln 128 (Eq.6). On these inputs chunk 0 raises the running maximum, so the chunk order
+    # decides how chunk 1 is quantised: the ascending order must not match.
+    w = small_workload(lengths=(130 * 128,), hq=1, hkv=1, dtype="e4m3", mu_scale=0.5, seed=6)
+    p = oracle.Problem.from_workload(w)
+    seg = oracle.segments(p)
+    pooled = oracle.pool(p, seg)
+    last = len(seg) - 1
+    assert int(seg.D[last]) == 129
+    sel = oracle.select(p, 0.05, 1, 0, seg=seg, pooled=pooled, seg_ids=[last])
+    picked = sel.selected(seg, last)
+    assert 128 not in picked and len(picked) < 100          # both chunks hold pruned blocks
+    Ot, lt = oracle.attend(p, sel.sel_full, seg=seg, pooled=pooled, seg_ids=[last], eq15=True)
+    Q = dequant(p, p.q, p.c_q)[:, 0]
+    K, V = gathered(p, 0)
+    K, V = K[:, 0], V[:, 0]
+    # the operand-format means: the mean of each block's E4M3 codes (exact in fp64), rounded to E4M3 by the
+    # encoder pinned above, times the tensor's scale
+    kraw = torch.from_numpy(oracle.round_e4m3(K.numpy() / p.c_k)).reshape(130, 128, D)  # exact codes again
+    vraw = torch.from_numpy(oracle.round_e4m3(V.numpy() / p.c_v)).reshape(130, 128, D)
+    kop = torch.from_numpy(oracle.round_e4m3(kraw.mean(1).numpy())) * p.c_k
+    vop = torch.from_numpy(oracle.round_e4m3(vraw.mean(1).numpy())) * p.c_v
+    pruned = [J for J in range(129) if J not in set(picked.tolist())]
+    worst_desc, best_asc = 0.0, 0.0
+    for i in (0, 1, 64, 127):
+        r = 129 * 128 + i
+        s = Q[r] @ K[:r + 1].T / math.sqrt(D)
+        res = []
+        for chunks in ((1, 0), (0, 1)):
+            m, l, o = torch.tensor(float("-inf"), dtype=torch.float64), torch.tensor(0.0, dtype=torch.float64), 0.0
+            for J in sorted(picked.tolist(), reverse=True):
+                sl = slice(128 * J, min(128 * J + 128, r + 1))
+                m, l, o = _eq15_step(m, l, o, s[sl], V[sl])
+            for chunk in chunks:
+                Js = [J for J in pruned if J // 128 == chunk]
+                sm = Q[r] @ kop[Js].T / math.sqrt(D) + math.log(128.0)
+                m, l, o = _eq15_step(m, l, o, sm, vop[Js])
+            res.append(((o / l).numpy(), float(m + torch.log(l) - math.log(256.0))))
+        worst_desc = max(worst_desc, rel_err(Ot[0, i], res[0][0]))
+        best_asc = max(best_asc, rel_err(Ot[0, i], res[1][0]))
+        assert abs(lt[0, i] - res[0][1]) < 1e-12
+    assert worst_desc < 1e-12
+    assert best_asc > 1e-6
+
+
+def test_eq15_stays_within_the_fp8_tolerance_of_the_exact_output():
+    w = small_workload(lengths=(700, 300), hq=8, hkv=2, dtype="e4m3", mu_scale=0.7)
+    p = oracle.Problem.from_workload(w)
+    exact = oracle.run(p, alpha=0.2, sink=1, window=1)
+    quant = oracle.run(p, alpha=0.2, sink=1, window=1, eq15=True)
+    d = quant["O"] - exact["O"]
+    rel_rms = float(np.sqrt((d ** 2).sum() / (exact["O"] ** 2).sum()))
+    assert 1e-4 < rel_rms < 6e-2
+    assert np.array_equal(quant["idx"], exact["idx"])        # the selection does not depend on the mode
