@@ -330,13 +330,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     res = dict(metric=METRIC, value=ms_step / world, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
                ms_per_step=ms_step, higher_is_better=False, scaling="weak", vs_baseline=None,
                dtype=w.dtype, data="synthetic",
-               config=dict(workload=f"{args.workload}: batch {w.batch}, L={max(w.lengths)}"
-                                    + (f" new tokens after a {max(kv_lengths_of(w)) - max(w.lengths)}-token prefix"
-                                       if w.kv_lengths is not None else "")
-                                    + f", Hq={w.hq}, Hkv={w.hkv}, d=128, B=128, page 64, alpha={w.alpha}, "
-                                    f"sink {w.sink_blocks}, window {w.window_blocks}",
-                           tokens=w.total_tokens, inputs_larger_than_l2=True, l2_flush=False,
-                           parallelism=f"replicas x{world}"),
+               config=workload_config(args.workload, w, world),
                stage1_ms=s1_ms, stage2_ms=s2_ms,
                executed_tflops=achieved_tflops,
                dense_equiv_tflops=acc["dense_equiv_flop"] / (ms_step * 1e-3) / 1e12,
@@ -370,6 +364,15 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     return res
 
 
+def workload_config(name: str, w, world: int) -> dict:
+    """The `config` object of the JSON line, the same for both arms."""
+    prefix = (f" new tokens after a {max(kv_lengths_of(w)) - max(w.lengths)}-token prefix"
+              if w.kv_lengths is not None else "")
+    return dict(workload=f"{name}: batch {w.batch}, L={max(w.lengths)}{prefix}, Hq={w.hq}, Hkv={w.hkv}, d=128, "
+                         f"B=128, page 64, alpha={w.alpha}, sink {w.sink_blocks}, window {w.window_blocks}",
+                tokens=w.total_tokens, inputs_larger_than_l2=True, l2_flush=False, parallelism=f"replicas x{world}")
+
+
 def run_reference(args):
     """The fp64 CPU oracle as the reference arm: each step times a bounded sample of the layer."""
     dev = "cuda" if torch.cuda.is_available() else "cpu"
@@ -396,7 +399,8 @@ def run_reference(args):
     v = float(np.mean(times))
     return dict(impl="reference", metric=METRIC, value=v, unit=UNIT, n_gpus=1, steps=args.steps,
                 warmup=args.warmup, ms_per_step=v, higher_is_better=False, scaling="weak", vs_baseline=None,
-                dtype="f64", data="synthetic", config=dict(workload=args.workload, tokens=w.total_tokens),
+                dtype="f64", data="synthetic",
+                config=workload_config(args.workload, w, int(os.environ.get("WORLD_SIZE", "1"))),
                 cpu_baseline=dict(value=v, unit=UNIT, cores=cores, kind="oracle", sample=sample),
                 e2e=dict(value=v, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
 
