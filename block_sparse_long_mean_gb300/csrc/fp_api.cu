@@ -149,6 +149,9 @@ fp_status make_ctx(const fp_problem *p, void *workspace, size_t ws_bytes, fp_str
     return FP_OK;
 }
 
+// A null pointer, or one on an a-byte boundary (a a power of two).
+bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
+
 fp_status launched(cudaError_t e) {
     if (e != cudaSuccess) {
         fprintf(stderr, "libfp: CUDA error: %s\n", cudaGetErrorString(e));
@@ -202,6 +205,10 @@ fp_status fp_select(const fp_problem *p, const void *q, const void *k_pages, con
         (c.s.nblocks > 0 && (!k_pages || !v_pages || !kbar || !vbar || !kbar_op || !vbar_op)))
         return FP_ERR_INVALID_ARG;
     if (c.s.nseg > 0 && !csr_idx) return FP_ERR_INVALID_ARG;
+    // tensors read through TMA start on 16-byte boundaries
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(kbar_op, 16) ||
+        !aligned(vbar_op, 16))
+        return FP_ERR_INVALID_ARG;
     cudaError_t e = cudaMemsetAsync(c.status(), 0, 64 * 4, c.stream);
     if (e == cudaSuccess) e = launch_prep(c);
     if (e == cudaSuccess && c.s.nblocks > 0) e = launch_pool(c, k_pages, v_pages, kbar, vbar, kbar_op, vbar_op);
@@ -239,6 +246,10 @@ fp_status fp_attention(const fp_problem *p, const void *q, const void *k_pages, 
     if (c.s.total_tokens > 0 && (!q || !k_pages || !v_pages || !out)) return FP_ERR_INVALID_ARG;
     if (c.s.nseg > 0 && !dense && (!csr_cu || !csr_idx)) return FP_ERR_INVALID_ARG;
     if (c.s.nseg > 0 && corr && (!kbar_op || !vbar_op)) return FP_ERR_INVALID_ARG;
+    // TMA-read tensors and the 16-byte output stores start on 16-byte boundaries; lse takes fp32 stores
+    if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(kbar_op, 16) ||
+        !aligned(vbar_op, 16) || !aligned(out, 16) || !aligned(lse, 4))
+        return FP_ERR_INVALID_ARG;
     cudaError_t e = cudaMemsetAsync(c.status(), 0, 64 * 4, c.stream);
     if (e == cudaSuccess) e = launch_prep(c);
     if (e == cudaSuccess && c.s.nseg > 0)

@@ -83,6 +83,9 @@ extern "C" fp_status fp_select_noalloc(const fp_problem *p, const void *q, const
         (s.nblocks > 0 && (!k_pages || !v_pages || !kbar || !vbar || !kbar_op || !vbar_op)))
         return FP_ERR_INVALID_ARG;
     if (s.nseg > 0 && !csr_idx) return FP_ERR_INVALID_ARG;
+    // tensors read through TMA start on 16-byte boundaries (as for fp_select)
+    for (const void *t : {q, k_pages, v_pages, (const void *)kbar_op, (const void *)vbar_op})
+        if (reinterpret_cast<uintptr_t>(t) & 15) return FP_ERR_INVALID_ARG;
     char *scratch = nullptr;
     st = scratch_address(&scratch);
     if (st != FP_OK) return st;

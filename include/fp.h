@@ -47,6 +47,9 @@
  *                never selected).
  *   out        [T, Hq, 128] bf16
  *   lse        [T, Hq] fp32, natural-log softmax denominator (optional)
+ * q, k_pages, v_pages, kbar_op, vbar_op and out start on 16-byte boundaries
+ * (TMA reads, 16-byte stores), lse on a 4-byte one; a misaligned pointer is
+ * rejected with FP_ERR_INVALID_ARG before anything is enqueued.
  *   kbar, vbar [num_blocks, Hkv, 128] fp32 block means; request b's blocks
  *                are rows blk_base(b) .. blk_base(b) + ceil(L_b^kv/128) - 1,
  *                blk_base(b) = sum_{b' < b} ceil(L_b'^kv/128)
@@ -85,7 +88,7 @@ typedef struct CUstream_st *fp_stream_t;
 typedef enum {
     FP_OK = 0,
     /* detected on the host: nothing was enqueued */
-    FP_ERR_INVALID_ARG = -1,      /* null pointer, negative size, inconsistent description */
+    FP_ERR_INVALID_ARG = -1,      /* null or misaligned pointer, negative size, inconsistent description */
     FP_ERR_UNSUPPORTED = -2,      /* outside the limits listed above */
     FP_ERR_WORKSPACE = -3,        /* workspace smaller than fp_workspace_bytes() */
     FP_ERR_CUDA = -4,             /* a CUDA runtime call or kernel launch failed */

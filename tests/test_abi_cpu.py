@@ -97,6 +97,20 @@ def test_host_rejects_bad_arguments_before_any_device_work():
                               None) == -1
     assert B.lib.fp_attention(p.ref, fake, fake, fake, fake, fake, 10, None, None, 1, fake, None, fake, need,
                               None) == -1
+    # misaligned tensors: TMA-read inputs and the output need 16 bytes, lse 4
+    odd8, odd2 = ctypes.c_void_p((1 << 20) + 8), ctypes.c_void_p((1 << 20) + 2)
+    assert B.lib.fp_select(p.ref, odd8, fake, fake, 0.1, 1, 1, fake, fake, 10 ** 6, fake, fake, fake, fake, fake,
+                           need, None) == -1
+    assert B.lib.fp_select(p.ref, fake, fake, fake, 0.1, 1, 1, fake, fake, 10 ** 6, fake, fake, odd8, fake, fake,
+                           need, None) == -1
+    assert B.lib.fp_attention(p.ref, fake, odd8, fake, fake, fake, 10, fake, fake, 1, fake, None, fake, need,
+                              None) == -1
+    assert B.lib.fp_attention(p.ref, fake, fake, fake, fake, fake, 10, fake, fake, 1, odd8, None, fake, need,
+                              None) == -1
+    assert B.lib.fp_attention(p.ref, fake, fake, fake, fake, fake, 10, fake, fake, 1, fake, odd2, fake, need,
+                              None) == -1
+    assert B.lib.fp_select_noalloc(p.ref, fake, fake, odd8, 0.1, 1, 1, fake, fake, 10 ** 6, fake, fake, fake, fake,
+                                   None, None) == -1
     # FP8 without scales
     p8 = problem([256], hq=8, hkv=2, dtype="e4m3", c_q=0.0, c_k=1.0, c_v=1.0)
     assert B.lib.fp_workspace_bytes(p8.ref) == -1
