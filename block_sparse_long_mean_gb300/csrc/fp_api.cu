@@ -205,9 +205,10 @@ fp_status fp_select(const fp_problem *p, const void *q, const void *k_pages, con
         (c.s.nblocks > 0 && (!k_pages || !v_pages || !kbar || !vbar || !kbar_op || !vbar_op)))
         return FP_ERR_INVALID_ARG;
     if (c.s.nseg > 0 && !csr_idx) return FP_ERR_INVALID_ARG;
-    // tensors read through TMA start on 16-byte boundaries
+    // tensors read through TMA start on 16-byte boundaries; the int32 / fp32 outputs on 4-byte ones
     if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(kbar_op, 16) ||
-        !aligned(vbar_op, 16))
+        !aligned(vbar_op, 16) || !aligned(csr_cu, 4) || !aligned(csr_idx, 4) || !aligned(kbar, 4) ||
+        !aligned(vbar, 4))
         return FP_ERR_INVALID_ARG;
     cudaError_t e = cudaMemsetAsync(c.status(), 0, 64 * 4, c.stream);
     if (e == cudaSuccess) e = launch_prep(c);
@@ -226,6 +227,8 @@ fp_status fp_csr_expand64(const fp_problem *p, const int32_t *csr_cu, const int3
     if (st != FP_OK) return st;
     if (tile_idx_capacity < 0 || !tile_cu) return FP_ERR_INVALID_ARG;
     if (c.s.nseg > 0 && (!csr_cu || !csr_idx || (tile_idx_capacity > 0 && !tile_idx))) return FP_ERR_INVALID_ARG;
+    if (!aligned(csr_cu, 4) || !aligned(csr_idx, 4) || !aligned(tile_cu, 4) || !aligned(tile_idx, 4))
+        return FP_ERR_INVALID_ARG;
     cudaError_t e = cudaMemsetAsync(c.status(), 0, 64 * 4, c.stream);
     if (e == cudaSuccess) e = launch_prep(c);
     if (e == cudaSuccess) e = launch_expand64(c, csr_cu, csr_idx, tile_cu, tile_idx, tile_idx_capacity);
@@ -248,7 +251,8 @@ fp_status fp_attention(const fp_problem *p, const void *q, const void *k_pages, 
     if (c.s.nseg > 0 && corr && (!kbar_op || !vbar_op)) return FP_ERR_INVALID_ARG;
     // TMA-read tensors and the 16-byte output stores start on 16-byte boundaries; lse takes fp32 stores
     if (!aligned(q, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(kbar_op, 16) ||
-        !aligned(vbar_op, 16) || !aligned(out, 16) || !aligned(lse, 4))
+        !aligned(vbar_op, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(csr_cu, 4) ||
+        !aligned(csr_idx, 4))
         return FP_ERR_INVALID_ARG;
     cudaError_t e = cudaMemsetAsync(c.status(), 0, 64 * 4, c.stream);
     if (e == cudaSuccess) e = launch_prep(c);

@@ -86,6 +86,10 @@ extern "C" fp_status fp_select_noalloc(const fp_problem *p, const void *q, const
     // tensors read through TMA start on 16-byte boundaries (as for fp_select)
     for (const void *t : {q, k_pages, v_pages, (const void *)kbar_op, (const void *)vbar_op})
         if (reinterpret_cast<uintptr_t>(t) & 15) return FP_ERR_INVALID_ARG;
+    // the int32 / fp32 outputs on 4-byte ones
+    for (const void *t : {(const void *)csr_cu, (const void *)csr_idx, (const void *)kbar, (const void *)vbar,
+                          (const void *)device_status})
+        if (reinterpret_cast<uintptr_t>(t) & 3) return FP_ERR_INVALID_ARG;
     char *scratch = nullptr;
     st = scratch_address(&scratch);
     if (st != FP_OK) return st;

@@ -111,6 +111,14 @@ def test_host_rejects_bad_arguments_before_any_device_work():
                               None) == -1
     assert B.lib.fp_select_noalloc(p.ref, fake, fake, odd8, 0.1, 1, 1, fake, fake, 10 ** 6, fake, fake, fake, fake,
                                    None, None) == -1
+    # int32 / fp32 arrays need 4 bytes
+    assert B.lib.fp_select(p.ref, fake, fake, fake, 0.1, 1, 1, odd2, fake, 10 ** 6, fake, fake, fake, fake, fake,
+                           need, None) == -1
+    assert B.lib.fp_select(p.ref, fake, fake, fake, 0.1, 1, 1, fake, fake, 10 ** 6, odd2, fake, fake, fake, fake,
+                           need, None) == -1
+    assert B.lib.fp_attention(p.ref, fake, fake, fake, fake, odd2, 10, fake, fake, 1, fake, None, fake, need,
+                              None) == -1
+    assert B.lib.fp_csr_expand64(p.ref, fake, fake, fake, odd2, 10, fake, need, None) == -1
     # FP8 without scales
     p8 = problem([256], hq=8, hkv=2, dtype="e4m3", c_q=0.0, c_k=1.0, c_v=1.0)
     assert B.lib.fp_workspace_bytes(p8.ref) == -1
