@@ -29,6 +29,10 @@ fp_status describe(const fp_problem *p, Sizes *s) {
     if (p->num_pages < 0 || p->page_table_stride < 0) return FP_ERR_INVALID_ARG;
     if (p->host_cu_seqlens[0] != 0) return FP_ERR_INVALID_ARG;
     if ((p->seqlens_kv == nullptr) != (p->host_seqlens_kv == nullptr)) return FP_ERR_INVALID_ARG;
+    // the device int32 arrays are read with 4-byte loads
+    if ((reinterpret_cast<uintptr_t>(p->cu_seqlens) | reinterpret_cast<uintptr_t>(p->seqlens_kv) |
+         reinterpret_cast<uintptr_t>(p->page_table)) & 3)
+        return FP_ERR_INVALID_ARG;
     Sizes r;
     r.g = g;
     for (int b = 0; b < p->batch; ++b) {

@@ -122,6 +122,10 @@ def test_host_rejects_bad_arguments_before_any_device_work():
     # FP8 without scales
     p8 = problem([256], hq=8, hkv=2, dtype="e4m3", c_q=0.0, c_k=1.0, c_v=1.0)
     assert B.lib.fp_workspace_bytes(p8.ref) == -1
+    # a misaligned device int32 array in the description
+    p = problem([256], hq=8, hkv=2)
+    p.c.page_table = (1 << 20) + 2
+    assert B.lib.fp_num_segments(p.ref) == -1
     # device cu_seqlens missing although tokens exist
     p = problem([256], hq=8, hkv=2)
     p.c.cu_seqlens = None
