@@ -48,9 +48,10 @@
  *   out        [T, Hq, 128] bf16
  *   lse        [T, Hq] fp32, natural-log softmax denominator (optional)
  * q, k_pages, v_pages, kbar_op, vbar_op and out start on 16-byte boundaries
- * (TMA reads, 16-byte stores); lse, the means, the CSR arrays and the other
- * int32 outputs on 4-byte ones. A misaligned pointer is rejected with
- * FP_ERR_INVALID_ARG before anything is enqueued.
+ * (TMA reads, 16-byte stores); lse, the means, the CSR arrays, the other
+ * int32 outputs and the description's device int32 arrays on 4-byte ones. A
+ * misaligned pointer is rejected with FP_ERR_INVALID_ARG before anything is
+ * enqueued.
  *   kbar, vbar [num_blocks, Hkv, 128] fp32 block means; request b's blocks
  *                are rows blk_base(b) .. blk_base(b) + ceil(L_b^kv/128) - 1,
  *                blk_base(b) = sum_{b' < b} ceil(L_b'^kv/128)
