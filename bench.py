@@ -277,10 +277,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     total_ms = start.elapsed_time(stop)
     s1 = [e[0].elapsed_time(e[1]) for e in ev]
     s2 = [e[1].elapsed_time(e[2]) for e in ev]
-    if dist_on:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist_on, dev)
     ms_step = total_ms / args.steps
 
     # end to end through the public API from pinned host buffers
@@ -362,6 +359,15 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
         ms_cpu, cores, sample, _ = oracle_sample_time(w, cu, idx, target_s=args.cpu_seconds)
         res["cpu_baseline"] = dict(value=ms_cpu, unit=UNIT, cores=cores, kind="oracle", sample=sample)
     return res
+
+
+def max_over_ranks(ms: float, dist_on: bool, device) -> float:
+    """The job's time: the slowest rank's (every rank receives it)."""
+    if not dist_on:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
 
 
 def workload_config(name: str, w, world: int) -> dict:
