@@ -73,7 +73,6 @@ def peaks():
 
 def accounting(w, cu: np.ndarray, idx: np.ndarray):
     """FLOP and byte counts of one layer from the workload and its CSR."""
-    import oracle   # segment enumeration only (host bookkeeping)
     op_seg = segments_of(w)
     D = op_seg["D"]
     rows = op_seg["rows"]
