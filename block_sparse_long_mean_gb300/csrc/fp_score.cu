@@ -16,13 +16,16 @@
 // |kbar|_2, so |s_rJ(screen) - s_rJ(exact)| <= eps_J = max_r |q_r| (|kbar -
 // kbar_op| + 2^-12 |kbar|) / sqrt(d) + 2e-4 (Cauchy-Schwarz; the second term
 // covers fp32 accumulation and the exp/log approximations), hence
-// |lE_J(screen) - lE_J| <= eps_J. Every block whose decision (or whose claim
+// |lE_J(screen) - lE_J| <= eps_J. max_r |q_r| is bounded by sqrt(d) max |q_ri|
+// for bf16 and by the rows' own norms for e4m3, whose coarser means make the
+// bound weigh more. Every block whose decision (or whose claim
 // to the maximum) is not settled by these bounds is recomputed in fp32 from
 // the fp32 means, so the CSR matches an exact evaluation except for blocks
 // within fp32 rounding of the threshold.
 //
 // Exponentials are computed only for blocks that can matter. A block's
-// maximum logit ms_J over the tile's rows bounds its log-energy from both
+// maximum logit ms_J over the tile's rows (for a full tile, returned by the
+// TMEM load itself: tcgen05.ld.red.max) bounds its log-energy from both
 // sides, ms_J <= lE_J <= ms_J + ln(rows); the first chunk processed holds the
 // diagonal block, and one block-wide maximum there gives a proven lower bound
 // of max_J lE_J. A later block whose upper bound lies below ln(alpha) plus that
