@@ -6,9 +6,10 @@ CPU-baseline leg are its only users. The product library never imports it.
 The arithmetic lives in ``fp_oracle.c`` (plain C, fp64, POSIX threads). This
 wrapper marshals numpy arrays to it, and does host-side bookkeeping only:
 segment enumeration (request b, KV head h, tile t), CSR assembly from the
-oracle's own selection, and scattering tile rows back to [T, Hq, d] through
+oracle's own selection, scattering tile rows back to [T, Hq, d] through
 the PackGQA row map (pos(r) = floor(r/g), head(r) = h g + r mod g; FlashPrefill
-V2 Sec.3.3 Eq.13).
+V2 Sec.3.3 Eq.13), and the integer work of Stage 2 under a given CSR (each
+tile's visit order, correction masks and page rows; the KV-split plan).
 """
 from __future__ import annotations
 
@@ -351,6 +352,70 @@ def attend(p: Problem, sel_full: np.ndarray, correction: bool = True, dense: boo
     if rc:
         raise RuntimeError(f"oracle attention failed: {rc}")
     return O, lse
+
+
+def tile_schedule(p: Problem, seg: Segments, s: int, cu: np.ndarray, idx: np.ndarray, correction: bool = True,
+                  dense: bool = False) -> np.ndarray:
+    """The Stage 2 iteration sequence of segment s under a given CSR, as rows (J, m0, m1, m2, m3, r0, r1).
+
+    FlashPrefill V2 Sec.3.3 "Index-Driven Sparse Traversal" (Eq.17) walks a tile's selected blocks in descending
+    order; each is one exact iteration (J >= 0) that reads the block's K/V through the page table (Eq.22):
+    r0 and r1 are the pool rows (page * page_size + slot) of the block's first and last page chunk of
+    min(page_size, 128) tokens, or num_pages * page_size for a chunk past the request's KV. Sec.3.2
+    "Implementation" then adds the pruned causal blocks in chunks of 128 means with the mask
+    todo = valid & ~selected, valid = {J < D}: one iteration per chunk c that holds a todo block, chunks in
+    descending order, J = -1 - c, m0..m3 = the chunk's todo bits (bit i of word k: block 128c + 32k + i),
+    r0 = the chunk's first pooled-mean row. Dense mode (alpha = 0) walks every block J <= D, no chunks."""
+    D = int(seg.D[s])
+    b = int(seg.b[s])
+    if dense:
+        S = np.arange(D, -1, -1)
+    else:
+        S = np.sort(np.asarray(idx[cu[s]:cu[s + 1]], dtype=np.int64))[::-1]
+    Lkv = int(p.kv_lengths()[b])
+    ps = p.page_size
+    pse = min(ps, p.block)
+    npc = p.block // pse
+    oob = p.k_pages.shape[0] * ps
+    rows = []
+
+    def pool_row(tok):
+        if tok >= Lkv:
+            return oob
+        return int(p.page_table[b, tok // ps]) * ps + tok % ps
+
+    for J in S:
+        rows.append((int(J), 0, 0, 0, 0, pool_row(int(J) * p.block), pool_row(int(J) * p.block + (npc - 1) * pse)))
+    if correction and not dense and D > 0:
+        todo = np.ones(D, dtype=bool)
+        todo[S[S < D]] = False
+        for c in range((D + 127) // 128 - 1, -1, -1):
+            bits = np.zeros(128, dtype=bool)
+            part = todo[128 * c:min(128 * c + 128, D)]
+            bits[:len(part)] = part
+            if not bits.any():
+                continue
+            words = [int(np.sum(bits[32 * k:32 * k + 32].astype(np.uint64) << np.arange(32, dtype=np.uint64)))
+                     for k in range(4)]
+            rows.append((-1 - c, *words, int(seg.blk_base[b]) + 128 * c, 0))
+    return np.array(rows, dtype=np.int64).reshape(-1, 7)
+
+
+def split_plan(costs: np.ndarray, n_sms: int, min_iters: int = 8, max_ctas: int = 160, tiles_per_sm: int = 4):
+    """Count-balanced KV splits (FlashPrefill V2 Sec.3.3 Eq.18) as this build applies them: while the tiles
+    number fewer than tiles_per_sm x n_sms, a tile of n > C* iterations runs as U = ceil(n / C*) contiguous
+    runs of ceil(n / U) iterations, C* = max(min_iters, ceil(sum n / min(n_sms, max_ctas))). Returns
+    (C* or None when splits are off, list of per-tile run lists [(it_lo, it_hi), ...])."""
+    costs = np.asarray(costs, dtype=np.int64)
+    if len(costs) >= tiles_per_sm * n_sms:
+        return None, [[(0, int(c))] for c in costs]
+    target = max(min_iters, -(-int(costs.sum()) // min(n_sms, max_ctas)))
+    runs = []
+    for c in costs.tolist():
+        u = -(-c // target) if c > target else 1
+        per = -(-c // u) if c else 0
+        runs.append([(k * per, min(c, (k + 1) * per)) for k in range(u)])
+    return target, runs
 
 
 def tile_rows_to_tokens(p: Problem, seg: Segments, seg_ids: Sequence[int], O_tiles: np.ndarray,

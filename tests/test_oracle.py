@@ -765,3 +765,98 @@ def test_eq15_stays_within_the_fp8_tolerance_of_the_exact_output():
     rel_rms = float(np.sqrt((d ** 2).sum() / (exact["O"] ** 2).sum()))
     assert 1e-4 < rel_rms < 6e-2
     assert np.array_equal(quant["idx"], exact["idx"])        # the selection does not depend on the mode
+
+
+# ------------------------------------------- Stage 2 integer work (visit order, correction masks, splits)
+
+def _schedule_problem(length, page, permute, seed=3):
+    """One request, one query head on one KV head (g = 1: tile t holds positions 128 t .. 128 t + 127, so its
+    diagonal block is D = t); zero tensors, only the lengths and the page table matter."""
+    q = np.zeros((length, 1, D), np.uint16)
+    k = np.zeros((length, 1, D), np.uint16)
+    return paged_problem(q, [k], [k], 1, 1, page=page, seed=seed, permute=permute)
+
+
+def test_tile_schedule_hand_example():
+    # D = 300, CSR {0, 5, 299, 300}: Eq.17 visits the selected blocks descending; todo = {J < 300} minus the
+    # selected = {1..4, 6..298}; every 128-block chunk holds a todo block, visited 2, 1, 0
+    p = _schedule_problem(128 * 301, page=64, permute=False)
+    seg = oracle.segments(p)
+    s = 300
+    assert int(seg.D[s]) == 300
+    cu = np.zeros(len(seg) + 1, np.int64)
+    cu[s + 1:] = 4
+    idx = np.array([0, 5, 299, 300])
+    got = oracle.tile_schedule(p, seg, s, cu, idx)
+    full = 0xffffffff
+    want = [
+        # identity page table of 64-token pages: block J's chunks start at rows 128 J and 128 J + 64
+        (300, 0, 0, 0, 0, 38400, 38464),
+        (299, 0, 0, 0, 0, 38272, 38336),
+        (5, 0, 0, 0, 0, 640, 704),
+        (0, 0, 0, 0, 0, 0, 64),
+        # chunk 2: blocks 256..287 all pruned, 288..298 pruned (bits 0..10), 299 selected, nothing past D
+        (-3, full, 0x7ff, 0, 0, 256, 0),
+        (-2, full, full, full, full, 128, 0),
+        # chunk 0: blocks 0 and 5 selected
+        (-1, full & ~1 & ~(1 << 5), full, full, full, 0, 0),
+    ]
+    assert got.tolist() == [list(r) for r in want]
+    # without correction: the four exact iterations only; dense mode: every block 300 .. 0
+    assert oracle.tile_schedule(p, seg, s, cu, idx, correction=False)[:, 0].tolist() == [300, 299, 5, 0]
+    dense = oracle.tile_schedule(p, seg, s, cu, idx, dense=True)
+    assert dense[:, 0].tolist() == list(range(300, -1, -1))
+
+
+def test_tile_schedule_page_rows_and_chunk_skipping():
+    # 32-token pages through a permuted table: a block's first and last page chunks start at its tokens 128 J
+    # and 128 J + 96. A chunk of means whose blocks are all selected is skipped.
+    p = _schedule_problem(1000, page=32, permute=True, seed=11)
+    seg = oracle.segments(p)
+    s = len(seg) - 1
+    D = int(seg.D[s])
+    assert D == 7
+    pt = p.page_table[0]
+    cu = np.zeros(len(seg) + 1, np.int64)
+    cu[s + 1:] = D + 1
+    idx = np.arange(D + 1)       # every block selected: no correction chunk
+    got = oracle.tile_schedule(p, seg, s, cu, idx)
+    assert got[:, 0].tolist() == list(range(7, -1, -1))
+    for row in got:
+        J = int(row[0])
+        assert row[5] == pt[4 * J] * 32 and row[6] == pt[4 * J + 3] * 32
+    # the last block of the 1000-token request: its last page chunk (tokens 992..999) is page 31
+    assert got[0, 6] == pt[31] * 32
+
+
+def test_tile_schedule_out_of_range_chunk_row():
+    # 130-token request with 16-token pages: block 1 holds tokens 128..129 only, so its last page chunk
+    # (token 240) lies past the request and reads the pool's end row
+    p = _schedule_problem(130, page=16, permute=False)
+    seg = oracle.segments(p)
+    s = 1
+    assert int(seg.D[s]) == 1
+    cu = np.array([0, 1, 3])
+    idx = np.array([0, 0, 1])
+    got = oracle.tile_schedule(p, seg, s, cu, idx)
+    oob = p.k_pages.shape[0] * 16
+    assert got[0].tolist() == [1, 0, 0, 0, 0, 128, oob]
+    assert got[1].tolist() == [0, 0, 0, 0, 0, 0, 112]
+
+
+def test_split_plan_closed_forms():
+    # 4 tiles on 2 SMs (fewer than 4 x 2): C* = max(8, ceil(117 / 2)) = 59; the 100-iteration tile runs as
+    # two runs of 50, the others whole
+    target, runs = oracle.split_plan([100, 7, 7, 3], n_sms=2)
+    assert target == 59
+    assert runs == [[(0, 50), (50, 100)], [(0, 7)], [(0, 7)], [(0, 3)]]
+    # 130 iterations against C* = 59: three runs of ceil(130 / 3) = 44, the last one shorter
+    target, runs = oracle.split_plan([130, 1, 1, 1], n_sms=2)
+    assert target == max(8, -(-133 // 2)) == 67
+    assert runs[0] == [(0, 65), (65, 130)]
+    # the floor of 8 iterations per run
+    target, runs = oracle.split_plan([20, 1, 1], n_sms=152)
+    assert target == 8 and runs[0] == [(0, 7), (7, 14), (14, 20)]
+    # as many tiles as 4 x SMs: no splits
+    target, runs = oracle.split_plan([1000] * 8, n_sms=2)
+    assert target is None and all(r == [(0, 1000)] for r in runs)
