@@ -13,6 +13,7 @@
 // ordering) race on it and must be serialised by the caller.
 #include <mutex>
 #include <stdio.h>
+#include <utility>
 
 #include "fp_internal.cuh"
 
@@ -27,31 +28,69 @@ constexpr int kMaxDevices = 64;
 // address with cudaGetSymbolAddress instead.
 static __device__ __align__(256) char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The array's address belongs to one CUDA context: a device reset, or a
+// different context made current on the same device, loads the library's
+// device code again at another address. Addresses are therefore cached per
+// context, keyed by the context's unique id (cuCtxGetId: never reused within
+// the process, unlike a context handle).
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    char *ptr;
+};
 std::mutex g_mu;
-char *g_scratch_ptr[kMaxDevices] = {};
+ScratchEntry g_scratch[kMaxDevices] = {};
+int g_scratch_n = 0, g_scratch_next = 0;
 
-// Device address of the scratch on the current device, looked up once per
-// device (the first call on each device does it, with that device current).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// The unique id of the current context; false if the driver cannot say.
+bool current_context_id(unsigned long long *id) {
+    static const std::pair<CtxGetCurrentFn, CtxGetIdFn> fns = [] {
+        void *cur = nullptr, *gid = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &cur, 12000, cudaEnableDefault, &q1) !=
+                cudaSuccess || q1 != cudaDriverEntryPointSuccess)
+            cur = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &gid, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+            q2 != cudaDriverEntryPointSuccess)
+            gid = nullptr;
+        return std::make_pair(reinterpret_cast<CtxGetCurrentFn>(cur), reinterpret_cast<CtxGetIdFn>(gid));
+    }();
+    if (!fns.first || !fns.second) return false;
+    CUcontext ctx = nullptr;
+    if (fns.first(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return fns.second(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch in the current context. The first call in
+// each context (so the first on each device, and the first after a device
+// reset) looks it up with cudaGetSymbolAddress; later calls take it from the
+// cache. Without a context id the lookup is done on every call.
 fp_status scratch_address(char **out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        fprintf(stderr, "libfp: cudaGetDevice failed: %s\n", cudaGetErrorString(e));
+    // before the runtime's first call on a thread no context may be current yet: then the lookup below
+    // makes the device's primary context current, and the next call finds it in the cache
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (have_id)
+        for (int i = 0; i < g_scratch_n; ++i)
+            if (g_scratch[i].ctx_id == id) {
+                *out = g_scratch[i].ptr;
+                return FP_OK;
+            }
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) {
+        fprintf(stderr, "libfp: cudaGetSymbolAddress of the static scratch failed: %s\n", cudaGetErrorString(e));
         return FP_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) return FP_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess || !ptr) {
-            fprintf(stderr, "libfp: cudaGetSymbolAddress of the static scratch failed: %s\n",
-                    cudaGetErrorString(e));
-            return FP_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = static_cast<char *>(ptr);
+    if (have_id) {
+        // oldest entry out when the table is full
+        const int slot = g_scratch_n < kMaxDevices ? g_scratch_n++ : (g_scratch_next++ % kMaxDevices);
+        g_scratch[slot] = ScratchEntry{id, static_cast<char *>(ptr)};
     }
-    *out = g_scratch_ptr[dev];
+    *out = static_cast<char *>(ptr);
     return FP_OK;
 }
 
