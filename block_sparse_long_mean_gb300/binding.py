@@ -29,7 +29,8 @@ STATUS = {
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTS = ["fp_workspace_bytes", "fp_num_segments", "fp_num_blocks", "fp_csr_capacity", "fp_select",
-           "fp_attention", "fp_device_status", "fp_status_string", "fp_select_noalloc", "fp_csr_expand64"]
+           "fp_attention", "fp_device_status", "fp_status_string", "fp_select_noalloc", "fp_csr_expand64",
+           "fp_read_select_stats", "fp_attention_trace"]
 
 
 class FpError(RuntimeError):
@@ -47,6 +48,10 @@ class fp_problem(ctypes.Structure):
         ("num_pages", ctypes.c_int32), ("host_cu_seqlens", ctypes.c_void_p),
         ("seqlens_kv", ctypes.c_void_p), ("host_seqlens_kv", ctypes.c_void_p),
     ]
+
+
+class fp_select_stats(ctypes.Structure):
+    _fields_ = [("status", ctypes.c_int32), ("exact_tiles", ctypes.c_int32), ("exact_blocks", ctypes.c_int32)]
 
 
 def _load():
@@ -68,6 +73,10 @@ def _load():
     L.fp_csr_expand64.argtypes = [P, vp, vp, vp, vp, i64, vp, sz, vp]
     L.fp_device_status.restype = ctypes.c_int
     L.fp_device_status.argtypes = [vp, vp]
+    L.fp_read_select_stats.restype = ctypes.c_int
+    L.fp_read_select_stats.argtypes = [vp, ctypes.POINTER(fp_select_stats), vp]
+    L.fp_attention_trace.restype = ctypes.c_int
+    L.fp_attention_trace.argtypes = [P, vp, vp, vp, vp, vp, i64, vp, vp, i32, vp, vp, vp, sz, vp, vp, i64]
     L.fp_status_string.restype = ctypes.c_char_p
     L.fp_status_string.argtypes = [ctypes.c_int]
     return L
@@ -181,6 +190,20 @@ def fp_attention(p: Problem, q, k_pages, v_pages, csr_cu, csr_idx, kbar_op, vbar
     return code
 
 
+def fp_attention_trace(p: Problem, q, k_pages, v_pages, csr_cu, csr_idx, kbar_op, vbar_op, flags: int, out, lse,
+                       workspace, trace, stream=None, check: bool = True) -> int:
+    """fp_attention that also records its integer work (work list, visit sequences, correction masks) in
+    `trace`, a device int32 tensor (format in include/fp.h)."""
+    code = lib.fp_attention_trace(p.ref, _p(q), _p(k_pages), _p(v_pages), _p(csr_cu), _p(csr_idx),
+                                  int(csr_idx.numel()) if csr_idx is not None else 0, _p(kbar_op), _p(vbar_op),
+                                  int(flags), _p(out), _p(lse), _p(workspace),
+                                  int(workspace.numel() * workspace.element_size()), _stream(stream), _p(trace),
+                                  int(trace.numel()) if trace is not None else 0)
+    if check:
+        _check(code, "fp_attention_trace")
+    return code
+
+
 def fp_select_noalloc(p: Problem, q, k_pages, v_pages, alpha: float, sink_blocks: int, window_blocks: int, csr_cu,
                       csr_idx, kbar, vbar, kbar_op, vbar_op, device_status=None, stream=None,
                       check: bool = True) -> int:
@@ -207,6 +230,13 @@ def fp_csr_expand64(p: Problem, csr_cu, csr_idx, tile_cu, tile_idx, workspace, s
 
 def fp_device_status(workspace, stream=None) -> int:
     return lib.fp_device_status(_p(workspace), _stream(stream))
+
+
+def fp_read_select_stats(workspace, stream=None) -> dict:
+    """Counters of the last fp_select on this workspace (status, tiles and blocks that took the fp32 path)."""
+    st = fp_select_stats()
+    _check(lib.fp_read_select_stats(_p(workspace), ctypes.byref(st), _stream(stream)), "fp_read_select_stats")
+    return dict(status=st.status, exact_tiles=st.exact_tiles, exact_blocks=st.exact_blocks)
 
 
 def fp_status_string(code: int) -> str:

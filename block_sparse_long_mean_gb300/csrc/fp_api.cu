@@ -239,10 +239,15 @@ fp_status fp_csr_expand64(const fp_problem *p, const int32_t *csr_cu, const int3
     return launched(e);
 }
 
-fp_status fp_attention(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages,
-                       const int32_t *csr_cu, const int32_t *csr_idx, int64_t csr_idx_capacity,
-                       const void *kbar_op, const void *vbar_op, int32_t flags, void *out, float *lse,
-                       void *workspace, size_t workspace_bytes, fp_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+fp_status attention_impl(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages,
+                         const int32_t *csr_cu, const int32_t *csr_idx, int64_t csr_idx_capacity,
+                         const void *kbar_op, const void *vbar_op, int32_t flags, void *out, float *lse,
+                         void *workspace, size_t workspace_bytes, fp_stream_t stream, int32_t *trace,
+                         int64_t trace_words) {
     Ctx c;
     fp_status st = make_ctx(p, workspace, workspace_bytes, stream, &c);
     if (st != FP_OK) return st;
@@ -262,8 +267,34 @@ fp_status fp_attention(const fp_problem *p, const void *q, const void *k_pages, 
     if (e == cudaSuccess) e = launch_prep(c);
     if (e == cudaSuccess && c.s.nseg > 0)
         e = launch_attention(c, q, k_pages, v_pages, csr_cu, csr_idx, csr_idx_capacity, kbar_op, vbar_op,
-                             (corr ? FP_MEAN_CORRECTION : 0) | (dense ? FP_DENSE : 0), out, lse);
+                             (corr ? FP_MEAN_CORRECTION : 0) | (dense ? FP_DENSE : 0), out, lse, trace,
+                             (int32_t)trace_words);
+    else if (e == cudaSuccess && trace)
+        e = cudaMemsetAsync(trace, 0, 8 * sizeof(int32_t), c.stream);  // an empty trace
     return launched(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+fp_status fp_attention(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages,
+                       const int32_t *csr_cu, const int32_t *csr_idx, int64_t csr_idx_capacity,
+                       const void *kbar_op, const void *vbar_op, int32_t flags, void *out, float *lse,
+                       void *workspace, size_t workspace_bytes, fp_stream_t stream) {
+    return attention_impl(p, q, k_pages, v_pages, csr_cu, csr_idx, csr_idx_capacity, kbar_op, vbar_op, flags, out,
+                          lse, workspace, workspace_bytes, stream, nullptr, 0);
+}
+
+fp_status fp_attention_trace(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages,
+                             const int32_t *csr_cu, const int32_t *csr_idx, int64_t csr_idx_capacity,
+                             const void *kbar_op, const void *vbar_op, int32_t flags, void *out, float *lse,
+                             void *workspace, size_t workspace_bytes, fp_stream_t stream, int32_t *trace,
+                             int64_t trace_words) {
+    // the trace is written in 16-byte pieces and counted in int32 words
+    if (!trace || !aligned(trace, 16) || trace_words < 8 || trace_words > INT32_MAX) return FP_ERR_INVALID_ARG;
+    return attention_impl(p, q, k_pages, v_pages, csr_cu, csr_idx, csr_idx_capacity, kbar_op, vbar_op, flags, out,
+                          lse, workspace, workspace_bytes, stream, trace, trace_words);
 }
 
 fp_status fp_device_status(const void *workspace, fp_stream_t stream) {
@@ -277,6 +308,22 @@ fp_status fp_device_status(const void *workspace, fp_stream_t stream) {
         return FP_ERR_CUDA;
     }
     return (fp_status)code;
+}
+
+fp_status fp_read_select_stats(const void *workspace, fp_select_stats *stats, fp_stream_t stream) {
+    if (!workspace || !stats) return FP_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t words[4] = {0, 0, 0, 0};
+    cudaError_t e = cudaMemcpyAsync(words, workspace, sizeof words, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        fprintf(stderr, "libfp: CUDA error: %s\n", cudaGetErrorString(e));
+        return FP_ERR_CUDA;
+    }
+    stats->status = words[kStatusCode];
+    stats->exact_tiles = words[kStatusExactTiles];
+    stats->exact_blocks = words[kStatusExactBlocks];
+    return FP_OK;
 }
 
 const char *fp_status_string(fp_status s) {

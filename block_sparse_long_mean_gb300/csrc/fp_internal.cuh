@@ -89,8 +89,9 @@ struct ReqInfo {
 };
 static_assert(sizeof(ReqInfo) == 48, "ReqInfo is three 16-byte words");
 
-// Status word slots in the workspace (int32 each).
-enum StatusSlot { kStatusCode = 0, kStatusDetail = 1 };
+// Status word slots in the workspace (int32 each). The slots after the code are counters of the last
+// fp_select, cleared with the status word when a call starts.
+enum StatusSlot { kStatusCode = 0, kStatusDetail = 1, kStatusExactTiles = 2, kStatusExactBlocks = 3 };
 
 // Byte offsets of the workspace regions, derived on the host from the sizes.
 struct WsLayout {
@@ -223,6 +224,7 @@ cudaError_t launch_expand64(const Ctx &c, const int32_t *csr_cu, const int32_t *
                             int32_t *tile_idx, int64_t capacity);
 cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, const void *v_pages,
                              const int32_t *csr_cu, const int32_t *csr_idx, int64_t capacity, const void *kbar_op,
-                             const void *vbar_op, int flags, void *out, float *lse);
+                             const void *vbar_op, int flags, void *out, float *lse, int32_t *trace = nullptr,
+                             int32_t trace_words = 0);
 
 }  // namespace fp

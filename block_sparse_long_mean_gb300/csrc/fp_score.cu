@@ -569,6 +569,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
             }
             if (scoring && rs.any2[ap]) {
                 // fp32 recomputation of every unsettled block and every candidate for the maximum
+                if (rt == 0) atomicAdd(status + kStatusExactTiles, 1);
+                int nrefined = 0;
                 for (int J = rt; J <= D; J += kRedThreads) {
                     const bool forced = J < sink || (J >= D - window && J < D) || J == D;
                     const bool bound = bstate[J] & kStBound;
@@ -625,6 +627,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     }
                     const int n = min(rs.nlist, kRefineList);
                     if (n == 0) break;
+                    nrefined += n;
                     for (int i = 0; i < n; ++i) {
                         const int J = rs.list[i];
                         const float *kb = kbar + ((int64_t)(r.blk_base + J) * hkv + sc.h) * kHeadDim;
@@ -649,6 +652,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     }
                     red_bar(set);
                 }
+                if (rt == 0) atomicAdd(status + kStatusExactBlocks, nrefined);
                 // every candidate for the maximum is now exact
                 float mex = -INFINITY;
                 for (int J = rt; J <= D; J += kRedThreads)

@@ -425,14 +425,19 @@ struct AttnParams {
     float *part_o, *part_lse;  // partial outputs of split tiles' runs
     uint32_t smem_bytes;
     int32_t *status;
+    int32_t *trace;      // integer-work trace (fp_attention_trace), or null
+    int32_t trace_cap;   // its capacity in words
 };
+
+// Words of the trace header, of an item header and of one iteration entry (fp.h, fp_attention_trace).
+constexpr int kTraceHeader = 8, kTraceItem = 8, kTraceEntry = 8;
 
 template <bool kSplit>
 __device__ __forceinline__ bool task_live(const TileTask &t) {
     return t.n_exact >= 0 && (kSplit ? t.it_hi > t.it_lo : t.n_exact + t.n_chunks > 0);
 }
 
-template <int kDtype, bool kSplit>
+template <int kDtype, bool kSplit, bool kTrace>
 __global__ void __launch_bounds__(kAThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
@@ -490,8 +495,21 @@ __global__ void __launch_bounds__(kAThreads, 1)
             // ------------------------------------------------------------------------ walker
             uint32_t gi = 0;
             bool ok = true;
+            // the trace entry of the next iteration (fp_attention_trace only; warp-uniform)
+            int32_t *tr = nullptr;
             // publishes iteration gi; `row` is this lane's page-chunk row (lane % npc) for a block
             auto emit = [&](int J, int flags, int tile, const TileTask &tk, uint4 mk, int row) -> bool {
+                if (kTrace && tr && J != kRecEnd) {
+                    const int row_last = __shfl_sync(0xffffffffu, row, npc - 1);
+                    if (lane == 0) {
+                        const int4 a = make_int4(J, flags, (int)mk.x, (int)mk.y);
+                        const int4 b = J >= 0 ? make_int4(0, 0, row, row_last)
+                                              : make_int4((int)mk.z, (int)mk.w, tk.blk_base + 128 * (-1 - J), 0);
+                        reinterpret_cast<int4 *>(tr)[0] = a;
+                        reinterpret_cast<int4 *>(tr)[1] = b;
+                    }
+                    tr += kTraceEntry;
+                }
                 const int slot = gi % kRing;
                 if (!mbar_wait(&sm.rec_empty[slot], ((gi / kRing) & 1) ^ 1, ab)) return false;
                 IterRec &rc = sm.ring[slot];
@@ -524,10 +542,32 @@ __global__ void __launch_bounds__(kAThreads, 1)
             const int nitems = kSplit ? sm.nitems : P.nseg;
             TileTask cur;
             if (w < nitems) cur = P.tasks[w];
+            if (kTrace && blockIdx.x == 0 && lane == 0) P.trace[2] = nitems;
             while (w < nitems && ok) {
                 const int wn = w + gridDim.x;
                 TileTask nxt;
                 if (wn < nitems) nxt = P.tasks[wn];  // overlaps this tile
+                if (kTrace) {
+                    // the item's header, then one entry per iteration as emit publishes it
+                    const bool live = task_live<kSplit>(cur);
+                    const int lo = kSplit ? cur.it_lo : 0, hi = kSplit ? cur.it_hi : cur.n_exact + cur.n_chunks;
+                    const int n = live ? hi - lo : 0;
+                    const int words = kTraceItem + kTraceEntry * n;
+                    int off = 0;
+                    if (lane == 0) off = atomicAdd(P.trace, words);
+                    off = __shfl_sync(0xffffffffu, off, 0);
+                    tr = nullptr;
+                    if (off < 0 || (int64_t)off + words > (int64_t)P.trace_cap - kTraceHeader) {
+                        if (lane == 0) P.trace[1] = 1;
+                    } else {
+                        tr = P.trace + kTraceHeader + off;
+                        if (lane == 0) {
+                            reinterpret_cast<int4 *>(tr)[0] = make_int4(w, cur.b, cur.h, cur.t);
+                            reinterpret_cast<int4 *>(tr)[1] = make_int4(cur.D, live ? lo : 0, live ? hi : 0, cur.n_exact);
+                        }
+                        tr += kTraceItem;
+                    }
+                }
                 if (task_live<kSplit>(cur)) {
                     // this item's iterations [it_lo, it_hi) of the tile's sequence: the selected blocks
                     // (iterations 0 .. n_exact - 1), then the correction chunks
@@ -1147,7 +1187,8 @@ size_t smem_request(size_t layout) {
 
 cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, const void *v_pages,
                              const int32_t *csr_cu, const int32_t *csr_idx, int64_t capacity, const void *kbar_op,
-                             const void *vbar_op, int flags, void *out, float *lse) {
+                             const void *vbar_op, int flags, void *out, float *lse, int32_t *trace,
+                             int32_t trace_words) {
     const int32_t nseg = (int32_t)c.s.nseg;
     // the histogram and, past it, the largest cost
     cudaError_t e = cudaMemsetAsync(c.hist(), 0, sizeof(int32_t) * (kCostBuckets + 1), c.stream);
@@ -1217,6 +1258,9 @@ cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, c
     prm.part_o = c.part_o();
     prm.part_lse = c.part_lse();
     prm.status = c.status();
+    prm.trace = trace;
+    prm.trace_cap = trace_words;
+    if (trace && (e = cudaMemsetAsync(trace, 0, kTraceHeader * sizeof(int32_t), c.stream)) != cudaSuccess) return e;
     auto launch = [&](auto kernel, size_t layout) -> cudaError_t {
         const size_t smem = smem_request(layout);
         prm.smem_bytes = (uint32_t)smem;
@@ -1225,12 +1269,22 @@ cudaError_t launch_attention(const Ctx &c, const void *q, const void *k_pages, c
         kernel<<<grid, kAThreads, smem, c.stream>>>(tm_q, tm_k, tm_v, tm_kb, tm_vb, prm);
         return cudaSuccess;
     };
-    if (fp8)
-        e = split ? launch(attn_tc_kernel<FP_DTYPE_E4M3, true>, sizeof(AttnSmem<FP_DTYPE_E4M3>))
-                  : launch(attn_tc_kernel<FP_DTYPE_E4M3, false>, sizeof(AttnSmem<FP_DTYPE_E4M3>));
-    else
-        e = split ? launch(attn_tc_kernel<FP_DTYPE_BF16, true>, sizeof(AttnSmem<FP_DTYPE_BF16>))
-                  : launch(attn_tc_kernel<FP_DTYPE_BF16, false>, sizeof(AttnSmem<FP_DTYPE_BF16>));
+    // the traced variants differ only in the walker's recording of its records
+    const size_t lay = fp8 ? sizeof(AttnSmem<FP_DTYPE_E4M3>) : sizeof(AttnSmem<FP_DTYPE_BF16>);
+    if (trace) {
+        if (fp8)
+            e = split ? launch(attn_tc_kernel<FP_DTYPE_E4M3, true, true>, lay)
+                      : launch(attn_tc_kernel<FP_DTYPE_E4M3, false, true>, lay);
+        else
+            e = split ? launch(attn_tc_kernel<FP_DTYPE_BF16, true, true>, lay)
+                      : launch(attn_tc_kernel<FP_DTYPE_BF16, false, true>, lay);
+    } else if (fp8) {
+        e = split ? launch(attn_tc_kernel<FP_DTYPE_E4M3, true, false>, lay)
+                  : launch(attn_tc_kernel<FP_DTYPE_E4M3, false, false>, lay);
+    } else {
+        e = split ? launch(attn_tc_kernel<FP_DTYPE_BF16, true, false>, lay)
+                  : launch(attn_tc_kernel<FP_DTYPE_BF16, false, false>, lay);
+    }
     if (e != cudaSuccess) return e;
     if (split)
         attn_combine_kernel<<<4 * kCombineTiles, kCombineThreads, 0, c.stream>>>(

@@ -193,6 +193,44 @@ fp_status fp_attention(const fp_problem *p, const void *q, const void *k_pages, 
                        const void *kbar_op, const void *vbar_op, int32_t flags, void *out, float *lse,
                        void *workspace, size_t workspace_bytes, fp_stream_t stream);
 
+/* fp_attention that also records the attention kernel's integer work, so that
+ * it can be checked against a host recomputation from the same CSR: the
+ * scheduler's work list (heaviest tiles first, Sec.3.3 "Sparsity-Aware Load
+ * Balancing"), each tile's visit sequence (selected blocks in descending order,
+ * Eq.17, then correction chunks in descending order), each correction chunk's
+ * mask (todo = valid & ~selected, Sec.3.2 "Implementation") and the page-table
+ * rows each block is read from (Eq.22). It computes the same outputs as
+ * fp_attention, a little more slowly. Arguments are fp_attention's, plus:
+ *   trace        device int32 [trace_words], 16-byte aligned, overwritten:
+ *                  words 0..7: header {words used after the header, 1 if the
+ *                    trace ran out of room (records past that point are
+ *                    dropped) else 0, number of work items, 0, 0, 0, 0, 0}
+ *                  then one record per work item, in no particular order:
+ *                    8 words {w, b, h, T, D, it_lo, it_hi, n_exact}: the item's
+ *                    position w in the work list, request, KV head, absolute
+ *                    packed tile, diagonal block, the item's iterations
+ *                    [it_lo, it_hi) of the tile's sequence (a whole tile: 0 and
+ *                    its iteration count; a run of a split tile, Eq.18, its
+ *                    contiguous slice; 0 and 0 for an item with no work) and
+ *                    the tile's selected-block count (-1 for a malformed segment);
+ *                    then it_hi - it_lo entries of 8 words
+ *                    {J, flags, m0, m1, m2, m3, r0, r1} in visit order:
+ *                      J >= 0  a selected block; r0, r1 = pool rows (page *
+ *                              page_size + slot) of its first and last page
+ *                              chunk of min(page_size, 128) tokens, or
+ *                              num_pages * page_size past the request's end
+ *                      J < 0   correction chunk c = -1 - J; m0..m3 = the mask of
+ *                              its blocks 128c .. 128c + 127 (bit i of mk = block
+ *                              128c + 32k + i); r0 = its first pooled-mean row
+ *                      flags   bit 0: first iteration of the item, bit 1: last
+ *   trace_words  capacity in int32 words (at most 2^31 - 1): 8 + 8 x (items +
+ *                iterations) always suffices */
+fp_status fp_attention_trace(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages,
+                             const int32_t *csr_cu, const int32_t *csr_idx, int64_t csr_idx_capacity,
+                             const void *kbar_op, const void *vbar_op, int32_t flags, void *out, float *lse,
+                             void *workspace, size_t workspace_bytes, fp_stream_t stream, int32_t *trace,
+                             int64_t trace_words);
+
 /* fp_select without a caller-provided workspace, for callers that cannot
  * allocate device memory (for example a plugin that receives only its input
  * and output tensors, or code on a path where cudaMalloc's implicit
@@ -203,9 +241,10 @@ fp_status fp_attention(const fp_problem *p, const void *q, const void *k_pages, 
  *   - Problems whose fp_select scratch (fp_workspace_bytes less the 21 MB of
  *     split partial outputs that only fp_attention uses) exceeds 16 MiB are
  *     rejected with FP_ERR_WORKSPACE before anything is enqueued.
- *   - It calls no allocator. The first call on each device looks up the
- *     array's device address with that device current; make that first call
- *     before any stream capture.
+ *   - It calls no allocator. The first call in each CUDA context (the first
+ *     on each device, and the first after a device reset, which moves the
+ *     array) looks up the array's device address in that context; make that
+ *     first call before any stream capture.
  *   - All calls share the array and it keeps the previous call's contents:
  *     calls whose work overlaps on the GPU race and must be serialised.
  *   - device_status (device int32, nullable) receives the call's device
@@ -238,6 +277,22 @@ fp_status fp_csr_expand64(const fp_problem *p, const int32_t *csr_cu, const int3
  * clears the status word when it starts), FP_OK if none, or FP_ERR_CUDA if
  * the stream reported an error. */
 fp_status fp_device_status(const void *workspace, fp_stream_t stream);
+
+/* Counters of the most recent fp_select on `workspace`, for tests and
+ * monitoring. The scoring kernel settles most blocks with bounds on their
+ * low-precision energies and recomputes the few it cannot settle in fp32
+ * (the exact path); these counters say how often that happened. */
+typedef struct {
+    int32_t status;       /* the device status code, as fp_device_status returns it */
+    int32_t exact_tiles;  /* packed query tiles whose selection took the fp32 recomputation */
+    int32_t exact_blocks; /* blocks those tiles recomputed in fp32 */
+} fp_select_stats;
+
+/* Waits for `stream`, then copies the counters that the most recent fp_select
+ * on `workspace` left there. A later fp_attention or fp_csr_expand64 on the
+ * same workspace clears them. Returns FP_OK, FP_ERR_INVALID_ARG for a null
+ * pointer, or FP_ERR_CUDA if the stream reported an error. */
+fp_status fp_read_select_stats(const void *workspace, fp_select_stats *stats, fp_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char *fp_status_string(fp_status s);

@@ -18,12 +18,19 @@ if not torch.cuda.is_available():
 from block_sparse_long_mean_gb300 import binding as B  # noqa: E402
 from block_sparse_long_mean_gb300 import synth  # noqa: E402
 
-from parity import BF16_MAX_ABS, BF16_REL_RMS, FP8_REL_RMS, compare, run_gpu  # noqa: E402
+from parity import BF16_MAX_ABS, BF16_REL_RMS, FP8_REL_RMS, compare, correction_effect, run_gpu  # noqa: E402
+
+
+def check_csr(rep):
+    # the whole CSR equals the oracle's except blocks within 1e-3 of the threshold; with none of those the
+    # offsets match too
+    assert rep.csr_mismatch == 0
+    assert rep.cu_equal or rep.near_flips > 0
 
 
 def check_bf16(rep):
     print(rep)
-    assert rep.csr_mismatch == 0
+    check_csr(rep)
     assert rep.rel_rms <= BF16_REL_RMS and rep.max_abs <= BF16_MAX_ABS
     assert rep.lse_max_abs <= 2e-2
     assert rep.mean_max_err <= 1e-4
@@ -31,7 +38,7 @@ def check_bf16(rep):
 
 def check_fp8(rep):
     print(rep)
-    assert rep.csr_mismatch == 0
+    check_csr(rep)
     assert rep.rel_rms <= FP8_REL_RMS
 
 
@@ -212,18 +219,21 @@ def test_llama8b_32k_sampled_parity():
     check_bf16(compare(run_gpu(w)))
 
 
-def test_qwen30b_128k_sampled_parity():
-    w = synth.make_workload("qwen30b_128k", device="cuda")
-    check_bf16(compare(run_gpu(w), n_random=32))
-
-
-def test_qwen30b_128k_fp8_sampled_parity_with_and_without_correction():
-    w = synth.make_workload("qwen30b_128k_fp8", device="cuda")
-    on = compare(run_gpu(w), n_random=24)
-    check_fp8(on)
-    off = compare(run_gpu(w, flags=0), n_random=24, check_means=False)
-    print("fp8 correction on/off rel-RMS vs the oracle of each mode:", on.rel_rms, off.rel_rms)
-    assert off.rel_rms <= FP8_REL_RMS
+@pytest.mark.parametrize("name", ["qwen30b_128k", "qwen30b_128k_fp8"])
+def test_qwen30b_128k_parity_with_and_without_correction(name):
+    # each mode against the oracle of that mode (whole CSR, sampled outputs), then both against exact dense
+    # causal attention on the same tiles: the mean correction must bring the GPU's output closer to it
+    # (V2 Sec.4.4 "Effect of Mean Correction", Sec.3.2 Eq.9)
+    w = synth.make_workload(name, device="cuda")
+    on, off, err_on, err_off = correction_effect(w, n_random=24)
+    check = check_fp8 if w.dtype == "e4m3" else check_bf16
+    check(on)
+    if w.dtype == "e4m3":
+        assert off.rel_rms <= FP8_REL_RMS
+    else:
+        assert off.rel_rms <= BF16_REL_RMS and off.max_abs <= BF16_MAX_ABS
+    print(f"{name}: rel-RMS from dense attention, correction on {err_on:.4e}, off {err_off:.4e}")
+    assert err_on < err_off
 
 
 @pytest.mark.parametrize("name", ["varlen16", "varlen16_fp8"])
