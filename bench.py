@@ -11,6 +11,12 @@ Prints one JSON line (rank 0). `value` is milliseconds per layer for the whole
 job (N GPUs each run one layer per step, so value = step time / N); lower is
 better. `--impl reference` times the fp64 CPU oracle on the host cores instead
 (a bounded sample of the same workload, extrapolated to a layer).
+
+Besides the timed steps the line reports this build's own dense (alpha = 0)
+mode of the same kernels and the speedup over it, Stage 1 against its floor
+max(HBM, MMA, MUFU), the output error of the corrected and uncorrected layer
+against that dense output, and the fp64 oracle timed over the whole layer on
+the host cores (the `cpu_baseline` leg).
 """
 from __future__ import annotations
 
@@ -34,6 +40,11 @@ METRIC = "sparse prefill-attn ms/layer & dense-equiv TFLOP/s at 128K; tensor-pip
 UNIT = "ms/layer"
 DEFAULT_WORKLOAD = "qwen30b_128k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300 datasheet dense tensor peaks (no 2:4 sparsity), for a second fraction beside the measured one
+NOMINAL_TFLOPS = {"bf16": 2250.0, "e4m3": 4500.0}
+# exp2 (MUFU) throughput of one SM per clock: 31.4 ex2.approx.ftz.f32 per clock per SM measured on GB300 with a
+# throughput probe (independent chains, all SMs), i.e. 32 per clock
+MUFU_EX2_PER_CLK_SM = 32.0
 # fp_select: prep, pool, score, csr scan, csr expand; fp_attention: prep, meta, bucket, scatter, attention, and the
 # split combine when the tiles number fewer than 4 x SMs (the library's rule for enabling KV splits)
 KERNELS_PER_STEP = 10
@@ -43,8 +54,8 @@ def kernels_per_step(nseg: int) -> int:
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     return KERNELS_PER_STEP + (1 if nseg < 4 * sms else 0)
 
-# DRAM bytes (read + write) of one attention-kernel launch on this workload, from one ncu capture
-# (profiles/attn_tc_qwen30b_128k.md), valid while the kernel's sources are those the capture ran.
+# DRAM bytes (read + write) of one attention-kernel launch on this workload, from one stored ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid while the kernel's sources are those the capture ran.
 ATTN_TRAFFIC = {"workload": "qwen30b_128k", "bytes": 1.362735e9 + 1.029140e9,
                 "sources_sha256": "9ec1379571af6e930303562307057c612f48208472448c66891ac42809ccfadb"}
 
@@ -103,7 +114,12 @@ def accounting(w, cu: np.ndarray, idx: np.ndarray):
                     + nblk * w.hkv * d * (4 + 4 + 2 * eb)            # means written (fp32 + operand copies)
                     + 4 * (nseg + 1) + 4 * int(cu[-1]))              # CSR written
     causal_blocks = int(np.sum(D + 1))
+    # Stage 1's own arithmetic as the method states it (Eq.19): one dot product of d MACs and one exponential
+    # per (query row, causal block J <= D) of every tile
+    row_blocks = float(np.sum(rows * (D + 1)))
     return dict(executed_flop=executed, dense_equiv_flop=dense_equiv, stage1_bytes=stage1_bytes,
+                dense_mode_executed_flop=tile * float(np.sum(D + 1)),
+                stage1_mma_flop=2.0 * d * row_blocks, stage1_exps=row_blocks,
                 nnz=int(cu[-1]), causal_blocks=causal_blocks, density=int(cu[-1]) / max(causal_blocks, 1),
                 corr_chunks=int(np.sum(chunks)), segments=nseg, rows=rows)
 
@@ -183,6 +199,21 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------- CPU oracle
+
+def oracle_layer_time(w, threads: int | None = None):
+    """Times the fp64 oracle on the whole layer: pooling, selection of every segment and mean-corrected
+    attention of every tile, on all host cores."""
+    import oracle
+    threads = threads or max(1, os.cpu_count() or 1)
+    op = oracle.Problem.from_workload(w)
+    t0 = time.perf_counter()
+    seg = oracle.segments(op)
+    pooled = oracle.pool(op, seg)
+    sel = oracle.select(op, w.alpha, w.sink_blocks, w.window_blocks, seg=seg, pooled=pooled, nthreads=threads)
+    oracle.attend(op, sel.sel_full, seg=seg, pooled=pooled, nthreads=threads)
+    elapsed = time.perf_counter() - t0
+    return elapsed * 1e3, threads, f"the whole layer: {len(seg)} segments pooled, selected and attended"
+
 
 def oracle_sample_time(w, cu: np.ndarray, idx: np.ndarray, target_s: float = 12.0, threads: int | None = None):
     """Times the fp64 oracle on a seeded sample of segments of the workload and extrapolates to one layer
@@ -321,8 +352,20 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     achieved_tflops = acc["executed_flop"] / (s2_mean * 1e-3) / 1e12
     peak_t = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     if w.dtype == "e4m3":
-        peak_t *= 2.0   # FP8 dense rate = 2x BF16 (nominal 4.5 vs 2.25 PFLOP/s)
-    stage1_gbs = acc["stage1_bytes"] / (float(np.mean(s1)) * 1e-3) / 1e9
+        peak_t *= 2.0   # no FP8 GEMM is measured: the BF16 burst times the nominal FP8/BF16 ratio (4.5 / 2.25)
+    nominal_t = NOMINAL_TFLOPS[w.dtype]
+    s1_mean = float(np.mean(s1))
+    stage1_gbs = acc["stage1_bytes"] / (s1_mean * 1e-3) / 1e9
+    hbm = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_ghz = (clk or {}).get("sm_mhz") or float(pk.get("sm_max_mhz", 2070.0))
+    sm_ghz = sm_ghz / 1e3
+    # Stage 1 floor: its bytes at the measured HBM rate, its pooled-key MACs at the tensor peak of its operand
+    # type, its exponentials at the MUFU rate (one per query row and causal block, as Eq.19 states them)
+    floor_hbm = acc["stage1_bytes"] / (hbm * 1e9) * 1e3
+    floor_mma = acc["stage1_mma_flop"] / (peak_t * 1e12) * 1e3
+    floor_mufu = acc["stage1_exps"] / (MUFU_EX2_PER_CLK_SM * sms * sm_ghz * 1e9) * 1e3
+    floor_ms = max(floor_hbm, floor_mma, floor_mufu)
     res = dict(metric=METRIC, value=ms_step / world, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
                ms_per_step=ms_step, higher_is_better=False, scaling="weak", vs_baseline=None,
                dtype=w.dtype, data="synthetic",
@@ -334,14 +377,30 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
                roofline=dict(bound="tensor", kernel="fp_attention (Stage 2: meta, bucket, scatter, attention kernels)",
                              achieved=achieved_tflops,
                              peak=peak_t, unit="TFLOP/s", frac=achieved_tflops / peak_t,
-                             peak_source=f"{pk_src} bf16 burst" + (" x2 for e4m3" if w.dtype == "e4m3" else ""),
-                             traffic=attn_traffic(args.workload), traffic_unit="bytes per launch"),
-               stage1_roofline=dict(bound="hbm", achieved=stage1_gbs, peak=float(pk.get("hbm_gbs", 6800.0)),
-                                    unit="GB/s", frac=stage1_gbs / float(pk.get("hbm_gbs", 6800.0))),
+                             peak_source=(f"{pk_src} bf16 burst (cuBLAS GEMM)" if w.dtype == "bf16" else
+                                          f"{pk_src} bf16 burst x2, the nominal e4m3/bf16 ratio (assumed: no "
+                                          f"e4m3 GEMM measured)"),
+                             nominal_peak=nominal_t, frac_of_nominal=achieved_tflops / nominal_t,
+                             nominal_source="GB300 datasheet dense (no 2:4 sparsity) tensor peak",
+                             traffic=attn_traffic(args.workload), traffic_unit="bytes per launch",
+                             traffic_source="stored ncu capture of these kernel sources (null once they change)"),
+               stage1_roofline=dict(bound="hbm", achieved=stage1_gbs, peak=hbm, unit="GB/s", frac=stage1_gbs / hbm,
+                                    floor_ms=floor_ms, frac_of_floor=floor_ms / s1_mean,
+                                    floor_parts_ms=dict(hbm=floor_hbm, mma=floor_mma, mufu=floor_mufu),
+                                    floor_rule=("max of: Stage 1 bytes at the measured HBM rate; 2 d MACs per "
+                                                "(query row, causal block) at the tensor peak; one exp per "
+                                                f"(query row, causal block) at {MUFU_EX2_PER_CLK_SM:g} ex2 per "
+                                                f"clock per SM x {sms} SMs x {sm_ghz * 1e3:.0f} MHz")),
                e2e=dict(value=e2e_ms, unit=UNIT, h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h)),
                gpu_launches=kernels_per_step(acc["segments"]) * args.steps,
                clocks=clk)
     if args.dense_steps > 0:
+        # this build's own dense mode (alpha = 0: every causal block exact, no correction) through the same
+        # attention kernel; it needs no selection, so it is timed as the fp_attention call alone
+        out_corr = bufs.out.clone()
+        B.fp_attention(p, w.q, w.k_pages, w.v_pages, bufs.csr_cu, bufs.csr_idx, bufs.kbar_op, bufs.vbar_op, 0,
+                       bufs.out, None, bufs.workspace, stream)
+        out_nocorr = bufs.out.clone()
         dstart, dstop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         B.fp_attention(p, w.q, w.k_pages, w.v_pages, bufs.csr_cu, bufs.csr_idx, bufs.kbar_op, bufs.vbar_op,
                        B.FP_DENSE, bufs.out, None, bufs.workspace, stream)
@@ -351,11 +410,28 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
                            B.FP_DENSE, bufs.out, None, bufs.workspace, stream)
         dstop.record(stream)
         torch.cuda.synchronize(dev)
+        code = B.fp_device_status(bufs.workspace, stream)
+        if code != 0:
+            raise RuntimeError(f"device status {B.STATUS.get(code, code)}")
         dense_ms = dstart.elapsed_time(dstop) / args.dense_steps
         res["dense_mode_ms"] = dense_ms
+        res["dense_mode_executed_tflops"] = acc["dense_mode_executed_flop"] / (dense_ms * 1e-3) / 1e12
         res["speedup_vs_dense_mode"] = dense_ms / ms_step
+
+        def rel_rms(a, b):
+            a, b = a.float(), b.float()
+            return float(torch.linalg.vector_norm(a - b) / torch.linalg.vector_norm(b))
+
+        # Sec.4.4 "Effect of Mean Correction": how far the sparse layer lies from dense attention, with and
+        # without the correction (the dense mode is itself checked against the oracle by the parity tests)
+        res["output_rel_rms_vs_dense_mode"] = dict(correction_on=rel_rms(out_corr, bufs.out),
+                                                   correction_off=rel_rms(out_nocorr, bufs.out))
+        del out_corr, out_nocorr
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        ms_cpu, cores, sample, _ = oracle_sample_time(w, cu, idx, target_s=args.cpu_seconds)
+        if args.cpu_mode == "full":
+            ms_cpu, cores, sample = oracle_layer_time(w)
+        else:
+            ms_cpu, cores, sample, _ = oracle_sample_time(w, cu, idx, target_s=args.cpu_seconds)
         res["cpu_baseline"] = dict(value=ms_cpu, unit=UNIT, cores=cores, kind="oracle", sample=sample)
     return res
 
@@ -417,7 +493,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--dense-steps", type=int, default=0)
+    ap.add_argument("--dense-steps", type=int, default=3, help="timed steps of the alpha = 0 dense mode (0: skip)")
+    ap.add_argument("--cpu-mode", default="full", choices=["full", "sample"],
+                    help="cpu_baseline: the oracle over the whole layer, or a timed sample extrapolated to it")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
