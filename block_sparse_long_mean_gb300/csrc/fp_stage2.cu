@@ -12,10 +12,11 @@
 // then one per correction chunk of 128 pooled means (Eq.6): TMA producers
 // bring the Q tile, the block's K and V pages through the page table (Eq.22)
 // or the chunk's means; one thread issues S = Q K^T and O += P V on tcgen05;
-// softmax warps keep one row per thread (online softmax in the base-2
-// domain, causal mask on the diagonal block, the log2|B_J| = 7 shift and the
-// correction mask on mean chunks, lazy rescaling of O); epilogue warps divide
-// by the denominator and write bf16 O and the LSE.
+// softmax warps keep half a row per thread (online softmax in the base-2
+// domain, row maxima returned by the TMEM load, causal mask on the diagonal
+// block, the log2|B_J| = 7 shift and the correction mask on mean chunks, lazy
+// rescaling of O); epilogue warps divide by the denominator and write bf16 O
+// and the LSE.
 // FP8 (Eq.15): Q, K, V and the means are E4M3, S = c_q c_k (Q~ K~^T),
 // P~ = e4m3(256 * 2^(x - m)) with the denominator summing P~, O = c_v ... / l.
 #include <math.h>
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const Spl
 //   warp 2      loader: Q, K and V tiles by TMA, as stages free up
 //   warp 3      idle
 //   warps 4-11  softmax: each warp owns 16 rows of the tile, each row spread
-//               over the 4 threads of a quad (two rows per thread)
+//               over two threads (64 consecutive keys each)
 //   warps 12-15 epilogue: O / l to bf16, LSE
 // Exp2 is the softmax's bound (one per score); two warps per scheduler hide
 // its latency, so the softmax of an iteration takes less time than its two
@@ -835,13 +836,14 @@ __global__ void __launch_bounds__(kAThreads, 1)
     } else if (warp < 12) {
         regs_set<kRegsSoftmax>();
         // -------------------------------------------------------------------------- softmax
-        // Warp w owns 16 rows of the tile, lanes 32 (w % 4) + 16 sub .. + 15 (TMEM lane = packed row).
-        // Thread t holds rows ra = t/4 and rb = t/4 + 8 of them and, of every 8 keys, the two at
-        // 2 (t % 4): a row's 128 scores are spread over the 4 threads of a quad, whose row maxima
-        // and sums combine with two shuffles.
+        // Warp w owns 16 rows of the tile: TMEM lanes 32 (w % 4) + 16 sub .. + 15 (TMEM lane = packed row).
+        // Thread t holds row 32 (w % 4) + 16 sub + t % 16 and the half t / 16 of its 128 keys, 64 consecutive
+        // ones (the .16x32bx2 shapes: the two half-warps read the same lanes at column offsets 0 and 64). The
+        // TMEM load returns the thread's maximum with the scores, and a row's two threads (t, t ^ 16) combine
+        // maxima and sums with one shuffle.
         const int quarter = warp & 3, sub = (warp - 4) >> 2;
-        const int c4 = lane & 3;
-        const int ra = 32 * quarter + 16 * sub + (lane >> 2), rb = ra + 8;  // rows of the tile
+        const int half = lane >> 4;
+        const int row = 32 * quarter + 16 * sub + (lane & 15);  // row of the tile
         const uint32_t tlane = static_cast<uint32_t>(32 * quarter + 16 * sub) << 16;
         const float LOG2E = 1.4426950408889634f;
         const float sl2 = P.c_q * P.c_k * LOG2E * rsqrtf((float)kHeadDim);
@@ -849,7 +851,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
         const float tau = kDtype == FP_DTYPE_E4M3 ? 0.f : 8.f;
         const float pshift = kDtype == FP_DTYPE_E4M3 ? 8.f : 0.f;  // FP8 probabilities in [0, 256] (Eq.15)
         const int gshift = __ffs(g) - 1;                            // g is a power of two
-        float mxa = -INFINITY, mxb = -INFINITY, la = 0.f, lb = 0.f;  // per row; l partial over this thread's keys
+        float mx = -INFINITY, l = 0.f;  // the row's running maximum (log2 units); l: this thread's half of the sum
         for (uint32_t gi = 0;; ++gi) {
             const int slot = gi % kRing;
             if (!mbar_wait(&sm.rec_full[slot], (gi / kRing) & 1, ab)) break;
@@ -865,193 +867,136 @@ __global__ void __launch_bounds__(kAThreads, 1)
             const uint32_t tO = tmem + tlane + kColO;
             const bool first = fl & 1;
             if (first) {
-                mxa = mxb = -INFINITY;
-                la = lb = 0.f;
+                mx = -INFINITY;
+                l = 0.f;
             }
             if (!mbar_wait(&sm.grp[gi & 3], (gi >> 2) & 1, ab)) break;  // group gi computed S(gi)
             tc_fence_after();
-            // sv[h][4k + e] (k < 8): key 64 h + 8k + 2 c4 + (e & 1), row ra (e < 2) or rb (e >= 2)
-            uint32_t sv[2][32];
-            tmem_ld_16x256b_x8(tS, sv[0]);
-            tmem_ld_16x256b_x8(tS + 64, sv[1]);
+            // v[j]: key 64 half + j of the thread's row; rmax their maximum
+            uint32_t v[64];
+            float rmax;
+            tmem_ld_16x32bx2_x64_max<64>(tS, v, rmax);
             tmem_ld_wait();
-            reg_fence32(sv[0]);
-            reg_fence32(sv[1]);
-            // pass 1: mask and row maxima of the raw dot products
-            float pa[4], pb[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) pa[u] = pb[u] = -INFINITY;
+            reg_fence64(v);
+            asm volatile("" : "+f"(rmax));
             const float shift = J < 0 ? 7.f : 0.f;  // log2 |B_J| of a full 128-token block for means
             const bool plain = J >= 0 ? J != D : (mw.x & mw.y & mw.z & mw.w) == 0xffffffffu;
-            if (plain) {
-                // every key takes part (a block off the diagonal, or chunk means with no selected block)
+            if (!plain) {
+                // masked keys become -inf and the maximum is taken again over the rest
+                float pm[8];
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+                if (J >= 0) {
+                    // causal mask on the diagonal block: key <= position - 128 J
+                    const int lim = ((row0 + row) >> gshift) - J * kBlock - 64 * half;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        pa[k & 3] = fmax3(pa[k & 3], __uint_as_float(sv[h][4 * k]), __uint_as_float(sv[h][4 * k + 1]));
-                        pb[k & 3] = fmax3(pb[k & 3], __uint_as_float(sv[h][4 * k + 2]), __uint_as_float(sv[h][4 * k + 3]));
+                    for (int j = 0; j < 64; ++j) {
+                        const float x = j <= lim ? __uint_as_float(v[j]) : -INFINITY;
+                        v[j] = __float_as_uint(x);
+                        pm[j & 7] = fmaxf(pm[j & 7], x);
                     }
-            } else if (J >= 0) {
-                // causal mask on the diagonal block: key <= position - 128 J
-                const int lima = ((row0 + ra) >> gshift) - J * kBlock - 2 * c4;
-                const int limb = ((row0 + rb) >> gshift) - J * kBlock - 2 * c4;
+                } else {
+                    // correction chunk: keep the means of pruned blocks only (bit k & 31 of word k / 32)
+                    const uint32_t w0 = half ? mw.z : mw.x, w1 = half ? mw.w : mw.y;
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int kk = 64 * h + 8 * k + (e & 1);  // key - 2 c4
-                            const bool keep = kk <= ((e < 2) ? lima : limb);
-                            const float v = keep ? __uint_as_float(sv[h][4 * k + e]) : -INFINITY;
-                            sv[h][4 * k + e] = __float_as_uint(v);
-                            if (e < 2) pa[k & 3] = fmaxf(pa[k & 3], v);
-                            else pb[k & 3] = fmaxf(pb[k & 3], v);
-                        }
-            } else {
-                // correction chunk: keep the means of pruned blocks only
-                const uint32_t wv[4] = {mw.x >> (2 * c4), mw.y >> (2 * c4), mw.z >> (2 * c4), mw.w >> (2 * c4)};
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            // key 64 h + 8 k + 2 c4 + (e & 1): word 2 h + k / 4, bit 8 (k % 4) + 2 c4 + (e & 1)
-                            const bool keep = (wv[2 * h + (k >> 2)] >> (8 * (k & 3) + (e & 1))) & 1u;
-                            const float v = keep ? __uint_as_float(sv[h][4 * k + e]) : -INFINITY;
-                            sv[h][4 * k + e] = __float_as_uint(v);
-                            if (e < 2) pa[k & 3] = fmaxf(pa[k & 3], v);
-                            else pb[k & 3] = fmaxf(pb[k & 3], v);
-                        }
-            }
-            float rma = fmaxf(fmaxf(pa[0], pa[1]), fmaxf(pa[2], pa[3]));
-            float rmb = fmaxf(fmaxf(pb[0], pb[1]), fmaxf(pb[2], pb[3]));
-            rma = fmaxf(rma, __shfl_xor_sync(0xffffffffu, rma, 1));
-            rmb = fmaxf(rmb, __shfl_xor_sync(0xffffffffu, rmb, 1));
-            rma = fmaxf(rma, __shfl_xor_sync(0xffffffffu, rma, 2));
-            rmb = fmaxf(rmb, __shfl_xor_sync(0xffffffffu, rmb, 2));
-            const float tma = fmaf(rma, sl2, shift), tmb = fmaf(rmb, sl2, shift);
-            // online softmax with lazy rescaling of O
-            const bool growa = first || tma > mxa + tau, growb = first || tmb > mxb + tau;
-            const float mna = growa ? fmaxf(mxa, tma) : mxa, mnb = growb ? fmaxf(mxb, tmb) : mxb;
-            const bool need_o = !first && (growa || growb);
-            if (__any_sync(0xffffffffu, need_o)) {
-                // O holds the sum up to iteration gi-1 of this tile: wait for that PV (in group gi + 1),
-                // then rescale this thread's part of its two rows in TMEM
-                if (!mbar_wait(&sm.grp[(gi + 1) & 3], ((gi + 1) >> 2) & 1, ab)) break;
-                tc_fence_after();
-                const float fa = (!first && growa) ? ex2(mxa - mna) : 1.f;
-                const float fb = (!first && growb) ? ex2(mxb - mnb) : 1.f;
-                const uint64_t f2a = f2pack(fa, fa), f2b = f2pack(fb, fb);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t ov[32];
-                    tmem_ld_16x256b_x8(tO + 64 * h, ov);
-                    tmem_ld_wait();
-                    reg_fence32(ov);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        float x0, x1;
-                        f2unpack(fmul2(f2pack(__uint_as_float(ov[4 * k]), __uint_as_float(ov[4 * k + 1])), f2a), x0, x1);
-                        ov[4 * k] = __float_as_uint(x0);
-                        ov[4 * k + 1] = __float_as_uint(x1);
-                        f2unpack(fmul2(f2pack(__uint_as_float(ov[4 * k + 2]), __uint_as_float(ov[4 * k + 3])), f2b), x0, x1);
-                        ov[4 * k + 2] = __float_as_uint(x0);
-                        ov[4 * k + 3] = __float_as_uint(x1);
+                    for (int j = 0; j < 64; ++j) {
+                        const bool keep = ((j < 32 ? w0 : w1) >> (j & 31)) & 1u;
+                        const float x = keep ? __uint_as_float(v[j]) : -INFINITY;
+                        v[j] = __float_as_uint(x);
+                        pm[j & 7] = fmaxf(pm[j & 7], x);
                     }
-                    tmem_st_16x256b_x8(tO + 64 * h, ov);
                 }
+                rmax = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7])));
             }
-            if (!first) {
-                la *= ex2(mxa - mna);
-                lb *= ex2(mxb - mnb);
-            }
-            mxa = mna;
-            mxb = mnb;
-            // pass 2: p = 2^(x - m) (FP8: 2^(x - m + 8)), partial row sums, P packed and written over S
-            const float offa = shift - mxa + pshift, offb = shift - mxb + pshift;
-            const uint64_t sl2x2 = f2pack(sl2, sl2), offa2 = f2pack(offa, offa), offb2 = f2pack(offb, offb);
-            uint64_t acca = f2pack(0.f, 0.f), accb = f2pack(0.f, 0.f);
+            rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, 16));
+            const float tm = fmaf(rmax, sl2, shift);
+            // online softmax with lazy rescaling of O
+            const bool grow = first || tm > mx + tau;
+            const float mn = grow ? fmaxf(mx, tm) : mx;
+            const bool need_o = !first && grow;
+            const float fo = need_o ? ex2(mx - mn) : 1.f;  // O's rescale factor
+            if (!first) l *= ex2(mx - mn);
+            mx = mn;
+            // pass 2: p = 2^(x - m) (FP8: 2^(x - m + 8)), this thread's part of the row sum, P packed and written
+            // over the S columns the PV MMA reads it from
+            const float off = shift - mx + pshift;
+            const uint64_t sl2x2 = f2pack(sl2, sl2), off2 = f2pack(off, off);
+            uint64_t acc = f2pack(0.f, 0.f);
             if (kDtype == FP_DTYPE_BF16) {
-                // P word 2k (k < 16) = keys 8k + 2 c4, +1 of row ra, word 2k + 1 the same of row rb:
-                // exactly the .16x128b layout of P columns 4k + c4
+                // P column 32 half + i holds keys 64 half + 2 i, + 1 as two bf16
                 uint32_t pw[32];
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        float y0, y1, y2, y3;
-                        f2unpack(ffma2(f2pack(__uint_as_float(sv[h][4 * k]), __uint_as_float(sv[h][4 * k + 1])), sl2x2, offa2),
-                                 y0, y1);
-                        f2unpack(ffma2(f2pack(__uint_as_float(sv[h][4 * k + 2]), __uint_as_float(sv[h][4 * k + 3])), sl2x2,
-                                       offb2),
-                                 y2, y3);
-                        const float p0 = ex2(y0), p1 = ex2(y1), p2 = ex2(y2), p3 = ex2(y3);
-                        acca = fadd2(acca, f2pack(p0, p1));
-                        accb = fadd2(accb, f2pack(p2, p3));
-                        const __nv_bfloat162 ba = __floats2bfloat162_rn(p0, p1), bb = __floats2bfloat162_rn(p2, p3);
-                        pw[2 * (8 * h + k)] = *reinterpret_cast<const uint32_t *>(&ba);
-                        pw[2 * (8 * h + k) + 1] = *reinterpret_cast<const uint32_t *>(&bb);
-                    }
-                tmem_st_16x128b_x16(tS, pw);
+                for (int i = 0; i < 32; ++i) {
+                    float y0, y1;
+                    f2unpack(ffma2(f2pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sl2x2, off2), y0,
+                             y1);
+                    const float p0 = ex2(y0), p1 = ex2(y1);
+                    acc = fadd2(acc, f2pack(p0, p1));
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+                    pw[i] = *reinterpret_cast<const uint32_t *>(&b2);
+                }
+                tmem_st_16x32bx2_x32<32>(tS, pw);
             } else {
-                // four e4m3 per column: column 2k + c4 / 2 holds keys 8k + 4 (c4 / 2) .. + 3, of row ra for an
-                // even c4 (own pair + the odd neighbour's) and of row rb for an odd c4 (.16x64b layout)
+                // P column 16 half + i holds keys 64 half + 4 i .. + 3 as four e4m3
                 uint32_t pw[16];
-                // the pair exchange moves two columns per shuffle; byte selectors for own/partner halves
-                const bool odd = c4 & 1;
-                const uint32_t sel_lo = odd ? 0x1054u : 0x5410u, sel_hi = odd ? 0x3276u : 0x7632u;
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                for (int i4 = 0; i4 < 16; i4 += 4) {
+                    uint32_t ua[4], ub[4];
 #pragma unroll
-                    for (int k4 = 0; k4 < 2; ++k4) {
-                        uint32_t ua[4], ub[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int k = 4 * k4 + j;
-                            float y0, y1, y2, y3;
-                            f2unpack(ffma2(f2pack(__uint_as_float(sv[h][4 * k]), __uint_as_float(sv[h][4 * k + 1])), sl2x2,
-                                           offa2),
-                                     y0, y1);
-                            f2unpack(ffma2(f2pack(__uint_as_float(sv[h][4 * k + 2]), __uint_as_float(sv[h][4 * k + 3])),
-                                           sl2x2, offb2),
-                                     y2, y3);
-                            const __nv_fp8x2_e4m3 qa(make_float2(ex2(y0), ex2(y1))), qb(make_float2(ex2(y2), ex2(y3)));
-                            ua[j] = qa.__x;
-                            ub[j] = qb.__x;
-                        }
-                        // Eq.15: the sum uses the quantised values; four of them (E4M3 -> f16 is exact) are summed
-                        // in f16 (exact unless their exponents lie more than 7 apart), then in fp32
-                        __half2 sa = __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ua[0], __NV_E4M3)),
-                                             __half2(__nv_cvt_fp8x2_to_halfraw2(ua[1], __NV_E4M3)));
-                        __half2 sb = __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ub[0], __NV_E4M3)),
-                                             __half2(__nv_cvt_fp8x2_to_halfraw2(ub[1], __NV_E4M3)));
-                        sa = __hadd2(sa, __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ua[2], __NV_E4M3)),
-                                                 __half2(__nv_cvt_fp8x2_to_halfraw2(ua[3], __NV_E4M3))));
-                        sb = __hadd2(sb, __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ub[2], __NV_E4M3)),
-                                                 __half2(__nv_cvt_fp8x2_to_halfraw2(ub[3], __NV_E4M3))));
-                        const float2 fa2 = __half22float2(sa), fb2 = __half22float2(sb);
-                        acca = fadd2(acca, f2pack(fa2.x, fa2.y));
-                        accb = fadd2(accb, f2pack(fb2.x, fb2.y));
-#pragma unroll
-                        for (int j = 0; j < 4; j += 2) {
-                            const uint32_t A = ua[j] | (ua[j + 1] << 16), B = ub[j] | (ub[j + 1] << 16);
-                            const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? A : B, 1);
-                            const uint32_t own = odd ? B : A;
-                            pw[8 * h + 4 * k4 + j] = __byte_perm(own, got, sel_lo);
-                            pw[8 * h + 4 * k4 + j + 1] = __byte_perm(own, got, sel_hi);
-                        }
+                    for (int u = 0; u < 4; ++u) {
+                        const int k = 4 * (i4 + u);
+                        float y0, y1, y2, y3;
+                        f2unpack(ffma2(f2pack(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), sl2x2, off2), y0, y1);
+                        f2unpack(ffma2(f2pack(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])), sl2x2, off2), y2,
+                                 y3);
+                        const __nv_fp8x2_e4m3 qa(make_float2(ex2(y0), ex2(y1))), qb(make_float2(ex2(y2), ex2(y3)));
+                        ua[u] = qa.__x;
+                        ub[u] = qb.__x;
+                        pw[i4 + u] = ua[u] | (ub[u] << 16);
                     }
-                tmem_st_16x64b_x16(tS, pw);
+                    // Eq.15: the sum uses the quantised values; four of them (E4M3 -> f16 is exact) are summed in
+                    // f16 (exact unless their exponents lie more than 7 apart), then in fp32
+                    __half2 sa = __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ua[0], __NV_E4M3)),
+                                         __half2(__nv_cvt_fp8x2_to_halfraw2(ua[1], __NV_E4M3)));
+                    __half2 sbb = __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ub[0], __NV_E4M3)),
+                                          __half2(__nv_cvt_fp8x2_to_halfraw2(ub[1], __NV_E4M3)));
+                    sa = __hadd2(sa, __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ua[2], __NV_E4M3)),
+                                             __half2(__nv_cvt_fp8x2_to_halfraw2(ua[3], __NV_E4M3))));
+                    sbb = __hadd2(sbb, __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ub[2], __NV_E4M3)),
+                                               __half2(__nv_cvt_fp8x2_to_halfraw2(ub[3], __NV_E4M3))));
+                    const float2 fa2 = __half22float2(sa), fb2 = __half22float2(sbb);
+                    acc = fadd2(acc, fadd2(f2pack(fa2.x, fa2.y), f2pack(fb2.x, fb2.y)));
+                }
+                tmem_st_16x32bx2_x16<16>(tS, pw);
             }
             {
                 float s0, s1;
-                f2unpack(acca, s0, s1);
-                la += s0 + s1;
-                f2unpack(accb, s0, s1);
-                lb += s0 + s1;
+                f2unpack(acc, s0, s1);
+                l += s0 + s1;
+            }
+            if (__any_sync(0xffffffffu, need_o)) {
+                // O holds the sum up to iteration gi-1 of this tile: wait for that PV (in group gi + 1),
+                // then rescale this thread's half of its row in TMEM. Done after P is written, while the
+                // scores are no longer live; the PV of this iteration waits for p_full, arrived below.
+                if (!mbar_wait(&sm.grp[(gi + 1) & 3], ((gi + 1) >> 2) & 1, ab)) break;
+                tc_fence_after();
+                const uint64_t f2 = f2pack(fo, fo);
+                // 16 columns at a time
+#pragma unroll
+                for (int c = 0; c < 64; c += 16) {
+                    uint32_t ov[16];
+                    tmem_ld_16x32bx2_x16<64>(tO + c, ov);
+                    tmem_ld_wait();
+                    reg_fence16(ov);
+#pragma unroll
+                    for (int k = 0; k < 16; k += 2) {
+                        float x0, x1;
+                        f2unpack(fmul2(f2pack(__uint_as_float(ov[k]), __uint_as_float(ov[k + 1])), f2), x0, x1);
+                        ov[k] = __float_as_uint(x0);
+                        ov[k + 1] = __float_as_uint(x1);
+                    }
+                    tmem_st_16x32bx2_x16<64>(tO + c, ov);
+                }
             }
             tmem_st_wait();
             tc_fence_before();
@@ -1059,16 +1004,11 @@ __global__ void __launch_bounds__(kAThreads, 1)
             if (lane == 0) mbar_arrive(&sm.p_full[sb]);
             if (fl & 2) {
                 // hand the row statistics to the epilogue once it has finished the previous tile
-                float ta = la + __shfl_xor_sync(0xffffffffu, la, 1);
-                float tb = lb + __shfl_xor_sync(0xffffffffu, lb, 1);
-                ta += __shfl_xor_sync(0xffffffffu, ta, 2);
-                tb += __shfl_xor_sync(0xffffffffu, tb, 2);
+                const float lr = l + __shfl_xor_sync(0xffffffffu, l, 16);
                 if (!mbar_wait(&sm.o_empty, (tile & 1) ^ 1, ab)) break;
-                if (c4 == 0) {
-                    sm.stat_m[ra] = mxa;
-                    sm.stat_l[ra] = ta;
-                    sm.stat_m[rb] = mxb;
-                    sm.stat_l[rb] = tb;
+                if (half == 0) {
+                    sm.stat_m[row] = mx;
+                    sm.stat_l[row] = lr;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.st_full);
