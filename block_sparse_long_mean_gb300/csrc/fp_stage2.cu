@@ -333,6 +333,9 @@ constexpr int kRing = 8;                    // iteration records in flight
 constexpr int kRingUsers = 10;              // MMA warp, 8 softmax warps, loader
 constexpr int32_t kRecEnd = -0x7fffffff;    // record after the CTA's last iteration
 constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;  // S_b at 128 b, O at 256, Q_b at 384 + 64 b
+// FP8 only, where a Q buffer takes 32 columns: the Eq.15 denominator sum P~ 1, 16 equal columns accumulated by
+// the tensor core next to O (between the two Q buffers)
+constexpr uint32_t kColL = 416;
 constexpr int kRegsProducer = 80, kRegsSoftmax = 160, kRegsEpilogue = 112;  // 128 x (80 + 2 x 160 + 112) = 64K
 
 template <int kDtype>
@@ -346,6 +349,16 @@ struct ACfg {
     static constexpr uint32_t kFmt = kDtype == FP_DTYPE_BF16 ? 1u : 0u;
     static constexpr uint32_t kIdescQK = instr_desc(kFmt, kFmt, false, false, 128, 128);
     static constexpr uint32_t kIdescPV = instr_desc(kFmt, kFmt, false, true, 128, 128);
+};
+
+// FP8: P~ (from TMEM) times a 128 x 16 tile of ones (K-major): the row sums of P~ in 16 columns
+constexpr uint32_t kIdescL8 = instr_desc(0, 0, false, false, 128, 16);
+
+// The B operand of the FP8 row-sum MMA: 16 rows of 128 E4M3 ones (two 8-row groups of the 128-byte swizzle
+// atom; every byte is 1.0, so the swizzle does not matter). BF16 keeps its row sums on the softmax warps.
+template <int kDtype> struct OnesTile {};
+template <> struct OnesTile<FP_DTYPE_E4M3> {
+    alignas(1024) uint32_t w[512];
 };
 
 // One pipeline iteration as the walker publishes it.
@@ -378,6 +391,7 @@ struct AttnSmem {
     alignas(1024) uint8_t q[ACfg<kDtype>::kTile];
     alignas(1024) uint8_t k[kKStages][ACfg<kDtype>::kTile];
     alignas(1024) uint8_t v[kVStages][ACfg<kDtype>::kTile];
+    OnesTile<kDtype> ones;
     float stat_m[128], stat_l[128];    // a finished tile's running max (log2) and denominator per row
     IterRec ring[kRing];
     uint8_t chunk_list[kMaxChunks];  // walker scratch: a tile's correction chunks, descending
@@ -479,6 +493,12 @@ __global__ void __launch_bounds__(kAThreads, 1)
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(&sm.tmem_base, 512);
+    if constexpr (kDtype == FP_DTYPE_E4M3) {
+        // the ones tile of the row-sum MMA, made visible to the tensor core (async proxy)
+        static_assert(kAThreads == 512, "one word of the ones tile per thread");
+        sm.ones.w[threadIdx.x] = 0x38383838u;  // E4M3 1.0 in every byte
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -775,6 +795,14 @@ __global__ void __launch_bounds__(kAThreads, 1)
                     else
                         umma_f8_ts(tmem + kColO, a, bd, C::kIdescPV, acc);
                 }
+                if constexpr (kDtype == FP_DTYPE_E4M3) {
+                    // Eq.15's denominator: sum of the quantised P~ per row, accumulated like O (N = 16)
+                    const uint32_t obase = smem_addr(sm.ones.w);
+#pragma unroll
+                    for (int k = 0; k < C::kNumK; ++k)
+                        umma_f8_ts(tmem + kColL, tmem + kColS + pb * 128 + k * (C::kKStep * C::kEb / 4),
+                                   sw128_desc(obase + k * 32, 16, 1024), kIdescL8, (!first || k > 0) ? 1u : 0u);
+                }
                 if (x.fl & 2) umma_commit(&sm.o_full);
             };
             It a, b, c;
@@ -937,39 +965,21 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 }
                 tmem_st_16x32bx2_x32<32>(tS, pw);
             } else {
-                // P column 16 half + i holds keys 64 half + 4 i .. + 3 as four e4m3
+                // P column 16 half + i holds keys 64 half + 4 i .. + 3 as four e4m3; Eq.15's denominator (the sum
+                // of these quantised values) is accumulated by the tensor core next to O
                 uint32_t pw[16];
 #pragma unroll
-                for (int i4 = 0; i4 < 16; i4 += 4) {
-                    uint32_t ua[4], ub[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int k = 4 * (i4 + u);
-                        float y0, y1, y2, y3;
-                        f2unpack(ffma2(f2pack(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), sl2x2, off2), y0, y1);
-                        f2unpack(ffma2(f2pack(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])), sl2x2, off2), y2,
-                                 y3);
-                        const __nv_fp8x2_e4m3 qa(make_float2(ex2(y0), ex2(y1))), qb(make_float2(ex2(y2), ex2(y3)));
-                        ua[u] = qa.__x;
-                        ub[u] = qb.__x;
-                        pw[i4 + u] = ua[u] | (ub[u] << 16);
-                    }
-                    // Eq.15: the sum uses the quantised values; four of them (E4M3 -> f16 is exact) are summed in
-                    // f16 (exact unless their exponents lie more than 7 apart), then in fp32
-                    __half2 sa = __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ua[0], __NV_E4M3)),
-                                         __half2(__nv_cvt_fp8x2_to_halfraw2(ua[1], __NV_E4M3)));
-                    __half2 sbb = __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ub[0], __NV_E4M3)),
-                                          __half2(__nv_cvt_fp8x2_to_halfraw2(ub[1], __NV_E4M3)));
-                    sa = __hadd2(sa, __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ua[2], __NV_E4M3)),
-                                             __half2(__nv_cvt_fp8x2_to_halfraw2(ua[3], __NV_E4M3))));
-                    sbb = __hadd2(sbb, __hadd2(__half2(__nv_cvt_fp8x2_to_halfraw2(ub[2], __NV_E4M3)),
-                                               __half2(__nv_cvt_fp8x2_to_halfraw2(ub[3], __NV_E4M3))));
-                    const float2 fa2 = __half22float2(sa), fb2 = __half22float2(sbb);
-                    acc = fadd2(acc, fadd2(f2pack(fa2.x, fa2.y), f2pack(fb2.x, fb2.y)));
+                for (int i = 0; i < 16; ++i) {
+                    const int k = 4 * i;
+                    float y0, y1, y2, y3;
+                    f2unpack(ffma2(f2pack(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), sl2x2, off2), y0, y1);
+                    f2unpack(ffma2(f2pack(__uint_as_float(v[k + 2]), __uint_as_float(v[k + 3])), sl2x2, off2), y2, y3);
+                    const __nv_fp8x2_e4m3 qa(make_float2(ex2(y0), ex2(y1))), qb(make_float2(ex2(y2), ex2(y3)));
+                    pw[i] = (uint32_t)qa.__x | ((uint32_t)qb.__x << 16);
                 }
                 tmem_st_16x32bx2_x16<16>(tS, pw);
             }
-            {
+            if constexpr (kDtype == FP_DTYPE_BF16) {
                 float s0, s1;
                 f2unpack(acc, s0, s1);
                 l += s0 + s1;
@@ -996,6 +1006,13 @@ __global__ void __launch_bounds__(kAThreads, 1)
                         ov[k + 1] = __float_as_uint(x1);
                     }
                     tmem_st_16x32bx2_x16<64>(tO + c, ov);
+                }
+                if constexpr (kDtype == FP_DTYPE_E4M3) {
+                    // the row sum accumulated beside O takes the same factor (columns 0 and 8 of its 16)
+                    uint32_t lw;
+                    tmem_ld_16x32bx2_x1<8>(tmem + tlane + kColL, lw);
+                    tmem_ld_wait();
+                    tmem_st_16x32bx2_x1<8>(tmem + tlane + kColL, __float_as_uint(__uint_as_float(lw) * fo));
                 }
             }
             tmem_st_wait();
@@ -1037,7 +1054,17 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 if (!(ok = mbar_wait(&sm.o_full, ti & 1, ab))) break;
                 if (!(ok = mbar_wait(&sm.st_full, ti & 1, ab))) break;
                 tc_fence_after();
-                const float mx = sm.stat_m[j], l = sm.stat_l[j];
+                float l;
+                if constexpr (kDtype == FP_DTYPE_E4M3) {
+                    // Eq.15's denominator from the tensor core (read before O is released below)
+                    uint32_t lw;
+                    tmem_ld_32x32b_x1(tmem + tlane + kColL, lw);
+                    tmem_ld_wait();
+                    l = __uint_as_float(lw);
+                } else {
+                    l = sm.stat_l[j];
+                }
+                const float mx = sm.stat_m[j];
                 const float inv = l > 0.f ? P.c_v / l : 0.f;
                 const bool part = kSplit && cur.slot >= 0;  // one run of a split tile: fp32 partial output
                 __nv_bfloat16 *orow = P.out + rowi * kHeadDim;

@@ -428,6 +428,18 @@ __device__ __forceinline__ void tmem_st_16x32bx2_x32(uint32_t taddr, const uint3
         : "memory");
 }
 template <int kHalf>
+__device__ __forceinline__ void tmem_ld_16x32bx2_x1(uint32_t taddr, uint32_t &r) {
+    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x1.b32 {%0}, [%1], %2;" : "=r"(r) : "r"(taddr), "n"(kHalf) : "memory");
+}
+template <int kHalf>
+__device__ __forceinline__ void tmem_st_16x32bx2_x1(uint32_t taddr, uint32_t r) {
+    asm volatile("tcgen05.st.sync.aligned.16x32bx2.x1.b32 [%0], %1, {%2};" ::"r"(taddr), "n"(kHalf), "r"(r) : "memory");
+}
+// 32 lanes x 1 column: thread i of the warp receives lane taddr.lane + i.
+__device__ __forceinline__ void tmem_ld_32x32b_x1(uint32_t taddr, uint32_t &r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+}
+template <int kHalf>
 __device__ __forceinline__ void tmem_ld_16x32bx2_x16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16], %17;"
