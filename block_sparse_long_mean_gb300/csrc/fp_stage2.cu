@@ -306,9 +306,10 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const Spl
 //   warp 0      walker: walks the CTA's tiles, looks up the CSR, the page table
 //               and the correction masks in batches, and publishes one record
 //               per iteration in a shared-memory ring, up to kRing ahead
-//   warp 1      MMA issue + TMEM owner
+//   warp 1      MMA issue + TMEM owner: one wait per MMA group, then issue
 //   warp 2      loader: Q, K and V tiles by TMA, as stages free up
-//   warp 3      idle
+//   warp 3      group scheduler: reads the records, waits for each MMA
+//               group's inputs and publishes the group for the MMA warp
 //   warps 4-11  softmax: each warp owns 16 rows of the tile, each row spread
 //               over two threads (64 consecutive keys each)
 //   warps 12-15 epilogue: O / l to bf16, LSE
@@ -330,7 +331,8 @@ constexpr int kAWarps = 16;
 constexpr int kAThreads = 32 * kAWarps;
 constexpr int kKStages = 3, kVStages = 3;
 constexpr int kRing = 8;                    // iteration records in flight
-constexpr int kRingUsers = 10;              // MMA warp, 8 softmax warps, loader
+constexpr int kRingUsers = 10;              // group scheduler, 8 softmax warps, loader
+constexpr int kGroupRing = 4;               // MMA groups published ahead by the scheduler
 constexpr int32_t kRecEnd = -0x7fffffff;    // record after the CTA's last iteration
 constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;  // S_b at 128 b, O at 256, Q_b at 384 + 64 b
 // FP8 only, where a Q buffer takes 32 columns: the Eq.15 denominator sum P~ 1, 16 equal columns accumulated by
@@ -381,6 +383,14 @@ struct alignas(16) IterRec {
     } u;
 };
 
+// One MMA group as the scheduler warp publishes it: what the MMA warp issues for group g.
+struct GroupRec {
+    int32_t pv;  // PV(g - 2): -1 none, else bit 0 the tile's first PV (overwrites O), bit 1 its last (O complete)
+    int32_t qk;  // QK^T(g): -1 none, else bit 0 the tile's first (copies Q into TMEM), bit 1 its last
+    int32_t qb;  // TMEM Q buffer of QK^T(g)
+    int32_t end; // 1: no more groups
+};
+
 // MMA group g: PV(g - 2) (when g >= 2 and that iteration exists) followed by
 // QK^T(g) (when iteration g exists), closed by one commit to grp[g % 4]; its
 // completion means S(g) is ready, K stage g % 3 and V stage (g - 2) % 3 are
@@ -395,7 +405,8 @@ struct AttnSmem {
     float stat_m[128], stat_l[128];    // a finished tile's running max (log2) and denominator per row
     IterRec ring[kRing];
     uint8_t chunk_list[kMaxChunks];  // walker scratch: a tile's correction chunks, descending
-    uint64_t q_full, q_empty, k_full[kKStages], v_full[kVStages], grp[4], p_full[2], qk_done[2], o_full, o_empty,
+    GroupRec group[kGroupRing];
+    uint64_t q_full, q_empty, k_full[kKStages], v_full[kVStages], grp[4], go[2], qk_done[2], o_full, o_empty,
         st_full, rec_full[kRing], rec_empty[kRing];
     uint32_t tmem_base;
     int abort, skip, nitems;
@@ -471,7 +482,8 @@ __global__ void __launch_bounds__(kAThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.p_full[i], 8);
+            // group 2 k + i may issue: 8 softmax arrivals (P of iteration 2 k + i - 2) and the scheduler's
+            mbar_init(&sm.go[i], 9);
             mbar_init(&sm.qk_done[i], 1);
         }
         for (int i = 0; i < 4; ++i) mbar_init(&sm.grp[i], 1);
@@ -718,48 +730,88 @@ __global__ void __launch_bounds__(kAThreads, 1)
                 ph = h;
                 prow = row;
             }
-        } else if (warp == 1) {
-            // ------------------------------------------------------------------------- MMA
-            // Group g = PV(g - 2) then QK^T(g), one commit. Per iteration i the warp reads the record
-            // of iteration i + 2 and takes every wait of group i + 2 except the softmax's P(i) first
-            // (they are normally long satisfied), then waits for P(i) and issues the group at once.
-            // The tensor core holds about one queued MMA, so waits between groups leave it idle. The
-            // whole warp runs the loop (operands stay warp-uniform); one elected lane issues.
+        } else if (warp == 3) {
+            // --------------------------------------------------------------------- group scheduler
+            // Group g = PV(g - 2) then QK^T(g). For each group this warp reads the records, waits for every
+            // input except the softmax's P(g - 2) (V and K stages, O free for a tile's first PV, Q loaded and
+            // its TMEM buffer free for a tile's first QK^T), then publishes the group and arrives on go[g % 2],
+            // which the softmax warps complete with P. The MMA warp thus has one wait per group: the tensor
+            // core holds about one queued MMA, so any bookkeeping between groups would leave it idle.
             struct It {
                 int tile, fl;
                 bool valid;
             };
-            // a wait whose outcome is the same in every lane (an abort seen by one lane ends them all),
-            // so the warp stays converged for elect.sync
-            auto wait_w = [&](uint64_t *bar, uint32_t parity) -> bool {
-                return __all_sync(0xffffffffu, mbar_wait_spin(bar, parity, ab));
-            };
-            uint32_t nrec = 0;  // next record to read
+            uint32_t nrec = 0;
             auto fetch = [&](It &x) -> bool {
                 const int slot = nrec % kRing;
-                if (!wait_w(&sm.rec_full[slot], (nrec / kRing) & 1)) return false;
+                if (!mbar_wait(&sm.rec_full[slot], (nrec / kRing) & 1, ab)) return false;
                 const int4 hd = *reinterpret_cast<const int4 *>(&sm.ring[slot]);  // J, tile, flags, row0
-                const int J = hd.x;
-                x.tile = hd.y;
-                x.fl = hd.z;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.rec_empty[slot]);
-                x.valid = J != kRecEnd;
+                x.tile = hd.y;
+                x.fl = hd.z;
+                x.valid = hd.x != kRecEnd;
                 if (x.valid) ++nrec;
                 return true;
             };
-            // QK^T(gi) of x: its Q (a new tile), the QK^Ts of tile - 2 done with TMEM Q buffer, its K block
-            auto qk_ready = [&](uint32_t gi, const It &x) -> bool {
-                if (x.fl & 1) {
-                    if (!wait_w(&sm.q_full, x.tile & 1)) return false;
-                    if (!wait_w(&sm.qk_done[x.tile & 1], ((x.tile >> 1) & 1) ^ 1)) return false;
+            It a, b, c;  // iterations g - 2, g - 1 and g
+            a.valid = b.valid = false;
+            bool more = true;  // records not yet exhausted
+            for (uint32_t g = 0;; ++g) {
+                // at most three groups ahead of the tensor core: the slot of group g - 4 is free once group g - 3
+                // has completed (group g - 4 was issued before it)
+                if (g >= 3 && !mbar_wait(&sm.grp[(g - 3) & 3], ((g - 3) >> 2) & 1, ab)) break;
+                c.valid = false;
+                if (more) {
+                    if (!fetch(c)) break;
+                    more = c.valid;
                 }
-                return wait_w(&sm.k_full[gi % kKStages], (gi / kKStages) & 1);
-            };
-            auto issue_qk = [&](uint32_t gi, const It &x) {
-                const int ks = gi % kKStages, sb = gi & 1, qb = x.tile & 1;
+                GroupRec gr{-1, -1, 0, 0};
+                bool ok = true;
+                if (a.valid) {
+                    // V(g - 2) loaded; O released by the epilogue before a tile's first PV
+                    ok = mbar_wait(&sm.v_full[(g - 2) % kVStages], ((g - 2) / kVStages) & 1, ab);
+                    if (ok && (a.fl & 1)) ok = mbar_wait(&sm.o_empty, (a.tile & 1) ^ 1, ab);
+                    gr.pv = a.fl & 3;
+                }
+                if (ok && c.valid) {
+                    if (c.fl & 1) {
+                        // a new tile: its Q in shared memory, and TMEM Q buffer tile % 2 done with tile - 2
+                        ok = mbar_wait(&sm.q_full, c.tile & 1, ab);
+                        if (ok) ok = mbar_wait(&sm.qk_done[c.tile & 1], ((c.tile >> 1) & 1) ^ 1, ab);
+                    }
+                    if (ok) ok = mbar_wait(&sm.k_full[g % kKStages], (g / kKStages) & 1, ab);
+                    gr.qk = c.fl & 3;
+                    gr.qb = c.tile & 1;
+                }
+                // go[g % 2] takes this group's arrivals once its phase for group g - 2 has completed. A group
+                // without a PV completes its phase by this warp's arrival alone, so it also waits until the MMA
+                // warp has passed the phase of group g - 2 (that group has completed): a barrier two phases ahead
+                // of its waiter would read as not yet complete
+                if (ok && g >= 2) ok = mbar_wait(&sm.go[g & 1], ((g - 2) >> 1) & 1, ab);
+                if (ok && g >= 2 && !a.valid) ok = mbar_wait(&sm.grp[(g - 2) & 3], ((g - 2) >> 2) & 1, ab);
+                if (!ok) break;
+                const bool last = !a.valid && !c.valid && !b.valid;
+                gr.end = last ? 1 : 0;
+                if (lane == 0) {
+                    sm.group[g % kGroupRing] = gr;
+                    // a group without a PV (the first two, an empty one, the end marker) has no P to wait for:
+                    // the scheduler's arrival completes its phase alone
+                    mbar_arrive_cnt(&sm.go[g & 1], a.valid ? 1u : 9u);
+                }
+                __syncwarp();
+                if (last) break;
+                a = b;
+                b = c;
+            }
+        } else if (warp == 1) {
+            // ------------------------------------------------------------------------- MMA
+            // Per group: one wait (go: the scheduler's inputs and the softmax's P), then the group's MMAs and
+            // one commit. The whole warp runs the loop (operands stay warp-uniform); one elected lane issues.
+            auto issue_qk = [&](uint32_t gi, int fl, int qb) {
+                const int ks = gi % kKStages, sb = gi & 1;
                 const uint32_t tq = tmem + kColQ + qb * 64;
-                if (x.fl & 1) {
+                if (fl & 1) {
                     // a new tile: copy its Q into TMEM buffer qb (last read by the QK^Ts of tile - 2)
                     const uint32_t qbase = smem_addr(sm.q);
 #pragma unroll
@@ -777,12 +829,12 @@ __global__ void __launch_bounds__(kAThreads, 1)
                     else
                         umma_f8_ts(tmem + kColS + sb * 128, tq + k * 8, bd, C::kIdescQK, k > 0);
                 }
-                if (x.fl & 2) umma_commit(&sm.qk_done[qb]);
+                if (fl & 2) umma_commit(&sm.qk_done[qb]);
             };
             // O (+)= P(i) V(i); a tile's first PV overwrites O
-            auto issue_pv = [&](uint32_t i, const It &x) {
+            auto issue_pv = [&](uint32_t i, int fl) {
                 const int vs = i % kVStages, pb = i & 1;
-                const bool first = x.fl & 1;
+                const bool first = fl & 1;
                 const uint32_t vbase = smem_addr(sm.v[vs]);
 #pragma unroll
                 for (int k = 0; k < C::kNumK; ++k) {
@@ -803,62 +855,22 @@ __global__ void __launch_bounds__(kAThreads, 1)
                         umma_f8_ts(tmem + kColL, tmem + kColS + pb * 128 + k * (C::kKStep * C::kEb / 4),
                                    sw128_desc(obase + k * 32, 16, 1024), kIdescL8, (!first || k > 0) ? 1u : 0u);
                 }
-                if (x.fl & 2) umma_commit(&sm.o_full);
+                if (fl & 2) umma_commit(&sm.o_full);
             };
-            It a, b, c;
-            a.valid = b.valid = c.valid = false;
-            bool ok = fetch(a);
-            if (ok && a.valid && (ok = qk_ready(0, a)) && elect_one()) {  // group 0
-                tc_fence_after();
-                issue_qk(0, a);
-                umma_commit(&sm.grp[0]);
-            }
-            __syncwarp();
-            if (ok && a.valid) ok = fetch(b);
-            if (ok && b.valid && (ok = qk_ready(1, b)) && elect_one()) {  // group 1
-                tc_fence_after();
-                issue_qk(1, b);
-                umma_commit(&sm.grp[1]);
-            }
-            __syncwarp();
-            if (ok && b.valid) ok = fetch(c);
-            for (uint32_t i = 0; ok && a.valid; ++i) {
-                // group i + 2: PV(i), then QK^T(i + 2) if that iteration exists. Its inputs other than
-                // P(i) are probed together (the probes' latencies overlap); only a missing one is waited for.
-                const uint32_t i2 = i + 2;
-                bool ready;
-                {
-                    // V(i); O free for a tile's first PV; K(i + 2); Q and its TMEM buffer for a new tile
-                    const uint32_t bv = smem_addr(&sm.v_full[i % kVStages]), pv = (i / kVStages) & 1;
-                    const bool nt = c.valid && (c.fl & 1);
-                    ready = mbar_test5(bv, pv,                                                       //
-                                       (a.fl & 1) ? smem_addr(&sm.o_empty) : bv,                     //
-                                       (a.fl & 1) ? ((a.tile & 1) ^ 1) : pv,                         //
-                                       c.valid ? smem_addr(&sm.k_full[i2 % kKStages]) : bv,          //
-                                       c.valid ? (i2 / kKStages) & 1 : pv,                           //
-                                       nt ? smem_addr(&sm.q_full) : bv, nt ? (c.tile & 1) : pv,      //
-                                       nt ? smem_addr(&sm.qk_done[c.tile & 1]) : bv,                 //
-                                       nt ? ((c.tile >> 1) & 1) ^ 1 : pv);
-                }
-                if (!__all_sync(0xffffffffu, ready)) {
-                    if (c.valid && !(ok = qk_ready(i2, c))) break;
-                    if ((a.fl & 1) && !(ok = wait_w(&sm.o_empty, (a.tile & 1) ^ 1))) break;
-                    if (!(ok = wait_w(&sm.v_full[i % kVStages], (i / kVStages) & 1))) break;
-                }
-                if (!(ok = wait_w(&sm.p_full[i & 1], (i >> 1) & 1))) break;
+            for (uint32_t g = 0;; ++g) {
+                // a wait whose outcome is the same in every lane, so the warp stays converged for elect.sync. It
+                // probes once, then blocks in try_wait rather than spinning: the warp shares its scheduler with
+                // two softmax warps, and the softmax is what this wait is usually for
+                if (!__all_sync(0xffffffffu, mbar_wait(&sm.go[g & 1], (g >> 1) & 1, ab))) break;
+                const int4 gr = *reinterpret_cast<const int4 *>(&sm.group[g % kGroupRing]);  // pv, qk, qb, end
+                if (gr.w) break;
                 if (elect_one()) {
                     tc_fence_after();
-                    issue_pv(i, a);
-                    if (c.valid) issue_qk(i2, c);
-                    umma_commit(&sm.grp[i2 & 3]);
+                    if (gr.x >= 0) issue_pv(g - 2, gr.x);
+                    if (gr.y >= 0) issue_qk(g, gr.y, gr.z);
+                    umma_commit(&sm.grp[g & 3]);
                 }
                 __syncwarp();
-                // the record of iteration i + 3, read while the group's last MMAs run
-                const bool more = c.valid;
-                a = b;
-                b = c;
-                c.valid = false;
-                if (more && !(ok = fetch(c))) break;
             }
         }
     } else if (warp < 12) {
@@ -987,7 +999,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
             if (__any_sync(0xffffffffu, need_o)) {
                 // O holds the sum up to iteration gi-1 of this tile: wait for that PV (in group gi + 1),
                 // then rescale this thread's half of its row in TMEM. Done after P is written, while the
-                // scores are no longer live; the PV of this iteration waits for p_full, arrived below.
+                // scores are no longer live; the PV of this iteration waits for the arrival below.
                 if (!mbar_wait(&sm.grp[(gi + 1) & 3], ((gi + 1) >> 2) & 1, ab)) break;
                 tc_fence_after();
                 const uint64_t f2 = f2pack(fo, fo);
@@ -1018,7 +1030,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.p_full[sb]);
+            if (lane == 0) mbar_arrive(&sm.go[sb]);  // P(gi) is ready for group gi + 2
             if (fl & 2) {
                 // hand the row statistics to the epilogue once it has finished the previous tile
                 const float lr = l + __shfl_xor_sync(0xffffffffu, l, 16);

@@ -70,6 +70,11 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// Arrives `count` times at once.
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                  : "memory");
@@ -164,23 +169,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Abort 
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63) == 0) {
-            if (*ab.flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                *ab.flag = 1;
-                return false;
-            }
-        }
-    }
-}
-
-// Same, polling with the non-blocking probe only: for the MMA-issuing thread,
-// which must notice a completed phase as early as possible.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, Abort ab) {
-    if (mbar_test(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_test(bar, parity)) return true;
-        if ((it & 255) == 0) {
             if (*ab.flag) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 *ab.flag = 1;
