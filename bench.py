@@ -56,8 +56,8 @@ def kernels_per_step(nseg: int) -> int:
 
 # DRAM bytes (read + write) of one attention-kernel launch on this workload, from one stored ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid while the kernel's sources are those the capture ran.
-ATTN_TRAFFIC = {"workload": "qwen30b_128k", "bytes": 1.362735e9 + 1.029140e9,
-                "sources_sha256": "9ec1379571af6e930303562307057c612f48208472448c66891ac42809ccfadb"}
+ATTN_TRAFFIC = {"sources_sha256": "3c53eac609f75a3815468d8bf5ee82cd823f29e3f21e4ebfe6e8709062ab17bc",
+                "bytes": {"qwen30b_128k": 1363542016 + 1025217536, "qwen30b_128k_fp8": 690000384 + 1015759872}}
 
 
 def attn_traffic(workload: str):
@@ -66,8 +66,8 @@ def attn_traffic(workload: str):
     for f in ("fp_stage2.cu", "fp_internal.cuh", "sm100_ptx.cuh"):
         with open(os.path.join(ROOT, "block_sparse_long_mean_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    if workload == ATTN_TRAFFIC["workload"] and h.hexdigest() == ATTN_TRAFFIC["sources_sha256"]:
-        return ATTN_TRAFFIC["bytes"]
+    if h.hexdigest() == ATTN_TRAFFIC["sources_sha256"]:
+        return ATTN_TRAFFIC["bytes"].get(workload)
     return None
 
 
