@@ -269,12 +269,19 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     bufs = B.Buffers(p, device=dev)
     stream = torch.cuda.current_stream(dev)
     flags = B.FP_MEAN_CORRECTION
+    # a chunk after a cached prefix: the prefix's block means were pooled by the previous chunk's selection
+    # (here: one fp_select before the warm-up) and fp_select_chunk pools only the blocks holding new tokens
+    chunked = w.kv_lengths is not None and args.prefix_means == "carried"
+    select = B.fp_select_chunk if chunked else B.fp_select
+    if chunked:
+        B.fp_select(p, w.q, w.k_pages, w.v_pages, w.alpha, w.sink_blocks, w.window_blocks, bufs.csr_cu,
+                    bufs.csr_idx, bufs.kbar, bufs.vbar, bufs.kbar_op, bufs.vbar_op, bufs.workspace, stream)
 
     def step(s1=None, s2=None, s3=None):
         if s1 is not None:
             s1.record(stream)
-        B.fp_select(p, w.q, w.k_pages, w.v_pages, w.alpha, w.sink_blocks, w.window_blocks, bufs.csr_cu,
-                    bufs.csr_idx, bufs.kbar, bufs.vbar, bufs.kbar_op, bufs.vbar_op, bufs.workspace, stream)
+        select(p, w.q, w.k_pages, w.v_pages, w.alpha, w.sink_blocks, w.window_blocks, bufs.csr_cu,
+               bufs.csr_idx, bufs.kbar, bufs.vbar, bufs.kbar_op, bufs.vbar_op, bufs.workspace, stream)
         if s2 is not None:
             s2.record(stream)
         B.fp_attention(p, w.q, w.k_pages, w.v_pages, bufs.csr_cu, bufs.csr_idx, bufs.kbar_op, bufs.vbar_op, flags,
@@ -369,7 +376,9 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     res = dict(metric=METRIC, value=ms_step / world, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
                ms_per_step=ms_step, higher_is_better=False, scaling="weak", vs_baseline=None,
                dtype=w.dtype, data="synthetic",
-               config=workload_config(args.workload, w, world),
+               config=dict(workload_config(args.workload, w, world),
+                           **({"prefix_block_means": "carried from the previous chunk (fp_select_chunk)" if chunked
+                               else "pooled again (fp_select)"} if w.kv_lengths is not None else {})),
                stage1_ms=s1_ms, stage2_ms=s2_ms,
                executed_tflops=achieved_tflops,
                dense_equiv_tflops=acc["dense_equiv_flop"] / (ms_step * 1e-3) / 1e12,
@@ -497,6 +506,9 @@ def main():
     ap.add_argument("--cpu-mode", default="full", choices=["full", "sample"],
                     help="cpu_baseline: the oracle over the whole layer, or a timed sample extrapolated to it")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--prefix-means", default="carried", choices=["carried", "pooled"],
+                    help="workloads with a cached prefix: keep the prefix's block means from the previous chunk "
+                         "(fp_select_chunk) or pool them again (fp_select)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -30,7 +30,7 @@ STATUS = {
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTS = ["fp_workspace_bytes", "fp_num_segments", "fp_num_blocks", "fp_csr_capacity", "fp_select",
            "fp_attention", "fp_device_status", "fp_status_string", "fp_select_noalloc", "fp_csr_expand64",
-           "fp_read_select_stats", "fp_attention_trace"]
+           "fp_read_select_stats", "fp_attention_trace", "fp_select_chunk"]
 
 
 class FpError(RuntimeError):
@@ -65,6 +65,8 @@ def _load():
         getattr(L, name).argtypes = [P]
     L.fp_select.restype = ctypes.c_int
     L.fp_select.argtypes = [P, vp, vp, vp, f32, i32, i32, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]
+    L.fp_select_chunk.restype = ctypes.c_int
+    L.fp_select_chunk.argtypes = [P, vp, vp, vp, f32, i32, i32, vp, vp, i64, vp, vp, vp, vp, vp, sz, vp]
     L.fp_select_noalloc.restype = ctypes.c_int
     L.fp_select_noalloc.argtypes = [P, vp, vp, vp, f32, i32, i32, vp, vp, i64, vp, vp, vp, vp, vp, vp]
     L.fp_attention.restype = ctypes.c_int
@@ -176,6 +178,19 @@ def fp_select(p: Problem, q, k_pages, v_pages, alpha: float, sink_blocks: int, w
                          int(workspace.numel() * workspace.element_size()), _stream(stream))
     if check:
         _check(code, "fp_select")
+    return code
+
+
+def fp_select_chunk(p: Problem, q, k_pages, v_pages, alpha: float, sink_blocks: int, window_blocks: int, csr_cu,
+                    csr_idx, kbar, vbar, kbar_op, vbar_op, workspace, stream=None, check: bool = True) -> int:
+    """fp_select for a chunk after a cached prefix whose block means are already in kbar/vbar/kbar_op/vbar_op."""
+    code = lib.fp_select_chunk(p.ref, _p(q), _p(k_pages), _p(v_pages), float(alpha), int(sink_blocks),
+                               int(window_blocks), _p(csr_cu), _p(csr_idx),
+                               int(csr_idx.numel()) if csr_idx is not None else 0, _p(kbar), _p(vbar), _p(kbar_op),
+                               _p(vbar_op), _p(workspace), int(workspace.numel() * workspace.element_size()),
+                               _stream(stream))
+    if check:
+        _check(code, "fp_select_chunk")
     return code
 
 

@@ -196,10 +196,14 @@ int64_t fp_csr_capacity(const fp_problem *p) {
     return st != FP_OK ? st : s.capacity;
 }
 
-fp_status fp_select(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages, float alpha,
-                    int32_t sink_blocks, int32_t window_blocks, int32_t *csr_cu, int32_t *csr_idx,
-                    int64_t csr_idx_capacity, float *kbar, float *vbar, void *kbar_op, void *vbar_op,
-                    void *workspace, size_t workspace_bytes, fp_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+fp_status select_impl(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages, float alpha,
+                      int32_t sink_blocks, int32_t window_blocks, int32_t *csr_cu, int32_t *csr_idx,
+                      int64_t csr_idx_capacity, float *kbar, float *vbar, void *kbar_op, void *vbar_op,
+                      void *workspace, size_t workspace_bytes, fp_stream_t stream, bool reuse_prefix) {
     Ctx c;
     fp_status st = make_ctx(p, workspace, workspace_bytes, stream, &c);
     if (st != FP_OK) return st;
@@ -216,11 +220,32 @@ fp_status fp_select(const fp_problem *p, const void *q, const void *k_pages, con
         return FP_ERR_INVALID_ARG;
     cudaError_t e = cudaMemsetAsync(c.status(), 0, 64 * 4, c.stream);
     if (e == cudaSuccess) e = launch_prep(c);
-    if (e == cudaSuccess && c.s.nblocks > 0) e = launch_pool(c, k_pages, v_pages, kbar, vbar, kbar_op, vbar_op);
+    if (e == cudaSuccess && c.s.nblocks > 0)
+        e = launch_pool(c, k_pages, v_pages, kbar, vbar, kbar_op, vbar_op, reuse_prefix);
     if (e == cudaSuccess && c.s.nseg > 0)
         e = launch_score(c, q, kbar, kbar_op, alpha, sink_blocks, window_blocks);
     if (e == cudaSuccess) e = launch_csr(c, csr_cu, csr_idx, csr_idx_capacity);
     return launched(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+fp_status fp_select(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages, float alpha,
+                    int32_t sink_blocks, int32_t window_blocks, int32_t *csr_cu, int32_t *csr_idx,
+                    int64_t csr_idx_capacity, float *kbar, float *vbar, void *kbar_op, void *vbar_op,
+                    void *workspace, size_t workspace_bytes, fp_stream_t stream) {
+    return select_impl(p, q, k_pages, v_pages, alpha, sink_blocks, window_blocks, csr_cu, csr_idx, csr_idx_capacity,
+                       kbar, vbar, kbar_op, vbar_op, workspace, workspace_bytes, stream, false);
+}
+
+fp_status fp_select_chunk(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages,
+                          float alpha, int32_t sink_blocks, int32_t window_blocks, int32_t *csr_cu, int32_t *csr_idx,
+                          int64_t csr_idx_capacity, float *kbar, float *vbar, void *kbar_op, void *vbar_op,
+                          void *workspace, size_t workspace_bytes, fp_stream_t stream) {
+    return select_impl(p, q, k_pages, v_pages, alpha, sink_blocks, window_blocks, csr_cu, csr_idx, csr_idx_capacity,
+                       kbar, vbar, kbar_op, vbar_op, workspace, workspace_bytes, stream, true);
 }
 
 fp_status fp_csr_expand64(const fp_problem *p, const int32_t *csr_cu, const int32_t *csr_idx, int32_t *tile_cu,

@@ -216,7 +216,7 @@ WsLayout layout(const fp_problem *p, const Sizes &s);
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_prep(const Ctx &c);
 cudaError_t launch_pool(const Ctx &c, const void *k_pages, const void *v_pages, float *kbar, float *vbar,
-                        void *kbar_op, void *vbar_op);
+                        void *kbar_op, void *vbar_op, bool reuse_prefix = false);
 cudaError_t launch_score(const Ctx &c, const void *q, const float *kbar, const void *kbar_op, float alpha, int sink,
                          int window);
 cudaError_t launch_csr(const Ctx &c, int32_t *csr_cu, int32_t *csr_idx, int64_t capacity);

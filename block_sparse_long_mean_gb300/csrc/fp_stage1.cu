@@ -122,6 +122,9 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t *__restrict__ 
 // sums the token groups. FP8 elements are descaled before summing. The
 // block's page ids are looked up once per CTA, and the per-head rounding
 // statistics are reduced within each warp before their shared atomics.
+// With reuse_prefix, a block lying wholly in the request's cached prefix
+// keeps the means already in the arrays (an earlier chunk's pooling of the
+// same keys and values) and only its rounding statistics are recomputed.
 template <int kDtype>
 __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ kp, const uint8_t *__restrict__ vp,
                                                    const int32_t *__restrict__ page_table, int pt_stride,
@@ -129,7 +132,8 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ k
                                                    int batch, int hkv, float c_k, float c_v,
                                                    float *__restrict__ kbar, float *__restrict__ vbar,
                                                    void *__restrict__ kbar_op, void *__restrict__ vbar_op,
-                                                   float2 *__restrict__ kstat, int32_t *__restrict__ status) {
+                                                   float2 *__restrict__ kstat, int reuse_prefix,
+                                                   int32_t *__restrict__ status) {
     using E = Elem<kDtype>;
     constexpr int kEb = E::kBytes;
     constexpr int kEpv = 16 / kEb;  // elements per 16-byte vector
@@ -142,6 +146,33 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint8_t *__restrict__ k
     const int b = find_req_by_block(req, batch, gb);
     const ReqInfo r = req[b];
     const int J = gb - r.blk_base;
+    if (reuse_prefix && (J + 1) * kBlock <= r.kv_len - r.len) {
+        // every token of the block precedes the new ones: its means are kept; the rounding statistics of the
+        // operand-format key mean go to this call's workspace, reduced in the same warp grouping as below
+        const int64_t base = (int64_t)gb * hkv * kHeadDim;
+        __syncthreads();
+        for (int x = threadIdx.x; x < hkv * kHeadDim; x += 256) {
+            const float mk = kbar[base + x];
+            const float kq = kDtype == FP_DTYPE_E4M3
+                                 ? float(reinterpret_cast<const __nv_fp8_e4m3 *>(kbar_op)[base + x]) * c_k
+                                 : __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(kbar_op)[base + x]);
+            float e2 = (mk - kq) * (mk - kq), n2 = mk * mk;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                e2 += __shfl_xor_sync(0xffffffffu, e2, o);
+                n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+            }
+            if ((threadIdx.x & 31) == 0) {
+                atomicAdd(&kst[0][x / kHeadDim], e2);
+                atomicAdd(&kst[1][x / kHeadDim], n2);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x < hkv)
+            kstat[(int64_t)gb * hkv + threadIdx.x] =
+                make_float2(sqrtf(kst[0][threadIdx.x]), sqrtf(kst[1][threadIdx.x]));
+        return;
+    }
     const int n = min(kBlock, r.kv_len - J * kBlock);
     const int npg = (n + page_size - 1) / page_size;  // pages holding the block's tokens (blocks start on a page)
     if (threadIdx.x < npg) {
@@ -345,18 +376,18 @@ cudaError_t launch_prep(const Ctx &c) {
 }
 
 cudaError_t launch_pool(const Ctx &c, const void *k_pages, const void *v_pages, float *kbar, float *vbar,
-                        void *kbar_op, void *vbar_op) {
+                        void *kbar_op, void *vbar_op, bool reuse_prefix) {
     const dim3 grid((unsigned)c.s.nblocks);
     if (c.p.dtype == FP_DTYPE_E4M3)
         pool_kernel<FP_DTYPE_E4M3><<<grid, 256, 0, c.stream>>>(
             (const uint8_t *)k_pages, (const uint8_t *)v_pages, c.p.page_table, c.p.page_table_stride,
             c.p.num_pages, c.p.page_size, c.req(), c.p.batch, c.p.num_kv_heads, c.p.c_k, c.p.c_v, kbar, vbar,
-            kbar_op, vbar_op, c.kstat(), c.status());
+            kbar_op, vbar_op, c.kstat(), reuse_prefix ? 1 : 0, c.status());
     else
         pool_kernel<FP_DTYPE_BF16><<<grid, 256, 0, c.stream>>>(
             (const uint8_t *)k_pages, (const uint8_t *)v_pages, c.p.page_table, c.p.page_table_stride,
             c.p.num_pages, c.p.page_size, c.req(), c.p.batch, c.p.num_kv_heads, 1.f, 1.f, kbar, vbar, kbar_op,
-            vbar_op, c.kstat(), c.status());
+            vbar_op, c.kstat(), reuse_prefix ? 1 : 0, c.status());
     return cudaGetLastError();
 }
 

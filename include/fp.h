@@ -166,6 +166,24 @@ fp_status fp_select(const fp_problem *p, const void *q, const void *k_pages, con
                     int64_t csr_idx_capacity, float *kbar, float *vbar, void *kbar_op, void *vbar_op,
                     void *workspace, size_t workspace_bytes, fp_stream_t stream);
 
+/* fp_select for one chunk of a chunked prefill (Sec.4.3 "Compatibility with
+ * Chunked Prefill"): the same outputs as fp_select, bit for bit, when kbar,
+ * vbar, kbar_op and vbar_op already hold the means that fp_select (or this
+ * call) wrote for the same request rows and the same keys and values, e.g.
+ * from the previous chunk of the request. The means of every block lying
+ * wholly in a request's cached prefix (blocks J with (J + 1) * 128 <=
+ * L_b^kv - L_b^q) are then kept as they are, since those tokens did not
+ * change; only the blocks holding new tokens are pooled from k_pages and
+ * v_pages, and the kept blocks' rounding statistics (workspace) are derived
+ * from the stored means. Each request's block rows sit at blk_base(b) as for
+ * fp_select, so the rows must hold that request's prefix means at this call's
+ * row positions (for example, a request that stays first in its batch). A
+ * request without a prefix is pooled in full. Arguments are fp_select's. */
+fp_status fp_select_chunk(const fp_problem *p, const void *q, const void *k_pages, const void *v_pages,
+                          float alpha, int32_t sink_blocks, int32_t window_blocks, int32_t *csr_cu, int32_t *csr_idx,
+                          int64_t csr_idx_capacity, float *kbar, float *vbar, void *kbar_op, void *vbar_op,
+                          void *workspace, size_t workspace_bytes, fp_stream_t stream);
+
 /* Stage 2 (Alg.1 steps 6-11). For every segment, walks its selected blocks in
  * descending order (Eq.17) with exact Q'K^T and PV (token-causal mask on the
  * diagonal block), then, with FP_MEAN_CORRECTION, one term per pruned block

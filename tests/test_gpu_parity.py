@@ -445,3 +445,81 @@ def test_kv_splits_are_deterministic():
     w = synth.make_workload("tiny_2k", device="cuda", lengths=[4096], hq=2, hkv=1, mu_scale=0.5, alpha=0.02)
     a, b = run_gpu(w), run_gpu(w)
     assert torch.equal(a.bufs.out, b.bufs.out) and torch.equal(a.bufs.lse, b.bufs.lse)
+
+
+# ---------------------------------------- chunked prefill: the prefix's block means carried between chunks
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_select_chunk_keeps_prefix_means_and_matches_fresh_select(dtype):
+    # one request prefilled in four chunks; fp_select_chunk gets the means arrays the previous chunk left, and
+    # must reproduce a fresh fp_select of the same chunk bit for bit (CSR, means), then the same attention
+    g, hkv = 4, 2
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[3000], hq=g * hkv, hkv=hkv, mu_scale=0.6,
+                            alpha=0.05 if dtype == "bf16" else 0.2, paging="random", dtype=dtype)
+    last = B.Problem.from_workload(w)
+    carried = B.Buffers(last)            # means arrays sized for the whole request, kept across chunks
+    for lo, hi in [(0, 1024), (1024, 1100), (1100, 2333), (2333, 3000)]:
+        c = _chunk(w, lo, hi)
+        p = B.Problem.from_workload(c)
+        fresh = B.Buffers(p)
+        B.fp_select(p, c.q, c.k_pages, c.v_pages, c.alpha, c.sink_blocks, c.window_blocks, fresh.csr_cu,
+                    fresh.csr_idx, fresh.kbar, fresh.vbar, fresh.kbar_op, fresh.vbar_op, fresh.workspace)
+        mine = B.Buffers(p)
+        B.fp_select_chunk(p, c.q, c.k_pages, c.v_pages, c.alpha, c.sink_blocks, c.window_blocks, mine.csr_cu,
+                          mine.csr_idx, carried.kbar, carried.vbar, carried.kbar_op, carried.vbar_op, mine.workspace)
+        assert B.fp_device_status(fresh.workspace) == B.FP_OK and B.fp_device_status(mine.workspace) == B.FP_OK
+        nb = B.fp_num_blocks(p)
+        assert torch.equal(mine.csr_cu, fresh.csr_cu)
+        nnz = int(fresh.csr_cu[-1])
+        assert torch.equal(mine.csr_idx[:nnz], fresh.csr_idx[:nnz])
+        for name in ("kbar", "vbar", "kbar_op", "vbar_op"):
+            assert torch.equal(getattr(carried, name)[:nb].float(), getattr(fresh, name)[:nb].float()), (lo, name)
+        flags = B.FP_MEAN_CORRECTION
+        B.fp_attention(p, c.q, c.k_pages, c.v_pages, fresh.csr_cu, fresh.csr_idx, fresh.kbar_op, fresh.vbar_op,
+                       flags, fresh.out, fresh.lse, fresh.workspace)
+        B.fp_attention(p, c.q, c.k_pages, c.v_pages, mine.csr_cu, mine.csr_idx, carried.kbar_op, carried.vbar_op,
+                       flags, mine.out, mine.lse, mine.workspace)
+        assert torch.equal(mine.out, fresh.out) and torch.equal(mine.lse, fresh.lse)
+    # the chunk's own oracle parity on the last chunk
+    check = check_fp8 if dtype == "e4m3" else check_bf16
+    check(compare(run_gpu(_chunk(w, 2333, 3000))))
+
+
+def test_select_chunk_does_not_read_the_prefix_keys_again():
+    # after the first chunk, overwrite the keys and values of every block wholly in the prefix of the second
+    # chunk: its CSR and means must not change (they come from the carried means), while a fresh fp_select
+    # of the corrupted pool does change
+    g, hkv = 4, 2
+    w = synth.make_workload("tiny_2k", device="cuda", lengths=[2600], hq=g * hkv, hkv=hkv, mu_scale=0.6,
+                            alpha=0.05, paging="random")
+    carried = B.Buffers(B.Problem.from_workload(w))
+    first = _chunk(w, 0, 1536)
+    p1 = B.Problem.from_workload(first)
+    b1 = B.Buffers(p1)
+    B.fp_select_chunk(p1, first.q, first.k_pages, first.v_pages, first.alpha, 1, 1, b1.csr_cu, b1.csr_idx,
+                      carried.kbar, carried.vbar, carried.kbar_op, carried.vbar_op, b1.workspace)
+    second = _chunk(w, 1536, 2600)
+    p2 = B.Problem.from_workload(second)
+    clean = B.Buffers(p2)
+    B.fp_select(p2, second.q, second.k_pages, second.v_pages, second.alpha, 1, 1, clean.csr_cu, clean.csr_idx,
+                clean.kbar, clean.vbar, clean.kbar_op, clean.vbar_op, clean.workspace)
+    # tokens 0 .. 1535 are the 12 complete prefix blocks; overwrite their pages
+    bad = synth.Workload(**{**second.__dict__})
+    bad.k_pages = second.k_pages.clone()
+    bad.v_pages = second.v_pages.clone()
+    prefix_pages = second.page_table[0, :1536 // 64].long()
+    bad.k_pages[prefix_pages] = (bad.k_pages[prefix_pages].float() * -3.0 + 1.0).to(bad.k_pages.dtype)
+    bad.v_pages[prefix_pages] = 0
+    mine = B.Buffers(p2)
+    B.fp_select_chunk(p2, bad.q, bad.k_pages, bad.v_pages, bad.alpha, 1, 1, mine.csr_cu, mine.csr_idx,
+                      carried.kbar, carried.vbar, carried.kbar_op, carried.vbar_op, mine.workspace)
+    assert B.fp_device_status(mine.workspace) == B.FP_OK
+    nb = B.fp_num_blocks(p2)
+    assert torch.equal(mine.csr_cu, clean.csr_cu)
+    nnz = int(clean.csr_cu[-1])
+    assert torch.equal(mine.csr_idx[:nnz], clean.csr_idx[:nnz])
+    assert torch.equal(carried.kbar[:nb], clean.kbar[:nb]) and torch.equal(carried.vbar[:nb], clean.vbar[:nb])
+    changed = B.Buffers(p2)
+    B.fp_select(p2, bad.q, bad.k_pages, bad.v_pages, bad.alpha, 1, 1, changed.csr_cu, changed.csr_idx, changed.kbar,
+                changed.vbar, changed.kbar_op, changed.vbar_op, changed.workspace)
+    assert not torch.equal(changed.kbar[:nb], clean.kbar[:nb])
