@@ -71,6 +71,7 @@ struct SCfg {
 
 // Fixed-size scratch of one reduction set.
 struct RedFixed {
+    float4 dbuf[32];  // the diagonal block's 128 logits: rows r, r + 32, r + 64, r + 96 at [r]
     int32_t list[kRefineList];
     int32_t cand[kCand];  // blocks with a screened log-energy
     float red[2][4];
@@ -478,16 +479,49 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     const float eps = valid ? qmax * (ks.x + 2.44140625e-4f * ks.y) * inv_sqrt_d + 2e-4f : 0.f;
                     const float ms = m * scale;
                     // the first chunk holds the diagonal block (usually the maximum): one block-wide max of the
-                    // lower bounds there gives m_run, a proven lower bound of max_J lE_J for the whole tile
-                    if (cc == 0) m_run = red_max(rs, set, valid ? ms - eps : -INFINITY, 1);
+                    // lower bounds there gives m_run, a proven lower bound of max_J lE_J for the whole tile. The
+                    // diagonal block contributes its screened log-energy less eps, which exceeds its maximum
+                    // logit by up to ln(rows); computed first, by its whole warp (its lane stages the 128 logits
+                    // in shared memory, each lane takes four rows), it leaves few candidates in any chunk.
+                    float lE_diag = 0.f;  // the diagonal block's screened log-energy (its own thread)
+                    if (cc == 0) {
+                        const int dj = D & 127;  // thread of the diagonal block within the set
+                        if ((dj >> 5) == (warp & 3)) {
+                            const int dl = dj & 31;
+                            if (lane == dl) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    rs.dbuf[i] = make_float4(__uint_as_float(v[0][i]), __uint_as_float(v[1][i]),
+                                                             __uint_as_float(v[2][i]), __uint_as_float(v[3][i]));
+                            }
+                            __syncwarp();
+                            // 2^(x k2 - m k2) for rows lane + 32 u; the rounding of m k2 (|logit| 2^-24) lies far
+                            // inside the bound's relative term (2^-12 |q||kbar| >= 2^-12 |logit|)
+                            const float k2 = scale * LOG2E;
+                            const float mk2 = -__shfl_sync(0xffffffffu, m, dl) * k2;
+                            const float4 x = rs.dbuf[lane];
+                            const float xs[4] = {x.x, x.y, x.z, x.w};
+                            float e = 0.f;
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int r = lane + 32 * u;
+                                if (r >= (row_span >> 8) && r < (row_span & 255)) e += ex2(fmaf(xs[u], k2, mk2));
+                            }
+                            e = warp_sum(e);
+                            lE_diag = ms + log2f(e) * LN2;
+                        }
+                        m_run = red_max(rs, set, J == D ? lE_diag - eps : (valid ? ms - eps : -INFINITY), 1);
+                    }
                     if (valid) {
                         eps_tile = fmaxf(eps_tile, eps);
                         const float hi = ms + lnrows + eps;
                         if (hi >= log_alpha + m_run) {
-                            // a candidate: screened log-energy (operand-format kbar, fp32 sums)
+                            // a candidate: screened log-energy (operand-format kbar, fp32 sums); the diagonal
+                            // block's is already known
                             const float k2 = scale * LOG2E;
                             float ps[4] = {0.f, 0.f, 0.f, 0.f};
-                            if (row_span == 128) {
+                            if (J == D) {
+                            } else if (row_span == 128) {
                                 // 2^(v k2 - m k2) with packed FMAs and sums; the rounding of m k2 (|logit| 2^-24)
                                 // lies far inside the bound's relative term (2^-12 |q||kbar| >= 2^-12 |logit|)
                                 const uint64_t k2x2 = f2pack(k2, k2), mk2 = f2pack(-m * k2, -m * k2);
@@ -509,7 +543,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                                     if (x >= (row_span >> 8) && x < (row_span & 255))
                                         ps[x & 3] += ex2((__uint_as_float(v[x >> 5][x & 31]) - m) * k2);
                             }
-                            const float lE = ms + log2f((ps[0] + ps[1]) + (ps[2] + ps[3])) * LN2;
+                            const float lE = J == D ? lE_diag : ms + log2f((ps[0] + ps[1]) + (ps[2] + ps[3])) * LN2;
                             blE[J] = lE;
                             bstate[J] = 0;
                             mlo = fmaxf(mlo, lE - eps);
