@@ -119,6 +119,22 @@ def test_host_rejects_bad_arguments_before_any_device_work():
     assert B.lib.fp_attention(p.ref, fake, fake, fake, fake, odd2, 10, fake, fake, 1, fake, None, fake, need,
                               None) == -1
     assert B.lib.fp_csr_expand64(p.ref, fake, fake, fake, odd2, 10, fake, need, None) == -1
+    # the chunk variant validates like fp_select
+    assert B.lib.fp_select_chunk(p.ref, fake, fake, fake, 0.1, 1, 1, fake, fake, 10 ** 6, fake, fake, fake, fake,
+                                 fake, need - 1, None) == -3
+    assert B.lib.fp_select_chunk(p.ref, fake, fake, fake, -0.5, 1, 1, fake, fake, 10 ** 6, fake, fake, fake, fake,
+                                 fake, need, None) == -1
+    # the traced attention: a trace buffer that is null, misaligned or smaller than its 8-word header
+    assert B.lib.fp_attention_trace(p.ref, fake, fake, fake, fake, fake, 10, fake, fake, 1, fake, None, fake, need,
+                                    None, None, 64) == -1
+    assert B.lib.fp_attention_trace(p.ref, fake, fake, fake, fake, fake, 10, fake, fake, 1, fake, None, fake, need,
+                                    None, odd8, 64) == -1
+    assert B.lib.fp_attention_trace(p.ref, fake, fake, fake, fake, fake, 10, fake, fake, 1, fake, None, fake, need,
+                                    None, fake, 7) == -1
+    # statistics read-back: null workspace or output
+    stats = B.fp_select_stats()
+    assert B.lib.fp_read_select_stats(None, ctypes.byref(stats), None) == -1
+    assert B.lib.fp_read_select_stats(fake, None, None) == -1
     # FP8 without scales
     p8 = problem([256], hq=8, hkv=2, dtype="e4m3", c_q=0.0, c_k=1.0, c_v=1.0)
     assert B.lib.fp_workspace_bytes(p8.ref) == -1

@@ -57,6 +57,9 @@ def test_stress_varlen_parity(g, hkv, page):
     rep = compare(run_gpu(w))
     check_bf16(rep)
     assert rep.density > 0.3
+    # the dense selection leaves blocks the screening bounds cannot settle: the scoring kernel's exact fp32
+    # path runs (and its CSR is still the oracle's)
+    assert rep.exact_tiles > 0
 
 
 def test_dense_mode_matches_oracle_dense():
