@@ -56,8 +56,8 @@ def kernels_per_step(nseg: int) -> int:
 
 # DRAM bytes (read + write) of one attention-kernel launch on this workload, from one stored ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid while the kernel's sources are those the capture ran.
-ATTN_TRAFFIC = {"sources_sha256": "3c53eac609f75a3815468d8bf5ee82cd823f29e3f21e4ebfe6e8709062ab17bc",
-                "bytes": {"qwen30b_128k": 1363542016 + 1025217536, "qwen30b_128k_fp8": 690000384 + 1015759872}}
+ATTN_TRAFFIC = {"sources_sha256": "16cde06dd371df59ba954e253b332cc8060ccb40450582ce1e6d513466601cc0",
+                "bytes": {"qwen30b_128k": 1364675840 + 1029784320, "qwen30b_128k_fp8": 691466496 + 1018871808}}
 
 
 def attn_traffic(workload: str):
