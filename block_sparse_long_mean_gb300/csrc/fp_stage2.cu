@@ -313,11 +313,12 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const Spl
 //   warps 4-11  softmax: each warp owns 16 rows of the tile, each row spread
 //               over two threads (64 consecutive keys each)
 //   warps 12-15 epilogue: O / l to bf16, LSE
-// Exp2 is the softmax's bound (one per score); two warps per scheduler hide
-// its latency, so the softmax of an iteration takes less time than its two
-// MMAs.
+// The softmax of an iteration is its critical chain: its exponentials (one
+// per score, 512 cycles of MUFU for a 128 x 128 tile) run on both softmax
+// warps of a scheduler at once, and the loads, maxima and handoffs around
+// them are latency; together they take longer than the iteration's two MMAs.
 // TMEM: two S buffers (P of an iteration is written over its S), one O
-// buffer and two Q buffers. Each tile's Q is copied from shared memory into
+// buffer and two Q buffers (E4M3: and the 16 columns of its row sums). Each tile's Q is copied from shared memory into
 // TMEM once (tcgen05.cp), so both MMAs take A from TMEM and read only K or V
 // from shared memory: at 128x128x16 per instruction, an MMA reading both
 // operands from shared memory would take all of its bandwidth.
