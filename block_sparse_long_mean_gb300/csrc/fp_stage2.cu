@@ -318,10 +318,10 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const Spl
 // warps of a scheduler at once, and the loads, maxima and handoffs around
 // them are latency; together they take longer than the iteration's two MMAs.
 // TMEM: two S buffers (P of an iteration is written over its S), one O
-// buffer and two Q buffers (E4M3: and the 16 columns of its row sums). Each tile's Q is copied from shared memory into
-// TMEM once (tcgen05.cp), so both MMAs take A from TMEM and read only K or V
-// from shared memory: at 128x128x16 per instruction, an MMA reading both
-// operands from shared memory would take all of its bandwidth.
+// buffer and two Q buffers (E4M3: and the 16 columns of its row sums). Each
+// tile's Q is copied from shared memory into TMEM once (tcgen05.cp), at its
+// first QK^T: that frees the one shared-memory Q buffer, so the next tile's Q
+// loads a whole tile ahead, and both MMAs then take A from TMEM.
 // The iterations of all the CTA's tiles form one stream. MMA group g issues
 // PV(g - 2) then QK^T(g), so the tensor core computes the next scores while
 // the softmax works on these. Every tcgen05 operation of the CTA comes from
