@@ -914,40 +914,59 @@ __global__ void __launch_bounds__(kAThreads, 1)
             if (!mbar_wait(&sm.grp[gi & 3], (gi >> 2) & 1, ab)) break;  // group gi computed S(gi)
             tc_fence_after();
             // v[j]: key 64 half + j of the thread's row; rmax their maximum
-            uint32_t v[64];
-            float rmax;
-            tmem_ld_16x32bx2_x64_max<64>(tS, v, rmax);
-            tmem_ld_wait();
-            reg_fence64(v);
-            asm volatile("" : "+f"(rmax));
             const float shift = J < 0 ? 7.f : 0.f;  // log2 |B_J| of a full 128-token block for means
             const bool plain = J >= 0 ? J != D : (mw.x & mw.y & mw.z & mw.w) == 0xffffffffu;
-            if (!plain) {
-                // masked keys become -inf and the maximum is taken again over the rest
-                float pm[8];
+            uint32_t v[64];
+            float rmax;
+            if (plain) {
+                tmem_ld_16x32bx2_x64_max<64>(tS, v, rmax);
+                tmem_ld_wait();
+                reg_fence64(v);
+                asm volatile("" : "+f"(rmax));
+            } else {
+                // Masked keys become -inf and the maximum is taken over the rest. The thread's 64 keys load as
+                // four groups of 16, each with its maximum: a group whose keys are all kept keeps that maximum,
+                // and only a group the mask cuts through is masked key by key.
+                float gm[4];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+                for (int q = 0; q < 4; ++q) tmem_ld_16x32bx2_x16_max<64>(tS + 16 * q, v + 16 * q, gm[q]);
+                tmem_ld_wait();
+                reg_fence64(v);
+                asm volatile("" : "+f"(gm[0]), "+f"(gm[1]), "+f"(gm[2]), "+f"(gm[3]));
+                // kept keys of the thread's half: bit j of kw[j / 32] for key 64 half + j
+                uint32_t kw0, kw1;
                 if (J >= 0) {
                     // causal mask on the diagonal block: key <= position - 128 J
                     const int lim = ((row0 + row) >> gshift) - J * kBlock - 64 * half;
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        const float x = j <= lim ? __uint_as_float(v[j]) : -INFINITY;
-                        v[j] = __float_as_uint(x);
-                        pm[j & 7] = fmaxf(pm[j & 7], x);
-                    }
+                    kw0 = lim >= 31 ? 0xffffffffu : lim < 0 ? 0u : (2u << lim) - 1u;
+                    kw1 = lim >= 63 ? 0xffffffffu : lim < 32 ? 0u : (2u << (lim - 32)) - 1u;
                 } else {
                     // correction chunk: keep the means of pruned blocks only (bit k & 31 of word k / 32)
-                    const uint32_t w0 = half ? mw.z : mw.x, w1 = half ? mw.w : mw.y;
+                    kw0 = half ? mw.z : mw.x;
+                    kw1 = half ? mw.w : mw.y;
+                }
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        const bool keep = ((j < 32 ? w0 : w1) >> (j & 31)) & 1u;
-                        const float x = keep ? __uint_as_float(v[j]) : -INFINITY;
-                        v[j] = __float_as_uint(x);
-                        pm[j & 7] = fmaxf(pm[j & 7], x);
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t b = ((q < 2 ? kw0 : kw1) >> (16 * (q & 1))) & 0xffffu;
+                    if (b == 0u) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) v[16 * q + i] = __float_as_uint(-INFINITY);
+                        gm[q] = -INFINITY;
+                    } else if (b != 0xffffu) {
+                        float p0 = -INFINITY, p1 = -INFINITY;
+#pragma unroll
+                        for (int i = 0; i < 16; i += 2) {
+                            const float x0 = (b >> i) & 1u ? __uint_as_float(v[16 * q + i]) : -INFINITY;
+                            const float x1 = (b >> (i + 1)) & 1u ? __uint_as_float(v[16 * q + i + 1]) : -INFINITY;
+                            v[16 * q + i] = __float_as_uint(x0);
+                            v[16 * q + i + 1] = __float_as_uint(x1);
+                            p0 = fmaxf(p0, x0);
+                            p1 = fmaxf(p1, x1);
+                        }
+                        gm[q] = fmaxf(p0, p1);
                     }
                 }
-                rmax = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], fmax3(pm[5], pm[6], pm[7])));
+                rmax = fmaxf(fmaxf(gm[0], gm[1]), fmaxf(gm[2], gm[3]));
             }
             rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, 16));
             const float tm = fmaf(rmax, sl2, shift);

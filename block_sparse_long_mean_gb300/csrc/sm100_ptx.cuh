@@ -452,6 +452,15 @@ __device__ __forceinline__ void tmem_ld_16x32bx2_x64_max(uint32_t taddr, uint32_
         : "r"(taddr), "n"(kHalf)
         : "memory");
 }
+// 16 columns per thread (.x16) into r[0..15], with the largest of the 16 values (.red.max).
+template <int kHalf>
+__device__ __forceinline__ void tmem_ld_16x32bx2_x16_max(uint32_t taddr, uint32_t *r, float &mx) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.16x32bx2.x16.max.f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, %16, [%17], %18;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=f"(mx)
+        : "r"(taddr), "n"(kHalf)
+        : "memory");
+}
 // Same without the reduction, and 32-bit columns written back from 64 registers.
 template <int kHalf>
 __device__ __forceinline__ void tmem_ld_16x32bx2_x64(uint32_t taddr, uint32_t (&r)[64]) {
