@@ -56,8 +56,8 @@ def kernels_per_step(nseg: int) -> int:
 
 # DRAM bytes (read + write) of one attention-kernel launch on this workload, from one stored ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid while the kernel's sources are those the capture ran.
-ATTN_TRAFFIC = {"sources_sha256": "e6abb2e317eee3c237c674318591230ed5637b9c6bb474b314eb8833e7b907f8",
-                "bytes": {"qwen30b_128k": 1364675840 + 1029784320, "qwen30b_128k_fp8": 691466496 + 1018871808}}
+ATTN_TRAFFIC = {"sources_sha256": "c99ada5a0ad8c573e2d9171bb46f5456303e5f3b9c427636035e3f8f15c4f02e",
+                "bytes": {"qwen30b_128k": 1365835776 + 1029804800, "qwen30b_128k_fp8": 692387584 + 1018726144}}
 
 
 def attn_traffic(workload: str):
