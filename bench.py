@@ -56,7 +56,7 @@ def kernels_per_step(nseg: int) -> int:
 
 # DRAM bytes (read + write) of one attention-kernel launch on this workload, from one stored ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid while the kernel's sources are those the capture ran.
-ATTN_TRAFFIC = {"sources_sha256": "c99ada5a0ad8c573e2d9171bb46f5456303e5f3b9c427636035e3f8f15c4f02e",
+ATTN_TRAFFIC = {"sources_sha256": "c97d351f211582b7795886202cf33508bbe913a601268ce00faf0d35b54ef214",
                 "bytes": {"qwen30b_128k": 1365835776 + 1029804800, "qwen30b_128k_fp8": 692387584 + 1018726144}}
 
 
