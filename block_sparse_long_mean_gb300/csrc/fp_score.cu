@@ -80,23 +80,24 @@ struct RedFixed {
     int any2[2];  // per tile of the set, alternately: some candidate was left open (read after the tile's last barrier)
 };
 
-// Barriers of the two sets (index [set] or [set][stage / S buffer]).
+// Barriers of the two sets (index [set][Q buffer / stage / S buffer]).
 struct ScoreBars {
-    uint64_t q_full[2], q_empty[2], k_full[2][2], k_empty[2][2], s_full[2][2], s_empty[2][2];
+    uint64_t q_full[2][2], q_empty[2][2], k_full[2][2], k_empty[2][2], s_full[2][2], s_empty[2][2];
     uint32_t tmem_base;
     int abort;
 };
 
-// Shared-memory layout (byte offsets from a 1024-byte aligned base): Q buffer per set, nst chunk stages per
-// set, the barriers, then each set's scratch with per-block arrays for nb blocks (a multiple of 128).
+// Shared-memory layout (byte offsets from a 1024-byte aligned base): nq Q buffers per set, nst chunk stages per
+// set, the barriers, then each set's scratch with per-block arrays for nb blocks (a multiple of 128). With two
+// Q buffers a set loads its next tile's Q while the current tile's MMAs still read the other.
 struct SLayout {
     uint32_t q, k, bars, fixed[2], lE[2], words[2], state[2], total;
 };
-__host__ __device__ inline SLayout score_layout(int tile, int nst, int nb) {
+__host__ __device__ inline SLayout score_layout(int tile, int nq, int nst, int nb) {
     SLayout L;
     uint32_t o = 0;
     L.q = o;
-    o += 2 * tile;
+    o += 2 * nq * tile;
     L.k = o;
     o += 2 * nst * tile;
     L.bars = o;
@@ -209,23 +210,25 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     const float *__restrict__ kbar, const float2 *__restrict__ kstat,
                     const ReqInfo *__restrict__ req, int batch, int hkv, int g, int mode, float log_alpha, int sink,
                     int window, float qscale, float kscale, int32_t nseg, int32_t *__restrict__ seg_count,
-                    uint32_t *__restrict__ mask, const uint8_t *__restrict__ qg, int hq, int nst, int nb,
+                    uint32_t *__restrict__ mask, const uint8_t *__restrict__ qg, int hq, int nq, int nst, int nb,
                     int32_t *__restrict__ status) {
     using C = SCfg<kDtype>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *const base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SLayout L = score_layout(C::kTile, nst, nb);
+    const SLayout L = score_layout(C::kTile, nq, nst, nb);
     ScoreBars &sm = *reinterpret_cast<ScoreBars *>(base + L.bars);
     uint8_t *const qbase = base + L.q, *const kbase = base + L.k;
-    auto qbuf = [=](int set) { return qbase + set * C::kTile; };
+    auto qbuf = [=](int set, int qi) { return qbase + (set * nq + qi) * C::kTile; };
     auto kbuf = [=](int set, int st) { return kbase + (set * nst + st) * C::kTile; };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (status_bad(status)) return;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.q_full[i], 1);
-            mbar_init(&sm.q_empty[i], 2);  // MMA commit + reduction set done with Q
+            for (int qi = 0; qi < 2; ++qi) {
+                mbar_init(&sm.q_full[i][qi], 1);
+                mbar_init(&sm.q_empty[i][qi], 2);  // MMA commit + reduction set done with Q
+            }
             for (int b = 0; b < 2; ++b) {
                 mbar_init(&sm.s_full[i][b], 1);
                 mbar_init(&sm.s_empty[i][b], 4);  // one arrival per warp of the set
@@ -247,8 +250,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     if (warp < 4 && (warp & 1) == 0) {
         sregs_set<kSRegsProducer>();
         // ------------------------------------------------------------ TMA producers of set warp / 2
-        // lane 0: the set's pooled-key chunks; lane 1: its Q tiles, each as soon as the set's previous tile
-        // is done with the Q buffer (its MMAs complete and its reduction past the Q maximum)
+        // lane 0: the set's pooled-key chunks; lane 1: its Q tiles, each as soon as the tile nq before it is done
+        // with that Q buffer (its MMAs complete and its reduction past the Q maximum)
         const int set = warp >> 1;
         if (lane < 2 && scoring) {
             if (lane == 0) {
@@ -259,11 +262,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
             for (int w = blockIdx.x + set * gridDim.x; w < nseg; w += 2 * gridDim.x, ++tile_it) {
                 const SegCoord sc = decode_seg(req, batch, g, nseg - 1 - w);
                 if (lane == 1) {
-                    if (!mbar_wait(&sm.q_empty[set], (tile_it & 1) ^ 1, ab)) break;
-                    mbar_arrive_expect_tx(&sm.q_full[set], C::kTile);
+                    const int qi = tile_it & (nq - 1);
+                    if (!mbar_wait(&sm.q_empty[set][qi], ((tile_it >> (nq - 1)) & 1) ^ 1, ab)) break;
+                    mbar_arrive_expect_tx(&sm.q_full[set][qi], C::kTile);
                     // rows before sc.lo (a chunk's first tile) read other tokens or the zero fill; they are masked
                     for (int i = 0; i < C::kBoxes; ++i)
-                        tma_load_4d(qbuf(set) + i * 16384, &tm_q, &sm.q_full[set], i * C::kBoxElems, 0, sc.h,
+                        tma_load_4d(qbuf(set, qi) + i * 16384, &tm_q, &sm.q_full[set][qi], i * C::kBoxElems, 0, sc.h,
                                     sc.q_pos);
                     continue;
                 }
@@ -295,7 +299,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
             uint32_t tile_it = 0, chunk_it = 0;
             for (int w = blockIdx.x + set * gridDim.x; w < nseg; w += 2 * gridDim.x, ++tile_it) {
                 const SegCoord sc = decode_seg(req, batch, g, nseg - 1 - w);
-                if (!wait_w(&sm.q_full[set], tile_it & 1)) break;
+                const int qi = tile_it & (nq - 1);
+                if (!wait_w(&sm.q_full[set][qi], (tile_it >> (nq - 1)) & 1)) break;
                 const int nch = sc.D / 128 + 1;
                 bool ok = true;
                 for (int cc = 0; cc < nch; ++cc, ++chunk_it) {
@@ -304,7 +309,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                     if (!(ok = wait_w(&sm.s_empty[set][sb], ((chunk_it >> 1) & 1) ^ 1))) break;
                     if (elect_one()) {
                         tc_fence_after();
-                        const uint32_t abase = smem_addr(kbuf(set, st)), bbase = smem_addr(qbuf(set));
+                        const uint32_t abase = smem_addr(kbuf(set, st)), bbase = smem_addr(qbuf(set, qi));
 #pragma unroll
                         for (int k = 0; k < C::kNumK; ++k) {
                             const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                         }
                         umma_commit(&sm.k_empty[set][st]);
                         umma_commit(&sm.s_full[set][sb]);
-                        if (cc == nch - 1) umma_commit(&sm.q_empty[set]);
+                        if (cc == nch - 1) umma_commit(&sm.q_empty[set][qi]);
                     }
                     __syncwarp();
                 }
@@ -376,7 +381,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
             // query rows of the tile: [lo, rows) packed as rows | lo << 8 (128 for a full tile); the packed
             // value, unpacked at each use, keeps the chunk loop within its registers
             const int row_span = sc.rows | (sc.lo << 8);
-            const int qb = set;
+            const int qi = (tile_it >> 1) & (nq - 1);  // the set's Q buffer of this tile (nq is 1 or 2)
             const int nch = D / 128 + 1;
             const float2 *ks_base = kstat + (int64_t)r.blk_base * hkv + sc.h;
             const float lnrows = logf((float)(sc.rows - sc.lo));
@@ -393,7 +398,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
             float mlo = -INFINITY, mhi = -INFINITY;  // this thread's bounds of max_J lE_J
             float m_run = -INFINITY;                 // proven lower bound of max_J lE_J
             if (scoring) {
-                if (!(ok = mbar_wait(&sm.q_full[qb], (tile_it >> 1) & 1, ab))) break;
+                if (!(ok = mbar_wait(&sm.q_full[set][qi], ((tile_it >> 1) >> (nq - 1)) & 1, ab))) break;
                 // a bound of |q_r|_2 over the tile's rows. BF16: sqrt(d) max_i |q_ri|, the largest element
                 // magnitude of this thread's row (an integer maximum over the magnitude bits of the 16-byte chunks
                 // of the swizzled tile). E4M3, whose operand-format means round coarsely and so weigh the bound
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
                         for (int ch = 0; ch < 16; ++ch) {
                             const int atom = ch >> 3, c16 = ch & 7;
-                            const uint4 u = *reinterpret_cast<const uint4 *>(qbuf(qb) + atom * 16384 + j * 128 +
+                            const uint4 u = *reinterpret_cast<const uint4 *>(qbuf(set, qi) + atom * 16384 + j * 128 +
                                                                              ((c16 ^ (j & 7)) << 4));
                             mx = __vmaxu2(mx, __vmaxu2(u.x & 0x7fff7fffu, u.y & 0x7fff7fffu));
                             mx = __vmaxu2(mx, __vmaxu2(u.z & 0x7fff7fffu, u.w & 0x7fff7fffu));
@@ -416,7 +421,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                         uint64_t ss2 = f2pack(0.f, 0.f);
 #pragma unroll
                         for (int ch = 0; ch < 8; ++ch) {
-                            const uint4 u = *reinterpret_cast<const uint4 *>(qbuf(qb) + j * 128 + ((ch ^ (j & 7)) << 4));
+                            const uint4 u = *reinterpret_cast<const uint4 *>(qbuf(set, qi) + j * 128 + ((ch ^ (j & 7)) << 4));
                             const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
@@ -436,7 +441,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                 const float qmax = red_max(rs, set, qbound, 0) * qscale;  // bounds |q_r|_2 (real units), every row
                 // the set is done with the Q tile in shared memory (the rare exact path reads Q from global
                 // memory): once the tile's MMAs are complete too, the next tile's Q may load into the buffer
-                if (rt == 0) mbar_arrive(&sm.q_empty[qb]);
+                if (rt == 0) mbar_arrive(&sm.q_empty[set][qi]);
                 // rounding statistics of this thread's block, loaded one chunk ahead
                 float2 ks_next = (128 * (nch - 1) + j <= D) ? __ldg(ks_base + (int64_t)(128 * (nch - 1) + j) * hkv)
                                                             : make_float2(0.f, 0.f);
@@ -765,9 +770,13 @@ cudaError_t launch_score(const Ctx &c, const void *q, const float *kbar, const v
     cudaGetDevice(&dev);
     if (cudaDeviceGetAttribute(&cap, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || cap <= 0)
         cap = 232448;
-    int nst = 2;
-    if (score_layout(tile, nst, nb).total + 1024 > (uint32_t)cap) nst = 1;
-    const size_t smem = score_layout(tile, nst, nb).total + 1024;
+    // two Q buffers per set (the next tile's Q loads during this tile) only beside two chunk stages: a second
+    // chunk stage is worth more than a second Q buffer (BF16 128K: 0.650 ms with 1 + 2, 0.685 ms with 2 + 1;
+    // E4M3, where 2 + 2 fit: 0.591 -> 0.582 ms)
+    int nq = 2, nst = 2;
+    if (score_layout(tile, nq, nst, nb).total + 1024 > (uint32_t)cap) nq = 1;
+    if (score_layout(tile, nq, nst, nb).total + 1024 > (uint32_t)cap) nst = 1;
+    const size_t smem = score_layout(tile, nq, nst, nb).total + 1024;
     if (smem > (size_t)cap) return cudaErrorInvalidConfiguration;
     cudaError_t e;
     if (fp8) {
@@ -776,14 +785,14 @@ cudaError_t launch_score(const Ctx &c, const void *q, const float *kbar, const v
         if (e != cudaSuccess) return e;
         score_tc_kernel<FP_DTYPE_E4M3><<<grid, kSThreads, smem, c.stream>>>(
             tm_q, tm_k, kbar, c.kstat(), c.req(), c.p.batch, hkv, g, mode, log_alpha, sink, window, c.p.c_q,
-            c.p.c_k, (int32_t)c.s.nseg, c.seg_count(), c.mask(), (const uint8_t *)q, hq, nst, nb, c.status());
+            c.p.c_k, (int32_t)c.s.nseg, c.seg_count(), c.mask(), (const uint8_t *)q, hq, nq, nst, nb, c.status());
     } else {
         e = cudaFuncSetAttribute(score_tc_kernel<FP_DTYPE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
         if (e != cudaSuccess) return e;
         score_tc_kernel<FP_DTYPE_BF16><<<grid, kSThreads, smem, c.stream>>>(
             tm_q, tm_k, kbar, c.kstat(), c.req(), c.p.batch, hkv, g, mode, log_alpha, sink, window, 1.f, 1.f,
-            (int32_t)c.s.nseg, c.seg_count(), c.mask(), (const uint8_t *)q, hq, nst, nb, c.status());
+            (int32_t)c.s.nseg, c.seg_count(), c.mask(), (const uint8_t *)q, hq, nq, nst, nb, c.status());
     }
     return cudaGetLastError();
 }
