@@ -267,7 +267,11 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     w = synth.make_workload(args.workload, device=dev, seed=synth.BASE_SEED + rank)
     p = B.Problem.from_workload(w)
     bufs = B.Buffers(p, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    # every launch and copy goes to a stream of its own (made the current one): the legacy default stream would
+    # order itself against the copy streams of the end-to-end pipeline
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
     flags = B.FP_MEAN_CORRECTION
     # a chunk after a cached prefix: the prefix's block means were pooled by the previous chunk's selection
     # (here: one fp_select before the warm-up) and fp_select_chunk pools only the blocks holding new tokens
@@ -391,10 +395,10 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
     e2e_serial()
     e2e_pipelined(2)
     torch.cuda.synchronize(dev)
-    # the host link is shared with the rest of the machine and has slow periods: each mode is timed three times
-    # and the median reported, with every sample in the line
+    # the host link is shared with the rest of the machine and has slow periods (both modes see them): each mode
+    # is timed five times and the median reported, with every sample in the line
     serial_runs, piped_runs = [], []
-    for _ in range(3):
+    for _ in range(5):
         es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         es.record(stream)
         for _ in range(e2e_steps):
@@ -473,7 +477,7 @@ def run_ours(args, rank: int, world: int, dist_on: bool):
                         how=("pipelined over two device input/output sets: step i's host-to-device copy overlaps "
                              "step i-1's compute and step i-2's device-to-host copy; every step's copies lie in "
                              "the timed region (serial_ms: copy in, compute, copy out, one after the other); "
-                             "each the median of three timed runs of the same steps")),
+                             "each the median of five timed runs of the same steps")),
                gpu_launches=kernels_per_step(acc["segments"]) * args.steps,
                clocks=clk)
     if args.dense_steps > 0:
