@@ -222,6 +222,13 @@ def test_llama8b_32k_sampled_parity():
     check_bf16(compare(run_gpu(w)))
 
 
+def test_384k_request_scoring_with_one_chunk_stage():
+    # one 393,216-token request (3,072 blocks): the scoring kernel's per-block scratch then leaves shared memory
+    # for one pooled-key chunk stage per set instead of two, a launch configuration no other workload reaches
+    w = synth.make_workload("qwen30b_128k", device="cuda", lengths=[393216], hq=8, hkv=1)
+    check_bf16(compare(run_gpu(w), n_random=24))
+
+
 @pytest.mark.parametrize("name", ["qwen30b_128k", "qwen30b_128k_fp8"])
 def test_qwen30b_128k_parity_with_and_without_correction(name):
     # each mode against the oracle of that mode (whole CSR, sampled outputs), then both against exact dense
